@@ -1,0 +1,501 @@
+#!/usr/bin/env python3
+"""DFlash block attention benchmark: K/V HBM GB/s and block-queries/s.
+
+A step is one dflash_block_attn call (argument check, split plan, paged K/V
+staging, QK^T, masked online softmax, PV, split combine) over one layer's
+paged KV cache for the workload below. Steps rotate over `layers` disjoint
+page sets so the bytes touched between two visits of the same layer exceed
+the 129 MB L2 (inputs larger than L2; no flush kernel in the timed region).
+The timed loop replays one CUDA graph per layer (one captured call each):
+the pages report FULL CUDA-graph capture as the way DFlash avoids being
+launch-bound, and a Python/ctypes launch per 10 us kernel would be.
+
+value = algorithmic K/V bytes per step (every visible (token, kv-head) row of
+K and V once, bf16) / device time per step, summed over ranks.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+WORKLOAD = "global_verify"
+WORKLOAD_DESC = ("global-layer verify: batch 1, block_len 9, 32 q heads / 4 KV heads (GQA 8), head_dim 512, "
+                 "context 8192, paged KV page size 16, shuffled page table over a 2x pool, bf16, causal=False")
+METRIC = "kv_hbm_gbs"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=WORKLOAD)
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--splits", type=int, default=-1, help="-1: the workload's own (auto unless fixed)")
+    ap.add_argument("--layers", type=int, default=0, help="page-set rotation count (0 = enough to exceed 4x L2)")
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle time for --impl reference")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- accounting
+
+
+def visible_union_keys(case):
+    """Keys any block query of each request can see (union of the rows' ranges)."""
+    T, W = case.block_len, case.window
+    n = 0
+    for L in case.seq_lens_host():
+        lo = max(0, L - T - W + 1) if W > 0 else 0
+        n += L - lo
+    return n
+
+
+def kv_bytes_per_step(case):
+    return visible_union_keys(case) * case.num_kv_heads * case.head_dim * case.k_cache.element_size() * 2
+
+
+def io_bytes_per_step(case):
+    q = case.q.numel() * case.q.element_size()
+    return 2 * q + case.q.shape[0] * case.q.shape[1] * 4  # q in, out, lse
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed loop runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period_ms), "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)  # let the first samples arrive before the timed region
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        samples = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, smax = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            samples.append((ts, sm, smax, parts))
+        inside = [s for s in samples if t0 <= s[0] <= t1]
+        use = inside if inside else samples
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, _, _, parts in use:
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[1] for s in use), "sm_max_mhz": max(s[2] for s in use),
+                "reasons": sorted(reasons), "samples": len(inside),
+                "samples_note": None if inside else "no sample fell inside the timed region; nearest samples used"}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) legs
+
+
+def host_copy_of_layer(case, layer=0):
+    """Host copy of one layer's inputs with its pages compacted (index work only)."""
+    pt = case.page_tables[layer]
+    used = pt[:, : pt.shape[1]].reshape(-1).unique()
+    remap = torch.full((case.k_cache.shape[0],), -1, dtype=torch.int32, device=pt.device)
+    remap[used.long()] = torch.arange(used.numel(), dtype=torch.int32, device=pt.device)
+    k = case.k_cache[used.long()].cpu()
+    v = case.v_cache[used.long()].cpu()
+    pt2 = remap[pt.long()].cpu()
+    return dict(q=case.q.cpu(), k=k, v=v, pt=pt2, sl=case.seq_lens.cpu())
+
+
+def time_oracle_full(case, budget_s):
+    """Oracle over whole steps (every row, every key) until the budget is used; seconds per step."""
+    import oracle
+
+    h = host_copy_of_layer(case)
+    threads = oracle.default_threads()
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle.block_attn(h["q"], h["k"], h["v"], h["pt"], h["sl"], case.block_len, causal=case.causal,
+                          window=case.window, scale=case.scale, num_threads=threads)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s or len(times) >= 50:
+            break
+    return statistics.median(times), len(times), threads
+
+
+def reference_arm(args, case):
+    """--impl reference: the fp64 oracle on the host cores, each step a key chunk of every row."""
+    import oracle
+
+    h = host_copy_of_layer(case)
+    threads = oracle.default_threads()
+    L = max(case.seq_lens_host())
+    # calibrate one full step, then size the per-step chunk to the budget
+    t0 = time.perf_counter()
+    oracle.block_attn(h["q"], h["k"], h["v"], h["pt"], h["sl"], case.block_len, causal=case.causal,
+                      window=case.window, scale=case.scale, num_threads=threads)
+    t_full = time.perf_counter() - t0
+    n_steps = args.steps + args.warmup
+    frac = min(1.0, args.ref_budget / max(1e-9, n_steps * t_full))
+    chunk = max(case.page_size, int(L * frac) // case.page_size * case.page_size)
+    chunk = min(chunk, L)
+    kb = L - chunk  # the block's own keys and the context just before them
+    for _ in range(args.warmup):
+        oracle.block_attn(h["q"], h["k"], h["v"], h["pt"], h["sl"], case.block_len, causal=case.causal,
+                          window=case.window, scale=case.scale, key_range=(kb, L), num_threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.block_attn(h["q"], h["k"], h["v"], h["pt"], h["sl"], case.block_len, causal=case.causal,
+                          window=case.window, scale=case.scale, key_range=(kb, L), num_threads=threads)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    scale_up = L / chunk  # every row of this workload sees all L keys
+    t_step = dt * scale_up
+    value = kv_bytes_per_step(case) / t_step / 1e9
+    sample = (f"each step: oracle over keys [{kb}, {L}) of all {case.q.shape[0] * case.q.shape[1]} rows "
+              f"({chunk} of {L} keys); time scaled by {scale_up:.2f} to a full step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "block_queries_per_s": case.batch / t_step,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+
+def traffic_from_profiles(kernel_name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None, None
+    try:
+        rec = json.load(open(path)).get(kernel_name)
+    except (ValueError, OSError):
+        return None, None
+    if not rec:
+        return None, None
+    if rec.get("source_sha256") != kernel_source_sha(rec.get("sources", [])):
+        return None, "kernel changed since the ncu capture"
+    return rec.get("dram_bytes_per_launch"), rec.get("note")
+
+
+def kernel_source_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        p = os.path.join(ROOT, f)
+        if not os.path.exists(p):
+            return None
+        h.update(open(p, "rb").read())
+    return h.hexdigest()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return float(d["hbm_gbs"]), "measured"
+        except (ValueError, KeyError, OSError):
+            pass
+    return 6800.0, "fallback"
+
+
+def main():
+    args = parse_args()
+    rank = env_int("RANK", 0)
+    world = env_int("WORLD_SIZE", 1)
+    local = env_int("LOCAL_RANK", 0)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if args.impl == "reference":
+        if rank != 0:
+            if dist:
+                dist.destroy_process_group()
+            return
+        import workloads
+
+        case = workloads.make_case(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
+        reference_arm(args, case)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    import workloads
+    import speculative_decoding_block_dflash_gb300 as dfl
+    from speculative_decoding_block_dflash_gb300 import build as build_mod
+
+    if rank == 0:
+        build_mod.build()
+    if dist:
+        dist.barrier()
+    dfl.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    probe = workloads.make_case(args.config, device=dev, layers=1)
+    per_layer = kv_bytes_per_step(probe)
+    layers = args.layers or max(2, math.ceil(4 * L2_BYTES / max(1, per_layer)))
+    del probe
+    torch.cuda.empty_cache()
+    case = workloads.make_case(args.config, device=dev, layers=layers)
+    splits_req = case.num_splits if args.splits < 0 else args.splits
+    dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
+    splits = dfl.plan_splits(dims, case.block_len, case.window, splits_req, args.kernel)
+    ws = torch.zeros(dfl.workspace_bytes(dims, case.block_len, splits), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(case.q)
+    lse = torch.empty(case.q.shape[:2], dtype=torch.float32, device=dev)
+
+    def call(layer, stream=None):
+        dfl.block_attn(case.q, case.k_cache, case.v_cache, case.page_tables[layer], case.seq_lens,
+                       case.block_len, causal=case.causal, window=case.window, scale=case.scale, out=out,
+                       lse=lse, num_splits=splits, kernel=args.kernel, workspace=ws, stream=stream)
+
+    # one CUDA graph per layer (captured on a side stream after an eager warm-up)
+    side = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(side):
+        for l in range(layers):
+            call(l)
+    torch.cuda.synchronize()
+    graphs = []
+    for l in range(layers):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            call(l)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    assert dfl.read_error(ws) == 0, "device-side check failed during warm-up"
+
+    stream = torch.cuda.current_stream(dev)
+    for k in range(max(3, args.warmup)):
+        graphs[k % layers].replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for k in range(args.steps):
+        graphs[k % layers].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if rank == 0:
+        sampler.stop()
+    ms_total_t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+    if dist:
+        dist.all_reduce(ms_total_t, op=dist.ReduceOp.MAX)
+    ms_per_step = float(ms_total_t.item()) / args.steps
+    kv = kv_bytes_per_step(case)
+    value = world * kv / (ms_per_step * 1e-3) / 1e9
+    bq = world * case.batch / (ms_per_step * 1e-3)
+
+    # eager ctypes path, one call per step, for reference (not the headline)
+    torch.cuda.synchronize()
+    n_eager = min(args.steps, 2000)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(n_eager):
+        call(k % layers)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / n_eager
+
+    # end to end through the public API with host buffers: H2D q/page_table/seq_lens
+    # from pinned memory, the call, D2H of out and lse -- every step
+    q_h = case.q.cpu().pin_memory()
+    pts_h = [pt.cpu().pin_memory() for pt in case.page_tables]
+    sl_h = case.seq_lens.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d = torch.empty_like(case.q)
+    pt_d = torch.empty_like(case.page_tables[0])
+    sl_d = torch.empty_like(case.seq_lens)
+    n_e2e = max(3, min(args.e2e_steps, args.steps))
+
+    def e2e_step(k):
+        q_d.copy_(q_h, non_blocking=True)
+        pt_d.copy_(pts_h[k % layers], non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        dfl.block_attn(q_d, case.k_cache, case.v_cache, pt_d, sl_d, case.block_len, causal=case.causal,
+                       window=case.window, scale=case.scale, out=out, lse=lse, num_splits=splits,
+                       kernel=args.kernel, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for k in range(3):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for k in range(n_e2e):
+        e2e_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms_t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+    if dist:
+        dist.all_reduce(e2e_ms_t, op=dist.ReduceOp.MAX)
+    e2e_ms = float(e2e_ms_t.item())
+    h2d = q_h.numel() * q_h.element_size() + pts_h[0].numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    assert dfl.read_error(ws) == 0, "device-side check failed"
+
+    tc = (args.kernel == "tc") or (args.kernel == "auto" and case.q.dtype == torch.bfloat16 and
+                                   _tc_used(dfl, dims, case, splits_req))
+    kernel_name = "dflash_tc_attn" if tc else "dflash_simt_attn"
+    launches_per_step = 1 if (tc or splits == 1) else 2
+    peak, peak_kind = measured_peaks()
+    traffic, traffic_note = traffic_from_profiles(kernel_name)
+    achieved = kv / (ms_per_step * 1e-3) / 1e9
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    clocks = sampler.summary(t_wall0, t_wall1)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        t_step, n_rep, threads = time_oracle_full(case, args.cpu_budget)
+        cpu = {"value": kv / t_step / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n_rep} full steps of layer 0 (all {case.q.shape[0] * case.q.shape[1]} rows, every "
+                         f"visible key), median {t_step * 1e3:.1f} ms per step"}
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if case.q.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC if args.config == WORKLOAD else args.config,
+                   "global_batch": case.batch * world, "block_len": case.block_len,
+                   "seq_len": max(case.seq_lens_host()), "splits": splits, "kernel": kernel_name,
+                   "l2": f"inputs larger than L2: {layers} rotated page sets x {kv / 1e6:.1f} MB K/V",
+                   "timed_path": "one CUDA-graph replay of one dflash_block_attn call per step",
+                   "parallelism": f"replicas x{world}"},
+        "block_queries_per_s": bq,
+        "query_rows_per_s": bq * case.block_len * case.num_q_heads,
+        "eager_ms_per_step": eager_ms,
+        "e2e": {"value": world * kv / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "public Python API, pinned host q/page_table/seq_lens in, out/lse back, every step; "
+                        "the KV cache is device-resident state"},
+        "gpu_launches": args.steps * launches_per_step,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": kernel_name,
+                     "achieved_basis": "algorithmic K/V bytes per launch / event-timed device time per step",
+                     "traffic_note": traffic_note},
+        "clocks": clocks,
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def _tc_used(dfl, dims, case, splits_req):
+    try:
+        dfl.plan_splits(dims, case.block_len, case.window, max(0, splits_req), "tc")
+        return True
+    except dfl.DflashError:
+        return False
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * dflash_attn.h -- C ABI of libdflash_attn: DFlash block attention on one GPU.
+ *
+ * The operation. In DFlash speculative decoding every request contributes a
+ * block of T = 1 + num_speculative_tokens queries (the bonus token plus the
+ * mask tokens; kenforever1 "dflash-gemma4-31b-notes", section "why non-causal
+ * attention": "num_query_per_req = 1 + num_speculative_tokens"). The block is
+ * processed as a whole: in the draft pass the queries come from the query
+ * embeddings and the context K/V from the target's hidden states; in the
+ * verify pass the block attends to the target's paged KV cache (same page,
+ * code comment "DFlash cross-attention"). Attention is non-causal by default
+ * ("DFlash verify/block attention needs causal=False", same page, PR #52
+ * table) with a causal switch (prhub report on vLLM PR #43445 "Allow causal
+ * DFlash", implementation steps 1-3: causal defaults to False). head_dim goes
+ * up to 512 (Gemma 4 31B global layers, same page, section "Global head_dim
+ * 512"), and sliding-window layers are supported (same page, hybrid attention).
+ *
+ * Definition computed (exact attention, fp32 accumulation on the GPU):
+ *   request b has L_b = seq_lens[b] keys, the block's own T keys being the
+ *   last T of them; block query i sits at position p_i = L_b - T + i.
+ *   Query head h reads KV head g = h / (Hq / Hkv).
+ *   Key j is visible to query i iff lo_i <= j <= hi_i with
+ *     hi_i = causal ? p_i : L_b - 1
+ *     lo_i = window > 0 ? max(0, p_i - window + 1) : 0
+ *   s_j = scale * <q_i, k_j>; out_i = sum_j softmax(s)_j v_j;
+ *   lse_i = log(sum_j exp(s_j))  (natural log).
+ *   Key j of request b is slot j % page_size of page page_table[b][j / page_size].
+ *
+ * Split-KV (flash-decoding style; cf. the FlashAttention "split-KV combine"
+ * of the prhub report on vLLM PR #52816 "DFlash2", review highlights). The
+ * union key range of request b, [lo_b, L_b) with lo_b = window > 0 ?
+ * max(0, L_b - T - window + 1) : 0, is cut into S chunks: base_b =
+ * lo_b rounded down to a multiple of page_size, chunk_b = ceil(ceil((L_b -
+ * base_b) / S) / page_size) * page_size, chunk c = [base_b + c*chunk_b,
+ * base_b + (c+1)*chunk_b) clipped to [lo_b, L_b). Each chunk yields a partial
+ * (o_c, lse_c) over its visible keys (o_c normalised; lse_c = -inf and o_c = 0
+ * when the chunk holds no visible key), and the combine is
+ *   m = max_c lse_c, w_c = exp(lse_c - m), out = sum_c w_c o_c / sum_c w_c,
+ *   lse = m + log(sum_c w_c).
+ *
+ * Conventions for every call:
+ *   - All pointers named "device" are CUDA device pointers owned by the
+ *     caller; the library allocates nothing, never synchronises the stream and
+ *     keeps no state between calls (re-entrant).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid argument returns an error code and launches nothing. The text of
+ *     the last error of the calling thread is available from
+ *     dflash_last_error_message().
+ *   - Values the host cannot see (page ids, seq_lens) are checked on the
+ *     device: an out-of-range page id is never dereferenced (its keys read as
+ *     zero) and a seq_len outside [T, min(max_seq_len, max_pages*page_size)]
+ *     makes the request produce zeros; both set bits in the error word of the
+ *     workspace, read with dflash_read_error(). An unsupported combination
+ *     returns DFLASH_ERR_UNSUPPORTED; the library never falls back to a
+ *     different mask.
+ */
+#ifndef DFLASH_ATTN_H
+#define DFLASH_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#define DFLASH_ABI_VERSION 1
+#define DFLASH_MAX_HEAD_DIM 512
+#define DFLASH_MAX_BLOCK_LEN 64
+#define DFLASH_MAX_SPLITS 256
+
+typedef enum dflash_status {
+    DFLASH_OK = 0,
+    DFLASH_ERR_INVALID_ARG = 1,  /* bad pointer, size, stride, dtype or scalar */
+    DFLASH_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim not a multiple of 16) */
+    DFLASH_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    DFLASH_ERR_DEVICE_CHECK = 4, /* the device saw a bad page id / seq_len (dflash_read_error) */
+    DFLASH_ERR_WORKSPACE = 5     /* workspace missing, misaligned or too small */
+} dflash_status;
+
+typedef enum dflash_dtype {
+    DFLASH_BF16 = 0, /* q, k_cache, v_cache, out in bfloat16 */
+    DFLASH_FP32 = 1  /* q, k_cache, v_cache, out in float32 */
+} dflash_dtype;
+
+/* Which kernel computes the attention. AUTO picks the tensor-core (tcgen05)
+   kernel for bf16 and the fp32 SIMT kernel for fp32. SIMT forces the CUDA-core
+   kernel (any dtype); TC forces the tensor-core kernel (bf16 only; returns
+   DFLASH_ERR_UNSUPPORTED for shapes it does not cover). */
+typedef enum dflash_kernel {
+    DFLASH_KERNEL_AUTO = 0,
+    DFLASH_KERNEL_SIMT = 1,
+    DFLASH_KERNEL_TC = 2
+} dflash_kernel;
+
+/* Device-side error bits accumulated (bitwise OR) in the workspace error word. */
+#define DFLASH_DEVERR_PAGE_ID 1u     /* page_table entry outside [0, num_pages) */
+#define DFLASH_DEVERR_SEQ_LEN 2u     /* seq_lens[b] < T or above the stated bounds */
+#define DFLASH_DEVERR_TIMEOUT 4u     /* a bounded pipeline wait gave up (kernel returned early) */
+
+/* Sizes and layout of one call. All counts are elements, not bytes. */
+typedef struct dflash_dims {
+    int32_t batch;          /* B, requests (>= 1) */
+    int32_t num_q_heads;    /* Hq (>= 1) */
+    int32_t num_kv_heads;   /* Hkv, divides Hq; query head h reads KV head h / (Hq/Hkv) */
+    int32_t head_dim;       /* D, multiple of 16, <= 512 */
+    int32_t page_size;      /* tokens per page, multiple of 8, <= 256 */
+    int32_t num_pages;      /* pages in the K/V pool (first extent of k_cache) */
+    int32_t max_pages;      /* columns of page_table (row stride of page_table) */
+    int32_t max_seq_len;    /* host-known upper bound on every seq_lens[b]; <= max_pages*page_size.
+                               Only used to plan the split count; 0 = max_pages*page_size */
+    dflash_dtype dtype;     /* element type of q, k_cache, v_cache and out */
+    int64_t kv_stride_page; /* k_cache/v_cache element stride between pages */
+    int64_t kv_stride_slot; /* ... between token slots of one page */
+    int64_t kv_stride_head; /* ... between KV heads; head_dim is contiguous (stride 1) */
+} dflash_dims;
+
+/* Per-call options; pass NULL for the defaults (auto splits, auto kernel, no
+   workspace -- only valid when the plan needs none, see dflash_workspace_bytes). */
+typedef struct dflash_opts {
+    int32_t num_splits;     /* 0 = auto (from the SM count and sizes); n >= 1 = exactly n chunks */
+    int32_t kernel;         /* a dflash_kernel value */
+    void* workspace;        /* device memory, 256-byte aligned, dflash_workspace_bytes() long.
+                               Holds the error word and the split partials. Must be zeroed
+                               (e.g. cudaMemset) once before its first use; the library keeps
+                               its counters at zero between calls. */
+    size_t workspace_bytes; /* size of workspace in bytes */
+    void* stream;           /* cudaStream_t; NULL = legacy default stream */
+} dflash_opts;
+
+/*
+ * Block attention for a batch of DFlash blocks over a paged KV cache.
+ *
+ *   q          device, [B*T, Hq, D] contiguous, dims->dtype. Rows b*T .. b*T+T-1
+ *              are request b's block (query i at row b*T+i).
+ *   k_cache    device, element (page, slot, head, d) at
+ *              page*kv_stride_page + slot*kv_stride_slot + head*kv_stride_head + d,
+ *              dims->dtype; 16-byte aligned base, strides multiples of 8 elements.
+ *   v_cache    device, same layout and dtype as k_cache.
+ *   page_table device, int32 [B, max_pages] row-major; entries past
+ *              ceil(L_b/page_size) are never read.
+ *   seq_lens   device, int32 [B]; L_b counts the block's own T keys (L_b >= T).
+ *   block_len  T, 1 <= T <= DFLASH_MAX_BLOCK_LEN.
+ *   causal     0 (default, non-causal: every block query sees every block key)
+ *              or 1 (query i sees keys up to its own position).
+ *   window     0 = global layer; W > 0 = sliding window of W keys ending at each
+ *              query's position. W < T is rejected (a non-causal block must see
+ *              all of its own keys).
+ *   scale      finite and > 0 (usually 1/sqrt(D)).
+ *   out        device, [B*T, Hq, D] contiguous, dims->dtype (written).
+ *   lse        device, float32 [B*T, Hq] (written) or NULL.
+ *   opts       NULL or options above.
+ * Returns DFLASH_OK once the work is enqueued on the stream.
+ */
+DFLASH_API dflash_status dflash_block_attn(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* page_table, const int32_t* seq_lens,
+                                const dflash_dims* dims, int32_t block_len, int32_t causal,
+                                int32_t window, float scale, void* out, float* lse,
+                                const dflash_opts* opts);
+
+/*
+ * Log-sum-exp combine of split partials (the formula in the file header).
+ *
+ *   partial_out  device, float32 [num_splits, num_rows, head_dim] contiguous.
+ *   partial_lse  device, float32 [num_splits, num_rows]; -inf marks an empty chunk.
+ *   num_splits   1 .. DFLASH_MAX_SPLITS; num_rows >= 1; head_dim multiple of 4, <= 512.
+ *   out          device, [num_rows, head_dim] of out_dtype (written); a row whose
+ *                chunks are all empty gets zeros.
+ *   lse          device, float32 [num_rows] (written) or NULL; -inf for all-empty rows.
+ *   stream       cudaStream_t or NULL.
+ */
+DFLASH_API dflash_status dflash_split_combine(const float* partial_out, const float* partial_lse,
+                                   int32_t num_splits, int64_t num_rows, int32_t head_dim,
+                                   dflash_dtype out_dtype, void* out, float* lse, void* stream);
+
+/* Number of chunks dflash_block_attn uses for these sizes when
+   opts->num_splits == requested (0 = auto), or a negative dflash_status code
+   for invalid dims. Host-only arithmetic (no CUDA call except a cached
+   device-attribute query for auto). */
+DFLASH_API int32_t dflash_plan_splits(const dflash_dims* dims, int32_t block_len, int32_t window,
+                           int32_t requested, int32_t kernel);
+
+/* Workspace bytes a call with these sizes and split count needs (split count
+   as returned by dflash_plan_splits). Layout, each part 256-byte aligned: the
+   error word (256 bytes), B*Hq int32 counters, then -- only when splits > 1 --
+   partial lse float32 [splits, B*T, Hq] and partial out float32
+   [splits, B*T, Hq, D]. Returns 0 for invalid dims. */
+DFLASH_API size_t dflash_workspace_bytes(const dflash_dims* dims, int32_t block_len, int32_t num_splits);
+
+/* Copy the workspace error word to *device_error (device->host copy on
+   `stream`, then a stream synchronisation; not for the hot path). With clear
+   != 0 the word is reset to zero afterwards. Returns DFLASH_ERR_DEVICE_CHECK
+   when the word is non-zero, DFLASH_OK when it is zero. */
+DFLASH_API dflash_status dflash_read_error(const void* workspace, void* stream, uint32_t* device_error,
+                                int32_t clear);
+
+/* Static text for a status code. */
+DFLASH_API const char* dflash_status_string(dflash_status status);
+
+/* Detail of the last failing call on the calling thread ("" if none). */
+DFLASH_API const char* dflash_last_error_message(void);
+
+/* DFLASH_ABI_VERSION of the loaded library. */
+DFLASH_API int32_t dflash_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_ATTN_H */

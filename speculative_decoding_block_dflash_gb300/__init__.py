@@ -1,0 +1,27 @@
+"""DFlash block attention for one GB300 (sm_103a).
+
+The compute lives in libdflash_attn.so (CUDA kernels behind the C ABI of
+include/dflash_attn.h); this package is its thin Python binding.
+"""
+from ._binding import (  # noqa: F401
+    BF16,
+    DEVERR_PAGE_ID,
+    DEVERR_SEQ_LEN,
+    DEVERR_TIMEOUT,
+    EXPORTED,
+    FP32,
+    KERNELS,
+    LIB_PATH,
+    DflashError,
+    Dims,
+    Opts,
+    abi_version,
+    block_attn,
+    load_library,
+    make_dims,
+    plan_splits,
+    read_error,
+    split_combine,
+    workspace_bytes,
+    workspace_for,
+)

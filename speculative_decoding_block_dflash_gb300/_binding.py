@@ -1,0 +1,268 @@
+"""ctypes binding of libdflash_attn (argument marshalling only).
+
+Every step of the attention runs in the library's CUDA kernels; this module
+only turns torch tensors into the pointers, sizes and strides that
+include/dflash_attn.h describes, picks the current CUDA stream, and keeps a
+small per-device workspace cache. There is no CPU fallback: if the library is
+missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libdflash_attn.so")
+
+# dflash_status
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_CHECK, ERR_WORKSPACE = range(6)
+# dflash_dtype
+BF16, FP32 = 0, 1
+# dflash_kernel
+KERNELS = {"auto": 0, "simt": 1, "tc": 2}
+# device error bits
+DEVERR_PAGE_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
+
+EXPORTED = (
+    "dflash_block_attn",
+    "dflash_split_combine",
+    "dflash_plan_splits",
+    "dflash_workspace_bytes",
+    "dflash_read_error",
+    "dflash_status_string",
+    "dflash_last_error_message",
+    "dflash_abi_version",
+)
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32),
+        ("max_seq_len", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("kv_stride_page", ctypes.c_int64),
+        ("kv_stride_slot", ctypes.c_int64),
+        ("kv_stride_head", ctypes.c_int64),
+    ]
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [
+        ("num_splits", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+class DflashError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"dflash status {status}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: Optional[str] = None):
+    """Load libdflash_attn.so (built by build.py) and declare its signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with speculative_decoding_block_dflash_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        dims_p, opts_p = ctypes.POINTER(Dims), ctypes.POINTER(Opts)
+        lib.dflash_block_attn.restype = ctypes.c_int
+        lib.dflash_block_attn.argtypes = [vp, vp, vp, vp, vp, dims_p, i32, i32, i32, f32, vp, vp, opts_p]
+        lib.dflash_split_combine.restype = ctypes.c_int
+        lib.dflash_split_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
+        lib.dflash_plan_splits.restype = i32
+        lib.dflash_plan_splits.argtypes = [dims_p, i32, i32, i32, i32]
+        lib.dflash_workspace_bytes.restype = ctypes.c_size_t
+        lib.dflash_workspace_bytes.argtypes = [dims_p, i32, i32]
+        lib.dflash_read_error.restype = ctypes.c_int
+        lib.dflash_read_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32), i32]
+        lib.dflash_status_string.restype = ctypes.c_char_p
+        lib.dflash_status_string.argtypes = [ctypes.c_int]
+        lib.dflash_last_error_message.restype = ctypes.c_char_p
+        lib.dflash_last_error_message.argtypes = []
+        lib.dflash_abi_version.restype = i32
+        lib.dflash_abi_version.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != OK:
+        lib = load_library()
+        msg = lib.dflash_last_error_message().decode() or lib.dflash_status_string(status).decode()
+        raise DflashError(status, msg)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def make_dims(q: torch.Tensor, k_cache: torch.Tensor, page_table: torch.Tensor, block_len: int,
+              max_seq_len: Optional[int] = None, batch: Optional[int] = None) -> Dims:
+    """Dims for q [B*T, Hq, D] and a cache [num_pages, page_size, Hkv, D] (any strides, d contiguous)."""
+    if q.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("q must be [B*T, Hq, D] and k_cache [num_pages, page_size, Hkv, D]")
+    B = batch if batch is not None else page_table.shape[0]
+    d = Dims()
+    d.batch = B
+    d.num_q_heads = q.shape[1]
+    d.num_kv_heads = k_cache.shape[2]
+    d.head_dim = q.shape[2]
+    d.page_size = k_cache.shape[1]
+    d.num_pages = k_cache.shape[0]
+    d.max_pages = page_table.shape[1]
+    d.max_seq_len = int(max_seq_len) if max_seq_len else 0
+    d.dtype = _dtype_code(q)
+    d.kv_stride_page, d.kv_stride_slot, d.kv_stride_head = (int(s) for s in k_cache.stride()[:3])
+    return d
+
+
+def plan_splits(dims: Dims, block_len: int, window: int = 0, requested: int = 0, kernel: str = "auto") -> int:
+    n = load_library().dflash_plan_splits(ctypes.byref(dims), int(block_len), int(window), int(requested),
+                                          KERNELS[kernel])
+    if n < 1:
+        _check(-n)
+    return n
+
+
+def workspace_bytes(dims: Dims, block_len: int, num_splits: int) -> int:
+    n = load_library().dflash_workspace_bytes(ctypes.byref(dims), int(block_len), int(num_splits))
+    if n == 0:
+        raise DflashError(ERR_INVALID_ARG, "invalid dims for workspace size")
+    return n
+
+
+_ws_cache = {}
+
+
+def workspace_for(device: torch.device, nbytes: int) -> torch.Tensor:
+    """A zero-initialised, 256-byte aligned device buffer of at least nbytes, cached per device."""
+    key = (device.type, device.index)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def block_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
+               seq_lens: torch.Tensor, block_len: int, causal: bool = False, window: int = 0,
+               scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+               lse: Optional[torch.Tensor] = None, num_splits: int = 0, kernel: str = "auto",
+               workspace: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
+               stream=None, want_lse: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """DFlash block attention (include/dflash_attn.h, dflash_block_attn).
+
+    q [B*T, Hq, D]; k_cache, v_cache [num_pages, page_size, Hkv, D] (head_dim
+    contiguous); page_table int32 [B, max_pages]; seq_lens int32 [B] on the
+    device. Returns (out [B*T, Hq, D] in q's dtype, lse fp32 [B*T, Hq] or None).
+    """
+    lib = load_library()
+    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
+        raise ValueError("v_cache must match k_cache in shape and strides")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    if page_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("page_table and seq_lens must be int32")
+    dims = make_dims(q, k_cache, page_table, block_len, max_seq_len)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[2])
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
+    splits = plan_splits(dims, block_len, window, num_splits, kernel)
+    need = workspace_bytes(dims, block_len, splits)
+    if workspace is None:
+        workspace = workspace_for(q.device, need)
+    opts = Opts()
+    opts.num_splits = splits
+    opts.kernel = KERNELS[kernel]
+    opts.workspace = workspace.data_ptr()
+    opts.workspace_bytes = workspace.numel() * workspace.element_size()
+    opts.stream = _stream_handle(stream)
+    st = lib.dflash_block_attn(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), page_table.data_ptr(),
+                               seq_lens.data_ptr(), ctypes.byref(dims), int(block_len), int(bool(causal)),
+                               int(window), float(scale), out.data_ptr(),
+                               lse.data_ptr() if lse is not None else None, ctypes.byref(opts))
+    _check(st)
+    return out, lse
+
+
+def split_combine(partial_out: torch.Tensor, partial_lse: torch.Tensor, out_dtype=torch.float32,
+                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Log-sum-exp combine (dflash_split_combine): partial_out fp32 [S, rows..., D],
+    partial_lse fp32 [S, rows...] -> out [rows..., D] (out_dtype), lse [rows...]."""
+    lib = load_library()
+    if partial_out.dtype != torch.float32 or partial_lse.dtype != torch.float32:
+        raise TypeError("partials must be fp32")
+    if not (partial_out.is_contiguous() and partial_lse.is_contiguous()):
+        raise ValueError("partials must be contiguous")
+    S, D = partial_out.shape[0], partial_out.shape[-1]
+    inner = tuple(partial_out.shape[1:-1])
+    rows = int(math.prod(inner)) if inner else 1
+    if out is None:
+        out = torch.empty(inner + (D,), dtype=out_dtype, device=partial_out.device)
+    if lse is None:
+        lse = torch.empty(inner, dtype=torch.float32, device=partial_out.device)
+    st = lib.dflash_split_combine(partial_out.data_ptr(), partial_lse.data_ptr(), S, rows, D,
+                                  _dtype_code(out), out.data_ptr(), lse.data_ptr(), _stream_handle(stream))
+    _check(st)
+    return out, lse
+
+
+def read_error(workspace: Optional[torch.Tensor] = None, clear: bool = True, stream=None) -> int:
+    """The workspace's device error word (DEVERR_* bits); synchronises the stream."""
+    lib = load_library()
+    if workspace is None:
+        if not torch.cuda.is_available():
+            return 0
+        workspace = _ws_cache.get(("cuda", torch.cuda.current_device()))
+        if workspace is None:
+            return 0
+    word = ctypes.c_uint32(0)
+    st = lib.dflash_read_error(workspace.data_ptr(), _stream_handle(stream), ctypes.byref(word), int(bool(clear)))
+    if st not in (OK, ERR_DEVICE_CHECK):
+        _check(st)
+    return int(word.value)
+
+
+def abi_version() -> int:
+    return int(load_library().dflash_abi_version())

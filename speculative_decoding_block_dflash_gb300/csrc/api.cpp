@@ -1,0 +1,354 @@
+// C-ABI front end of libdflash_attn: host-side validation, split planning,
+// workspace carve-up and kernel launches. See include/dflash_attn.h for the
+// contract of each entry point.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "dflash_internal.h"
+
+namespace dflash {
+namespace {
+
+thread_local std::string g_last_error;
+
+dflash_status fail(dflash_status s, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+dflash_status cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(DFLASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t elem_size(int32_t dtype) { return dtype == DFLASH_BF16 ? 2 : 4; }
+
+// Validation of the sizes and layout (no pointers).
+dflash_status check_dims(const dflash_dims* d, int32_t T)
+{
+    if (!d) return fail(DFLASH_ERR_INVALID_ARG, "dims is NULL");
+    if (d->batch < 1 || d->batch > 65535) return fail(DFLASH_ERR_INVALID_ARG, "batch %d outside [1, 65535]", d->batch);
+    if (d->num_q_heads < 1 || d->num_kv_heads < 1)
+        return fail(DFLASH_ERR_INVALID_ARG, "head counts must be >= 1 (Hq=%d, Hkv=%d)", d->num_q_heads,
+                    d->num_kv_heads);
+    if (d->num_q_heads % d->num_kv_heads != 0)
+        return fail(DFLASH_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                    d->num_q_heads, d->num_kv_heads);
+    if (d->num_q_heads > 1024) return fail(DFLASH_ERR_INVALID_ARG, "num_q_heads %d > 1024", d->num_q_heads);
+    if (d->head_dim < 1 || d->head_dim > DFLASH_MAX_HEAD_DIM)
+        return fail(DFLASH_ERR_INVALID_ARG, "head_dim %d outside [1, %d]", d->head_dim, DFLASH_MAX_HEAD_DIM);
+    if (d->head_dim % 16 != 0)
+        return fail(DFLASH_ERR_UNSUPPORTED, "head_dim %d is not a multiple of 16", d->head_dim);
+    if (d->page_size < 8 || d->page_size > 256 || d->page_size % 8 != 0)
+        return fail(DFLASH_ERR_INVALID_ARG, "page_size %d must be a multiple of 8 in [8, 256]", d->page_size);
+    if (d->num_pages < 1) return fail(DFLASH_ERR_INVALID_ARG, "num_pages %d < 1", d->num_pages);
+    if (d->max_pages < 1) return fail(DFLASH_ERR_INVALID_ARG, "max_pages %d < 1", d->max_pages);
+    const int64_t cap = (int64_t)d->max_pages * d->page_size;
+    if (cap > (int64_t)(1 << 30)) return fail(DFLASH_ERR_INVALID_ARG, "max_pages*page_size too large");
+    if (d->max_seq_len < 0 || d->max_seq_len > cap)
+        return fail(DFLASH_ERR_INVALID_ARG, "max_seq_len %d outside [0, max_pages*page_size=%lld]", d->max_seq_len,
+                    (long long)cap);
+    if (d->dtype != DFLASH_BF16 && d->dtype != DFLASH_FP32)
+        return fail(DFLASH_ERR_INVALID_ARG, "dtype %d is not DFLASH_BF16 or DFLASH_FP32", (int)d->dtype);
+    if (T < 1 || T > DFLASH_MAX_BLOCK_LEN)
+        return fail(DFLASH_ERR_INVALID_ARG, "block_len %d outside [1, %d]", T, DFLASH_MAX_BLOCK_LEN);
+    const int32_t maxL = d->max_seq_len ? d->max_seq_len : (int32_t)cap;
+    if (maxL < T) return fail(DFLASH_ERR_INVALID_ARG, "max_seq_len %d < block_len %d", maxL, T);
+    const int64_t es = (int64_t)elem_size(d->dtype);
+    if (d->kv_stride_page < 0 || d->kv_stride_slot < 0 || d->kv_stride_head < 0)
+        return fail(DFLASH_ERR_INVALID_ARG, "negative K/V stride");
+    if ((d->kv_stride_page * es) % 16 || (d->kv_stride_slot * es) % 16 || (d->kv_stride_head * es) % 16)
+        return fail(DFLASH_ERR_INVALID_ARG, "K/V strides must be multiples of 16 bytes");
+    if (d->kv_stride_head < d->head_dim && d->num_kv_heads > 1)
+        return fail(DFLASH_ERR_INVALID_ARG, "kv_stride_head %lld < head_dim %d", (long long)d->kv_stride_head,
+                    d->head_dim);
+    return DFLASH_OK;
+}
+
+int32_t max_len_of(const dflash_dims* d)
+{
+    return d->max_seq_len ? d->max_seq_len : d->max_pages * d->page_size;
+}
+
+std::mutex g_sm_mutex;
+int g_sm_count[64] = {0};
+
+}  // namespace
+
+int device_sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev >= 0 && dev < 64) {
+        std::lock_guard<std::mutex> lk(g_sm_mutex);
+        if (g_sm_count[dev] == 0) {
+            int n = 0;
+            if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+            g_sm_count[dev] = n;
+        }
+        return g_sm_count[dev];
+    }
+    return 148;
+}
+
+WorkspaceLayout workspace_layout(int32_t B, int32_t T, int32_t Hq, int32_t D, int32_t splits)
+{
+    WorkspaceLayout w;
+    w.err_off = 0;
+    w.counters_off = 256;
+    size_t off = w.counters_off + round_up(sizeof(int32_t) * (size_t)B * Hq, 256);
+    w.part_lse_off = off;
+    w.part_out_off = off;
+    if (splits > 1) {
+        const size_t rows = (size_t)B * T * Hq;
+        w.part_lse_off = off;
+        off += round_up(sizeof(float) * rows * splits, 256);
+        w.part_out_off = off;
+        off += round_up(sizeof(float) * rows * (size_t)splits * D, 256);
+    }
+    w.total = off;
+    return w;
+}
+
+}  // namespace dflash
+
+using namespace dflash;
+
+namespace {
+
+// Kernel the call will use: 1 = SIMT, 2 = tensor-core, or a negative status.
+int choose_kernel(const dflash_dims* d, int32_t T, int32_t window, int32_t requested)
+{
+    AttnParams p{};
+    p.B = d->batch;
+    p.T = T;
+    p.Hq = d->num_q_heads;
+    p.Hkv = d->num_kv_heads;
+    p.G = d->num_q_heads / d->num_kv_heads;
+    p.D = d->head_dim;
+    p.page_size = d->page_size;
+    p.window = window;
+    p.dtype = d->dtype;
+    p.sp = d->kv_stride_page;
+    p.ss = d->kv_stride_slot;
+    p.sh = d->kv_stride_head;
+    p.num_pages = d->num_pages;
+    if (requested == DFLASH_KERNEL_SIMT) return DFLASH_KERNEL_SIMT;
+    if (requested == DFLASH_KERNEL_TC) {
+        if (d->dtype != DFLASH_BF16 || !tc_supports(p)) return -DFLASH_ERR_UNSUPPORTED;
+        return DFLASH_KERNEL_TC;
+    }
+    if (requested != DFLASH_KERNEL_AUTO) return -DFLASH_ERR_INVALID_ARG;
+    if (d->dtype == DFLASH_BF16 && tc_supports(p)) return DFLASH_KERNEL_TC;
+    return DFLASH_KERNEL_SIMT;
+}
+
+// Work units (CTAs per split) of the chosen kernel.
+int64_t work_units(const dflash_dims* d, int32_t T, int kernel)
+{
+    if (kernel == DFLASH_KERNEL_TC) {
+        const int R = (d->num_q_heads / d->num_kv_heads) * T;
+        const int per_cta = 64;  // packed rows per tensor-core CTA, see tc_attn.cu
+        return (int64_t)d->batch * d->num_kv_heads * ((R + per_cta - 1) / per_cta);
+    }
+    return (int64_t)d->batch * d->num_q_heads * ((T + 15) / 16);
+}
+
+int32_t plan_splits_impl(const dflash_dims* d, int32_t T, int32_t window, int32_t requested, int kernel)
+{
+    if (requested > 0) return requested > DFLASH_MAX_SPLITS ? -DFLASH_ERR_INVALID_ARG : requested;
+    if (requested < 0) return -DFLASH_ERR_INVALID_ARG;
+    // Longest union key range any request can have.
+    int64_t span = max_len_of(d);
+    if (window > 0) span = std::min<int64_t>(span, (int64_t)window + T - 1 + d->page_size);
+    // Keep at least 256 keys per chunk; aim for one wave over the SMs.
+    const int64_t max_by_len = std::max<int64_t>(1, span / 256);
+    const int64_t units = work_units(d, T, kernel);
+    const int64_t sms = device_sm_count();
+    int64_t s = (sms + units - 1) / units;
+    s = std::min<int64_t>(s, max_by_len);
+    s = std::min<int64_t>(s, DFLASH_MAX_SPLITS);
+    return (int32_t)std::max<int64_t>(1, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dflash_abi_version(void) { return DFLASH_ABI_VERSION; }
+
+const char* dflash_status_string(dflash_status s)
+{
+    switch (s) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_ERR_INVALID_ARG: return "invalid argument";
+    case DFLASH_ERR_UNSUPPORTED: return "unsupported combination";
+    case DFLASH_ERR_CUDA: return "CUDA error";
+    case DFLASH_ERR_DEVICE_CHECK: return "device-side check failed (bad page id or seq_len)";
+    case DFLASH_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+const char* dflash_last_error_message(void) { return g_last_error.c_str(); }
+
+int32_t dflash_plan_splits(const dflash_dims* dims, int32_t block_len, int32_t window, int32_t requested,
+                           int32_t kernel)
+{
+    const dflash_status s = check_dims(dims, block_len);
+    if (s != DFLASH_OK) return -(int32_t)s;
+    const int k = choose_kernel(dims, block_len, window, kernel);
+    if (k < 0) return k;
+    return plan_splits_impl(dims, block_len, window, requested, k);
+}
+
+size_t dflash_workspace_bytes(const dflash_dims* dims, int32_t block_len, int32_t num_splits)
+{
+    if (check_dims(dims, block_len) != DFLASH_OK || num_splits < 1 || num_splits > DFLASH_MAX_SPLITS) return 0;
+    return workspace_layout(dims->batch, block_len, dims->num_q_heads, dims->head_dim, num_splits).total;
+}
+
+dflash_status dflash_block_attn(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* page_table, const int32_t* seq_lens, const dflash_dims* dims,
+                                int32_t block_len, int32_t causal, int32_t window, float scale, void* out,
+                                float* lse, const dflash_opts* opts)
+{
+    g_last_error.clear();
+    dflash_status s = check_dims(dims, block_len);
+    if (s != DFLASH_OK) return s;
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !out)
+        return fail(DFLASH_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+        return fail(DFLASH_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
+    if (!aligned(page_table, 4) || !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)))
+        return fail(DFLASH_ERR_INVALID_ARG, "page_table, seq_lens and lse must be 4-byte aligned");
+    if (causal != 0 && causal != 1) return fail(DFLASH_ERR_INVALID_ARG, "causal must be 0 or 1 (got %d)", causal);
+    if (window < 0) return fail(DFLASH_ERR_INVALID_ARG, "window %d < 0", window);
+    if (window > 0 && window < block_len)
+        return fail(DFLASH_ERR_INVALID_ARG, "window %d < block_len %d: the block would not see its own keys", window,
+                    block_len);
+    if (!std::isfinite(scale) || !(scale > 0.f))
+        return fail(DFLASH_ERR_INVALID_ARG, "scale must be finite and > 0");
+
+    const int32_t requested = opts ? opts->num_splits : 0;
+    const int32_t kreq = opts ? opts->kernel : DFLASH_KERNEL_AUTO;
+    const int kernel = choose_kernel(dims, block_len, window, kreq);
+    if (kernel < 0)
+        return fail((dflash_status)(-kernel), kernel == -DFLASH_ERR_UNSUPPORTED
+                                                  ? "the tensor-core kernel does not cover these sizes/dtype"
+                                                  : "unknown kernel selector %d",
+                    kreq);
+    const int32_t splits = plan_splits_impl(dims, block_len, window, requested, kernel);
+    if (splits < 1) return fail(DFLASH_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", requested, DFLASH_MAX_SPLITS);
+
+    const WorkspaceLayout wl = workspace_layout(dims->batch, block_len, dims->num_q_heads, dims->head_dim, splits);
+    void* ws = opts ? opts->workspace : nullptr;
+    const size_t ws_bytes = opts ? opts->workspace_bytes : 0;
+    if (ws) {
+        if (!aligned(ws, 256)) return fail(DFLASH_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+        if (ws_bytes < wl.total)
+            return fail(DFLASH_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed for %d splits", ws_bytes, wl.total,
+                        splits);
+    } else if (splits > 1) {
+        return fail(DFLASH_ERR_WORKSPACE, "%d splits need a workspace of %zu bytes", splits, wl.total);
+    }
+
+    AttnParams p{};
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.lse = lse;
+    char* wsb = static_cast<char*>(ws);
+    p.err = ws ? reinterpret_cast<uint32_t*>(wsb + wl.err_off) : nullptr;
+    p.counters = ws ? reinterpret_cast<int32_t*>(wsb + wl.counters_off) : nullptr;
+    p.part_lse = splits > 1 ? reinterpret_cast<float*>(wsb + wl.part_lse_off) : nullptr;
+    p.part_out = splits > 1 ? reinterpret_cast<float*>(wsb + wl.part_out_off) : nullptr;
+    p.B = dims->batch;
+    p.T = block_len;
+    p.Hq = dims->num_q_heads;
+    p.Hkv = dims->num_kv_heads;
+    p.G = dims->num_q_heads / dims->num_kv_heads;
+    p.D = dims->head_dim;
+    p.page_size = dims->page_size;
+    p.num_pages = dims->num_pages;
+    p.max_pages = dims->max_pages;
+    p.max_seq_len = max_len_of(dims);
+    p.sp = dims->kv_stride_page;
+    p.ss = dims->kv_stride_slot;
+    p.sh = dims->kv_stride_head;
+    p.causal = causal;
+    p.window = window;
+    p.scale = scale;
+    p.splits = splits;
+    p.dtype = dims->dtype;
+
+    cudaStream_t stream = opts ? static_cast<cudaStream_t>(opts->stream) : nullptr;
+    cudaError_t e = (kernel == DFLASH_KERNEL_TC) ? launch_tc_attn(p, stream) : launch_simt_attn(p, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+    if (splits > 1 && kernel != DFLASH_KERNEL_TC) {
+        e = launch_combine(p.part_out, p.part_lse, splits, (int64_t)p.B * p.T * p.Hq, p.D, p.dtype, out, lse, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    }
+    return DFLASH_OK;
+}
+
+dflash_status dflash_split_combine(const float* partial_out, const float* partial_lse, int32_t num_splits,
+                                   int64_t num_rows, int32_t head_dim, dflash_dtype out_dtype, void* out, float* lse,
+                                   void* stream)
+{
+    g_last_error.clear();
+    if (!partial_out || !partial_lse || !out) return fail(DFLASH_ERR_INVALID_ARG, "NULL pointer");
+    if (num_splits < 1 || num_splits > DFLASH_MAX_SPLITS)
+        return fail(DFLASH_ERR_INVALID_ARG, "num_splits %d outside [1, %d]", num_splits, DFLASH_MAX_SPLITS);
+    if (num_rows < 1 || num_rows > 0x7fffffffLL)
+        return fail(DFLASH_ERR_INVALID_ARG, "num_rows %lld outside [1, 2^31-1]", (long long)num_rows);
+    if (head_dim < 4 || head_dim > DFLASH_MAX_HEAD_DIM || head_dim % 4 != 0)
+        return fail(DFLASH_ERR_INVALID_ARG, "head_dim %d must be a multiple of 4 in [4, 512]", head_dim);
+    if (out_dtype != DFLASH_BF16 && out_dtype != DFLASH_FP32)
+        return fail(DFLASH_ERR_INVALID_ARG, "out_dtype %d invalid", (int)out_dtype);
+    if (!aligned(partial_out, 16) || !aligned(partial_lse, 4) || !aligned(out, 8) || (lse && !aligned(lse, 4)))
+        return fail(DFLASH_ERR_INVALID_ARG, "misaligned pointer");
+    cudaError_t e = launch_combine(partial_out, partial_lse, num_splits, num_rows, head_dim, out_dtype, out, lse,
+                                   static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    return DFLASH_OK;
+}
+
+dflash_status dflash_read_error(const void* workspace, void* stream, uint32_t* device_error, int32_t clear)
+{
+    g_last_error.clear();
+    if (!workspace || !device_error) return fail(DFLASH_ERR_INVALID_ARG, "NULL pointer");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the error word");
+    if (clear && word) {
+        e = cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(word), st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+    }
+    *device_error = word;
+    return word ? DFLASH_ERR_DEVICE_CHECK : DFLASH_OK;
+}
+
+}  // extern "C"

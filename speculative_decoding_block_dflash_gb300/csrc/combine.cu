@@ -1,0 +1,101 @@
+// Log-sum-exp combine of split-KV partials (flash-decoding style; the
+// "split-KV combine" step named in the prhub report on vLLM PR #52816
+// "DFlash2", review highlights):
+//   m = max_c lse_c, w_c = exp(lse_c - m), out = sum_c w_c o_c / sum_c w_c,
+//   lse = m + log(sum_c w_c); chunks with lse_c = -inf weigh nothing.
+//
+// One CTA per output row (query row x head); 128 threads, each owning four
+// consecutive head-dim elements (float4 loads, D <= 512). The chunk weights
+// are computed once per CTA into shared memory.
+#include <cmath>
+
+#include "dflash_device.cuh"
+
+namespace dflash {
+namespace {
+
+constexpr int kThreads = 128;
+
+__global__ void __launch_bounds__(kThreads)
+    combine_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse, int32_t S,
+                   int64_t rows, int32_t D, int32_t out_dtype, void* __restrict__ out,
+                   float* __restrict__ lse)
+{
+    __shared__ float w_s[DFLASH_MAX_SPLITS];
+    __shared__ float red[kThreads / 32];
+    __shared__ float m_sh, inv_sh, lse_sh;
+    const int64_t row = blockIdx.x;
+    const int tid = threadIdx.x;
+
+    // max over chunks
+    float m = -INFINITY;
+    for (int c = tid; c < S; c += kThreads) m = fmaxf(m, part_lse[(int64_t)c * rows + row]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((tid & 31) == 0) red[tid >> 5] = m;
+    __syncthreads();
+    if (tid == 0) {
+        float mm = red[0];
+        for (int w = 1; w < kThreads / 32; ++w) mm = fmaxf(mm, red[w]);
+        m_sh = mm;
+    }
+    __syncthreads();
+    m = m_sh;
+
+    float ws = 0.f;
+    for (int c = tid; c < S; c += kThreads) {
+        const float l = part_lse[(int64_t)c * rows + row];
+        const float w = (l == -INFINITY) ? 0.f : expf(l - m);
+        w_s[c] = w;
+        ws += w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+    __syncthreads();
+    if ((tid & 31) == 0) red[tid >> 5] = ws;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < kThreads / 32; ++w) t += red[w];
+        const bool empty = (m == -INFINITY) || !(t > 0.f);
+        inv_sh = empty ? 0.f : 1.f / t;
+        lse_sh = empty ? -INFINITY : m + logf(t);
+    }
+    __syncthreads();
+    const float inv = inv_sh;
+
+    const int d0 = tid * 4;
+    if (d0 < D) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (inv > 0.f) {
+            for (int c = 0; c < S; ++c) {
+                const float w = w_s[c];
+                if (w == 0.f) continue;
+                const float4 v = *reinterpret_cast<const float4*>(part_out + ((int64_t)c * rows + row) * D + d0);
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+            }
+        }
+        const int64_t o = row * D + d0;
+        store_elem(out, o + 0, acc.x * inv, out_dtype);
+        store_elem(out, o + 1, acc.y * inv, out_dtype);
+        store_elem(out, o + 2, acc.z * inv, out_dtype);
+        store_elem(out, o + 3, acc.w * inv, out_dtype);
+    }
+    if (tid == 0 && lse) lse[row] = lse_sh;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* part_out, const float* part_lse, int32_t splits, int64_t rows,
+                           int32_t D, int32_t out_dtype, void* out, float* lse, cudaStream_t stream)
+{
+    if (rows <= 0) return cudaSuccess;
+    combine_kernel<<<dim3((unsigned)rows), kThreads, 0, stream>>>(part_out, part_lse, splits, rows, D,
+                                                                  out_dtype, out, lse);
+    return cudaGetLastError();
+}
+
+}  // namespace dflash

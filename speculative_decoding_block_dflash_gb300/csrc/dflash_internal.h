@@ -1,0 +1,55 @@
+// Internal interface between the C-ABI front end (api.cpp) and the kernels.
+// Not installed; not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "dflash_attn.h"
+
+namespace dflash {
+
+// Everything a kernel needs for one dflash_block_attn call. Validated on the host.
+struct AttnParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    void* out;            // [B*T, Hq, D] dtype (nullptr when only partials are produced)
+    float* lse;           // [B*T, Hq] or nullptr
+    float* part_out;      // [S, B*T, Hq, D] when S > 1
+    float* part_lse;      // [S, B*T, Hq]    when S > 1
+    uint32_t* err;        // device error word or nullptr
+    int32_t* counters;    // [B*Hq] zero-initialised counters or nullptr
+    int32_t B, T, Hq, Hkv, G, D;
+    int32_t page_size, num_pages, max_pages, max_seq_len;
+    int64_t sp, ss, sh;   // K/V element strides: page, slot, head
+    int32_t causal, window;
+    float scale;
+    int32_t splits;
+    int32_t dtype;        // dflash_dtype
+};
+
+// Workspace carve-up (offsets in bytes from the workspace base).
+struct WorkspaceLayout {
+    size_t err_off, counters_off, part_lse_off, part_out_off, total;
+};
+WorkspaceLayout workspace_layout(int32_t B, int32_t T, int32_t Hq, int32_t D, int32_t splits);
+
+// Kernel launchers (return cudaSuccess or the launch error).
+cudaError_t launch_simt_attn(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_combine(const float* part_out, const float* part_lse, int32_t splits,
+                           int64_t rows, int32_t D, int32_t out_dtype, void* out, float* lse,
+                           cudaStream_t stream);
+
+// Tensor-core kernel: whether it covers these sizes, and its launcher.
+bool tc_supports(const AttnParams& p);
+cudaError_t launch_tc_attn(const AttnParams& p, cudaStream_t stream);
+
+// SM count of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace dflash

@@ -1,0 +1,209 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry
+point, and rejects bad arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import speculative_decoding_block_dflash_gb300 as dfl
+from speculative_decoding_block_dflash_gb300 import _binding as B
+from speculative_decoding_block_dflash_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dflash_attn.h")
+
+# Fake device addresses are only ever used in calls that must fail host-side
+# validation; on a machine with a GPU these tests are skipped so that a
+# validation slip can never hand such an address to a kernel.
+cpu_only = pytest.mark.skipif(torch.cuda.is_available(), reason="fake-pointer validation runs on CPU-only hosts")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return dfl.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"DFLASH_API\s+[\w\s\*]+?\b(dflash_\w+)\s*\(", text)
+
+
+def test_header_declares_the_binding_surface():
+    names = declared_functions()
+    assert sorted(names) == sorted(B.EXPORTED)
+    assert "dflash_block_attn" in names and "dflash_split_combine" in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # nothing but the C ABI is exported
+    out = os.popen(f"nm -D --defined-only {B.LIB_PATH}").read()
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert exported == set(declared_functions())
+
+
+def test_abi_version_matches_header(lib):
+    m = re.search(r"#define DFLASH_ABI_VERSION (\d+)", open(HEADER).read())
+    assert lib.dflash_abi_version() == int(m.group(1))
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.dflash_status_string(s).decode()
+    assert lib.dflash_status_string(99).decode() == "unknown status"
+
+
+def good_dims(**kw):
+    d = B.Dims()
+    vals = dict(batch=2, num_q_heads=32, num_kv_heads=4, head_dim=512, page_size=16, num_pages=1024,
+                max_pages=512, max_seq_len=0, dtype=B.BF16)
+    vals.update(kw)
+    for k, v in vals.items():
+        setattr(d, k, v)
+    d.kv_stride_head = kw.get("kv_stride_head", d.head_dim)
+    d.kv_stride_slot = kw.get("kv_stride_slot", d.num_kv_heads * d.head_dim)
+    d.kv_stride_page = kw.get("kv_stride_page", d.page_size * d.num_kv_heads * d.head_dim)
+    return d
+
+
+def test_workspace_layout(lib):
+    d = good_dims()
+    T = 9
+    n1 = lib.dflash_workspace_bytes(ctypes.byref(d), T, 1)
+    assert n1 == 256 + 256  # error word + 2*32 int32 counters (rounded)
+    S = 16
+    rows = 2 * T * 32
+    n = lib.dflash_workspace_bytes(ctypes.byref(d), T, S)
+    rnd = lambda x: (x + 255) // 256 * 256
+    assert n == 512 + rnd(4 * rows * S) + rnd(4 * rows * S * 512)
+    assert lib.dflash_workspace_bytes(ctypes.byref(d), T, 0) == 0
+    assert lib.dflash_workspace_bytes(ctypes.byref(good_dims(head_dim=520)), T, 1) == 0
+
+
+def test_plan_splits_explicit_and_invalid(lib):
+    d = good_dims()
+    assert lib.dflash_plan_splits(ctypes.byref(d), 9, 0, 7, 0) == 7
+    assert lib.dflash_plan_splits(ctypes.byref(d), 9, 0, 300, 0) == -B.ERR_INVALID_ARG
+    assert lib.dflash_plan_splits(ctypes.byref(good_dims(num_kv_heads=5)), 9, 0, 0, 0) == -B.ERR_INVALID_ARG
+    assert lib.dflash_plan_splits(ctypes.byref(good_dims(head_dim=72)), 9, 0, 0, 0) == -B.ERR_UNSUPPORTED
+    auto = lib.dflash_plan_splits(ctypes.byref(d), 9, 0, 0, 0)
+    assert 1 <= auto <= 256
+    # a sliding window bounds the useful split count by its span
+    assert lib.dflash_plan_splits(ctypes.byref(d), 9, 256, 0, 0) <= 2
+
+
+def test_head_dim_512_accepted_and_above_rejected(lib):
+    assert lib.dflash_plan_splits(ctypes.byref(good_dims(head_dim=512)), 9, 0, 1, 0) == 1
+    assert lib.dflash_plan_splits(ctypes.byref(good_dims(head_dim=528)), 9, 0, 1, 0) == -B.ERR_INVALID_ARG
+
+
+FAKE = 0x10000  # 64 KiB-aligned fake address, never dereferenced
+
+
+def call(lib, dims=None, T=9, causal=0, window=0, scale=0.04, opts=None, **ptrs):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, pt=FAKE, sl=FAKE, out=FAKE, lse=FAKE)
+    p.update(ptrs)
+    d = dims if dims is not None else good_dims()
+    return lib.dflash_block_attn(p["q"], p["k"], p["v"], p["pt"], p["sl"], ctypes.byref(d) if d else None, T,
+                                 causal, window, scale, p["out"], p["lse"], ctypes.byref(opts) if opts else None)
+
+
+@cpu_only
+@pytest.mark.parametrize("kw,code", [
+    (dict(dims=False), B.ERR_INVALID_ARG),
+    (dict(q=0), B.ERR_INVALID_ARG),
+    (dict(out=0), B.ERR_INVALID_ARG),
+    (dict(q=FAKE + 2), B.ERR_INVALID_ARG),
+    (dict(lse=FAKE + 2), B.ERR_INVALID_ARG),
+    (dict(T=0), B.ERR_INVALID_ARG),
+    (dict(T=65), B.ERR_INVALID_ARG),
+    (dict(causal=2), B.ERR_INVALID_ARG),
+    (dict(window=-1), B.ERR_INVALID_ARG),
+    (dict(window=4), B.ERR_INVALID_ARG),          # window < block_len
+    (dict(scale=0.0), B.ERR_INVALID_ARG),
+    (dict(scale=float("nan")), B.ERR_INVALID_ARG),
+    (dict(scale=float("inf")), B.ERR_INVALID_ARG),
+])
+def test_block_attn_rejects_bad_arguments(lib, kw, code):
+    if kw.get("dims") is False:
+        kw = dict(kw)
+        kw["dims"] = None
+        d = None
+        st = lib.dflash_block_attn(FAKE, FAKE, FAKE, FAKE, FAKE, None, 9, 0, 0, 0.04, FAKE, FAKE, None)
+        assert st == code
+        return
+    assert call(lib, **kw) == code
+    assert lib.dflash_last_error_message().decode()
+
+
+@cpu_only
+@pytest.mark.parametrize("dkw,code", [
+    (dict(num_kv_heads=3), B.ERR_INVALID_ARG),
+    (dict(head_dim=40), B.ERR_UNSUPPORTED),
+    (dict(head_dim=1024), B.ERR_INVALID_ARG),
+    (dict(page_size=12), B.ERR_INVALID_ARG),
+    (dict(page_size=512), B.ERR_INVALID_ARG),
+    (dict(batch=0), B.ERR_INVALID_ARG),
+    (dict(num_pages=0), B.ERR_INVALID_ARG),
+    (dict(max_seq_len=512 * 16 + 1), B.ERR_INVALID_ARG),
+    (dict(max_seq_len=4), B.ERR_INVALID_ARG),      # below block_len
+    (dict(dtype=7), B.ERR_INVALID_ARG),
+    (dict(kv_stride_slot=4 * 512 + 4), B.ERR_INVALID_ARG),   # 8-byte stride, not 16
+    (dict(kv_stride_head=256), B.ERR_INVALID_ARG),
+])
+def test_block_attn_rejects_bad_dims(lib, dkw, code):
+    assert call(lib, dims=good_dims(**dkw)) == code
+
+
+@cpu_only
+def test_split_needs_workspace(lib):
+    o = B.Opts()
+    o.num_splits = 4
+    assert call(lib, opts=o) == B.ERR_WORKSPACE
+    o.workspace = FAKE
+    o.workspace_bytes = 1024
+    assert call(lib, opts=o) == B.ERR_WORKSPACE
+    o.workspace = FAKE + 16  # misaligned
+    o.workspace_bytes = 1 << 40
+    assert call(lib, opts=o) == B.ERR_WORKSPACE
+    o.workspace = FAKE
+    o.num_splits = 257
+    assert call(lib, opts=o) == B.ERR_INVALID_ARG
+
+
+@cpu_only
+def test_forced_tc_kernel_rejects_fp32(lib):
+    o = B.Opts()
+    o.kernel = B.KERNELS["tc"]
+    assert call(lib, dims=good_dims(dtype=B.FP32), opts=o) == B.ERR_UNSUPPORTED
+    o.kernel = 9
+    assert call(lib, opts=o) == B.ERR_INVALID_ARG
+
+
+@cpu_only
+@pytest.mark.parametrize("args,code", [
+    ((0, FAKE, 2, 10, 64, B.FP32, FAKE, FAKE, None), B.ERR_INVALID_ARG),
+    ((FAKE, FAKE, 0, 10, 64, B.FP32, FAKE, FAKE, None), B.ERR_INVALID_ARG),
+    ((FAKE, FAKE, 257, 10, 64, B.FP32, FAKE, FAKE, None), B.ERR_INVALID_ARG),
+    ((FAKE, FAKE, 2, 0, 64, B.FP32, FAKE, FAKE, None), B.ERR_INVALID_ARG),
+    ((FAKE, FAKE, 2, 10, 66, B.FP32, FAKE, FAKE, None), B.ERR_INVALID_ARG),
+    ((FAKE, FAKE, 2, 10, 1024, B.FP32, FAKE, FAKE, None), B.ERR_INVALID_ARG),
+    ((FAKE, FAKE, 2, 10, 64, 3, FAKE, FAKE, None), B.ERR_INVALID_ARG),
+    ((FAKE + 4, FAKE, 2, 10, 64, B.FP32, FAKE, FAKE, None), B.ERR_INVALID_ARG),
+])
+def test_split_combine_rejects_bad_arguments(lib, args, code):
+    assert lib.dflash_split_combine(*args) == code
+
+
+def test_read_error_rejects_null(lib):
+    w = ctypes.c_uint32(0)
+    assert lib.dflash_read_error(None, None, ctypes.byref(w), 0) == B.ERR_INVALID_ARG
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        B.load_library(str(tmp_path / "missing.so"))

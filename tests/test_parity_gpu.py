@@ -1,0 +1,338 @@
+"""GPU parity: libdflash_attn (through its C ABI) against the fp64 oracle.
+
+Bars: bf16 outputs |gpu - oracle| <= 1e-2 + 1e-2*|oracle| element-wise (lse
+too); fp32 outputs <= 1e-5 absolute; page-table indexing bit-exact (a shuffled
+page table gives the same bits as the identity table over the same logical
+K/V). Small cases span several key tiles with ragged tails; the named
+workloads run at full size (every output where the oracle finishes in
+seconds, sampled rows otherwise) with the library's own split plan.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import speculative_decoding_block_dflash_gb300 as dfl
+from speculative_decoding_block_dflash_gb300 import build as build_mod
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 1e-2
+FP32_TOL = 1e-5
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_mod.build()
+    oracle.build()
+    dfl.load_library()
+
+
+def _tc_available(case):
+    dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
+    try:
+        dfl.plan_splits(dims, case.block_len, case.window, 0, "tc")
+        return True
+    except dfl.DflashError:
+        return False
+
+
+def run(case, kernel="auto", num_splits=None, page_table=None, **kw):
+    out, lse = dfl.block_attn(case.q, case.k_cache, case.v_cache,
+                              case.page_table if page_table is None else page_table,
+                              case.seq_lens, case.block_len, causal=case.causal, window=case.window,
+                              scale=case.scale, kernel=kernel,
+                              num_splits=case.num_splits if num_splits is None else num_splits, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def check_close(gpu, ref, tol_abs, tol_rel, what):
+    g = gpu.detach().float().cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite GPU values"
+    err = np.abs(g - ref)
+    bound = tol_abs + tol_rel * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; "
+                           f"max err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}")
+
+
+def tols(case):
+    return (FP32_TOL, 0.0) if case.q.dtype == torch.float32 else (BF16_TOL, BF16_TOL)
+
+
+def check_full(case, out, lse):
+    ref_o, ref_l = oracle.block_attn(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens,
+                                     case.block_len, causal=case.causal, window=case.window, scale=case.scale)
+    ta, tr = tols(case)
+    check_close(out, ref_o, ta, tr, f"{case.name} out")
+    check_close(lse, ref_l, ta, tr, f"{case.name} lse")
+
+
+def sample_rows(case, per_request=6, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b in range(case.batch):
+        picks = {(0, 0), (case.num_q_heads - 1, case.block_len - 1)}
+        while len(picks) < per_request:
+            picks.add((int(rng.integers(case.num_q_heads)), int(rng.integers(case.block_len))))
+        rows += [(b, h, i) for h, i in sorted(picks)]
+    return np.array(rows, dtype=np.int32)
+
+
+def check_sampled(case, out, lse, per_request=6):
+    rows = sample_rows(case, per_request)
+    ref_o, ref_l = oracle.block_attn_rows(case.q, case.k_cache, case.v_cache, case.page_table,
+                                          case.seq_lens, case.block_len, rows, causal=case.causal,
+                                          window=case.window, scale=case.scale)
+    idx = torch.tensor(rows[:, 0] * case.block_len + rows[:, 2], device=out.device, dtype=torch.long)
+    hh = torch.tensor(rows[:, 1], device=out.device, dtype=torch.long)
+    ta, tr = tols(case)
+    check_close(out[idx, hh], ref_o, ta, tr, f"{case.name} sampled out")
+    check_close(lse[idx, hh], ref_l, ta, tr, f"{case.name} sampled lse")
+
+
+KERNELS = ["simt", "tc"]
+
+
+def maybe_skip(case, kernel):
+    if kernel == "tc" and (case.q.dtype != torch.bfloat16 or not _tc_available(case)):
+        pytest.skip("tensor-core kernel does not cover this case")
+
+
+# ----------------------------------------------------------------------------- small cases
+
+
+def test_tiny_fp32_matches_oracle():
+    case = workloads.make_case("tiny", device="cuda")
+    out, lse = run(case)
+    check_full(case, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window", [0, 64])
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_ragged_small_bf16(kernel, causal, window, splits):
+    case = workloads.make_custom("ragged", 3, 9, 8, 2, 128, [9, 300, 777], causal=causal, window=window,
+                                 seed=11, device="cuda")
+    maybe_skip(case, kernel)
+    out, lse = run(case, kernel=kernel, num_splits=splits)
+    check_full(case, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("D", [64, 256, 512])
+@pytest.mark.parametrize("T", [9, 16])
+def test_gqa8_head_dims(kernel, D, T):
+    case = workloads.make_custom("gqa8", 2, T, 16, 2, D, [1000, 2500], seed=12 + D + T, device="cuda")
+    maybe_skip(case, kernel)
+    out, lse = run(case, kernel=kernel)
+    check_full(case, out, lse)
+
+
+@pytest.mark.parametrize("T", [1, 2, 33, 64])
+def test_block_len_extremes_simt(T):
+    case = workloads.make_custom("blk", 2, T, 4, 1, 64, [T, T + 200], causal=True, seed=13 + T, device="cuda")
+    out, lse = run(case, kernel="simt")
+    check_full(case, out, lse)
+
+
+def test_fp32_ragged_tight():
+    case = workloads.make_custom("fp32", 2, 9, 4, 2, 64, [100, 333], dtype=torch.float32, causal=True,
+                                 window=50, seed=14, device="cuda")
+    out, lse = run(case, num_splits=4)
+    check_full(case, out, lse)
+
+
+# ----------------------------------------------------------------------------- named workloads, full size
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_global_verify_full(kernel):
+    case = workloads.make_case("global_verify", device="cuda")
+    maybe_skip(case, kernel)
+    out, lse = run(case, kernel=kernel)
+    check_full(case, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name", ["sliding", "sliding_causal"])
+def test_sliding_full(kernel, name):
+    case = workloads.make_case(name, device="cuda")
+    maybe_skip(case, kernel)
+    out, lse = run(case, kernel=kernel)
+    check_full(case, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("B", [1, 2, 4, 8])
+def test_batch_sweep_sampled(kernel, B):
+    case = workloads.make_case(f"batch_sweep_b{B}", device="cuda")
+    maybe_skip(case, kernel)
+    out, lse = run(case, kernel=kernel)
+    check_sampled(case, out, lse)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_long_draft_split16_sampled(kernel):
+    case = workloads.make_case("long_draft", device="cuda")
+    maybe_skip(case, kernel)
+    assert case.num_splits == 16
+    out, lse = run(case, kernel=kernel)
+    check_sampled(case, out, lse, per_request=4)
+    del case
+    torch.cuda.empty_cache()
+
+
+# ----------------------------------------------------------------------------- exactness / invariants
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_page_table_permutation_is_bit_exact(kernel):
+    """Same logical K/V under the identity and a shuffled page table: identical bits."""
+    case = workloads.make_custom("perm", 2, 9, 16, 2, 256, [700, 1500], identity_pages=True, seed=15,
+                                 device="cuda")
+    maybe_skip(case, kernel)
+    a, la = run(case, kernel=kernel, num_splits=3)
+    pool = case.k_cache.shape[0]
+    perm = torch.randperm(pool, generator=torch.Generator().manual_seed(1)).cuda()
+    k2 = torch.empty_like(case.k_cache)
+    v2 = torch.empty_like(case.v_cache)
+    k2[perm] = case.k_cache
+    v2[perm] = case.v_cache
+    pt2 = perm[case.page_table.long()].to(torch.int32)
+    out2, lse2 = dfl.block_attn(case.q, k2, v2, pt2, case.seq_lens, case.block_len, scale=case.scale,
+                                kernel=kernel, num_splits=3)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(la, lse2)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_garbage_beyond_seq_len_does_not_leak(kernel):
+    """Slots past L_b in the last page hold NaN/Inf: the output must not see them."""
+    case = workloads.make_custom("nan", 2, 9, 8, 2, 128, [205, 390], seed=16, device="cuda")
+    maybe_skip(case, kernel)
+    ref_o, ref_l = oracle.block_attn(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens, 9,
+                                     scale=case.scale)
+    for b, L in enumerate(case.seq_lens_host()):
+        last = int(case.page_table[b, (L - 1) // 16])
+        case.k_cache[last, L % 16:] = float("nan")
+        case.v_cache[last, L % 16:] = float("inf")
+    out, lse = run(case, kernel=kernel, num_splits=2)
+    check_close(out, ref_o, BF16_TOL, BF16_TOL, "nan-poisoned out")
+    check_close(lse, ref_l, BF16_TOL, BF16_TOL, "nan-poisoned lse")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_noncausal_query_permutation(kernel):
+    case = workloads.make_custom("qperm", 1, 9, 8, 1, 128, [600], seed=17, device="cuda")
+    maybe_skip(case, kernel)
+    a, la = run(case, kernel=kernel)
+    perm = torch.randperm(9, generator=torch.Generator().manual_seed(2)).cuda()
+    case.q = case.q[perm].contiguous()
+    b, lb = run(case, kernel=kernel)
+    torch.testing.assert_close(b.float(), a[perm].float(), atol=2e-2, rtol=2e-2)
+    torch.testing.assert_close(lb, la[perm], atol=1e-3, rtol=1e-3)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_split_counts_agree(kernel):
+    case = workloads.make_custom("splits", 2, 16, 16, 2, 512, [3000, 5000], seed=18, device="cuda")
+    maybe_skip(case, kernel)
+    ref, lref = run(case, kernel=kernel, num_splits=1)
+    for s in (2, 16, 0):
+        out, lse = run(case, kernel=kernel, num_splits=s)
+        torch.testing.assert_close(out.float(), ref.float(), atol=1e-2, rtol=1e-2)
+        torch.testing.assert_close(lse, lref, atol=1e-3, rtol=1e-3)
+
+
+def test_window_covering_everything_equals_global():
+    case = workloads.make_custom("wg", 2, 9, 8, 2, 128, [300, 500], seed=19, device="cuda")
+    a, la = run(case)
+    case.window = 10000
+    b, lb = run(case)
+    torch.testing.assert_close(b.float(), a.float(), atol=1e-2, rtol=1e-2)
+    torch.testing.assert_close(lb, la, atol=1e-3, rtol=1e-3)
+
+
+def test_split_combine_matches_oracle():
+    g = torch.Generator(device="cuda").manual_seed(20)
+    S, rows, D = 7, 50, 512
+    po = torch.randn(S, rows, D, device="cuda", generator=g)
+    pl = torch.randn(S, rows, device="cuda", generator=g) * 3
+    pl[2] = -float("inf")
+    pl[:, 5] = -float("inf")  # an all-empty row
+    out, lse = dfl.split_combine(po, pl, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.split_combine(po.cpu().numpy(), pl.cpu().numpy())
+    ok = np.isfinite(ref_l)
+    check_close(out[torch.tensor(ok, device="cuda")], ref_o[ok], FP32_TOL, FP32_TOL, "combine out")
+    check_close(lse[torch.tensor(ok, device="cuda")], ref_l[ok], FP32_TOL, FP32_TOL, "combine lse")
+    assert torch.isneginf(lse[5]).item() and (out[5] == 0).all().item()
+    out_b, _ = dfl.split_combine(po, pl, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    check_close(out_b[torch.tensor(ok, device="cuda")], ref_o[ok], BF16_TOL, BF16_TOL, "combine bf16 out")
+
+
+# ----------------------------------------------------------------------------- device checks
+
+
+def test_bad_page_id_is_reported_not_dereferenced():
+    case = workloads.make_custom("badpage", 1, 9, 4, 1, 64, [200], seed=21, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    pt = case.page_table.clone()
+    pt[0, 3] = case.k_cache.shape[0] + 1000
+    pt[0, 5] = -7
+    dfl.block_attn(case.q, case.k_cache, case.v_cache, pt, case.seq_lens, 9, kernel="simt", workspace=ws)
+    assert dfl.read_error(ws) & dfl.DEVERR_PAGE_ID
+    assert dfl.read_error(ws) == 0  # cleared
+    dfl.block_attn(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens, 9, workspace=ws)
+    assert dfl.read_error(ws) == 0
+
+
+def test_bad_seq_len_is_reported():
+    case = workloads.make_custom("badlen", 2, 9, 4, 1, 64, [200, 300], seed=22, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    sl = case.seq_lens.clone()
+    sl[1] = 5  # shorter than the block
+    out, _ = dfl.block_attn(case.q, case.k_cache, case.v_cache, case.page_table, sl, 9, workspace=ws)
+    assert dfl.read_error(ws) & dfl.DEVERR_SEQ_LEN
+    assert (out[9:] == 0).all().item()
+    sl[1] = 10 ** 6  # beyond max_pages * page_size
+    dfl.block_attn(case.q, case.k_cache, case.v_cache, case.page_table, sl, 9, workspace=ws)
+    assert dfl.read_error(ws) & dfl.DEVERR_SEQ_LEN
+
+
+# ----------------------------------------------------------------------------- CUDA graphs
+
+
+def test_cuda_graph_capture_and_replay():
+    case = workloads.make_case("global_verify", device="cuda")
+    ref, lref = run(case)
+    dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
+    splits = dfl.plan_splits(dims, case.block_len, 0, 0)
+    ws = torch.zeros(dfl.workspace_bytes(dims, case.block_len, splits), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(case.q)
+    lse = torch.empty(case.q.shape[:2], dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dfl.block_attn(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens, 9, out=out, lse=lse,
+                       workspace=ws, num_splits=splits)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dfl.block_attn(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens, 9, out=out, lse=lse,
+                       workspace=ws, num_splits=splits)
+    out.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(lse, lref)
