@@ -163,9 +163,12 @@ int choose_kernel(const dflash_dims* d, int32_t T, int32_t window, int32_t reque
 int64_t work_units(const dflash_dims* d, int32_t T, int kernel)
 {
     if (kernel == DFLASH_KERNEL_TC) {
-        const int R = (d->num_q_heads / d->num_kv_heads) * T;
-        const int per_cta = 64;  // packed rows per tensor-core CTA, see tc_attn.cu
-        return (int64_t)d->batch * d->num_kv_heads * ((R + per_cta - 1) / per_cta);
+        AttnParams p{};
+        p.B = d->batch;
+        p.T = T;
+        p.Hkv = d->num_kv_heads;
+        p.G = d->num_q_heads / d->num_kv_heads;
+        return tc_ctas_per_split(p);
     }
     return (int64_t)d->batch * d->num_q_heads * ((T + 15) / 16);
 }

@@ -47,6 +47,7 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, int32_t
 
 // Tensor-core kernel: whether it covers these sizes, and its launcher.
 bool tc_supports(const AttnParams& p);
+int tc_ctas_per_split(const AttnParams& p);  // CTAs per split chunk (B * Hkv * row groups)
 cudaError_t launch_tc_attn(const AttnParams& p, cudaStream_t stream);
 
 // SM count of the current device (cached per device).

@@ -1,11 +1,949 @@
-// Tensor-core (tcgen05 / TMEM / TMA) block attention for bf16 -- placeholder
-// until the kernel lands: covers no sizes, so AUTO selects the SIMT kernel.
+// Tensor-core block attention for bf16 on sm_103a: tcgen05.mma with TMEM
+// accumulators, paged K/V staged by TMA into a shared-memory ring.
+//
+// Problem (DFlash block attention): per (request b, KV head g) the G query
+// heads x T block queries that share g are packed into R = Gc*T rows of one
+// tile ("num_query_per_req = 1 + num_speculative_tokens", kenforever1
+// "dflash-gemma4-31b-notes"; GQA 8 x 9 = 72 rows at the Gemma-4-31B global
+// layer shape). Every key byte is read once per CTA and feeds all R rows, so
+// the packed tile is a dense contraction: QK^T and PV run on the tensor cores.
+//
+// Transposed formulation. head_dim reaches 512 ("head_size <= 512", same
+// page), and an fp32 O accumulator of 128 x 512 would fill all 512 TMEM
+// columns. So the kernel computes
+//     S^T [128 keys x N rows]    = K_tile [128 x D] . Q^T [D x N]        (M = 128 keys)
+//     O^T [D x N] (4 chunks)    += V_tile^T [D x 128] . P^T [128 x N]   (M = 128 dims)
+// with N = R rounded up to 16 (<= 80): TMEM holds S^T (N columns) and O^T
+// (D/128 * N columns), 400 columns at D = 512, N = 80.
+//
+// Softmax (thread = one key lane of the tile): scores are masked by select
+// (non-causal rows see every key up to L-1, causal rows keys up to their own
+// position, a window W keeps the last W keys -- vLLM PR #43445 "Allow causal
+// DFlash"), the running row max m is shared by the 128 softmax threads
+// (cross-lane shuffle + shared-memory reduction) and only raised when a score
+// exceeds it by more than 2^8 in the exp2 domain (O^T and the per-thread row
+// sums are then rescaled by exp2(m_old - m_new)); P = exp2(s - m) is rounded
+// to bf16 and written to shared memory as the B operand of the PV MMA. The
+// row sum l is accumulated per key lane from the rounded P and reduced once
+// at the end.
+//
+// Warp roles (192 threads): warps 0-3 softmax + epilogue, warp 4 TMA
+// producer, warp 5 MMA issuer. Ring stages are 16 KB: a K stage is 128 keys x
+// 64 dims (K-major, 128-byte swizzle), a V stage 64 keys x 128 dims
+// (MN-major). One TMA box is one page's tokens of one KV head x 64 dims; the
+// page id comes from the page table (validated; out-of-range ids and pages
+// past the chunk are fetched at an out-of-bounds page coordinate, which the
+// TMA unit fills with zeros without touching memory). V rows of the last,
+// partial page past seq_len are zeroed in shared memory before the PV MMA so
+// garbage there can never reach the output.
+//
+// Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the kernel
+// records DFLASH_DEVERR_TIMEOUT, drains its own TMA copies and MMAs (bounded),
+// frees TMEM and returns.
+#include <cuda.h>
+
+#include <cmath>
+#include <mutex>
+
 #include "dflash_device.cuh"
 
 namespace dflash {
+namespace {
 
-bool tc_supports(const AttnParams&) { return false; }
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kTileKeys = 128;
+constexpr int kStageBytes = 16384;
+constexpr int kMaxPids = 512;
+constexpr int kMaxRows = 80;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThresh = 8.0f;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+constexpr int kOnesBytes = 4096;
 
-cudaError_t launch_tc_attn(const AttnParams&, cudaStream_t) { return cudaErrorNotSupported; }
+struct TcExtra {
+    int32_t Gc;    // query heads per CTA
+    int32_t n_rg;  // row groups per KV head (G / Gc)
+    int32_t R;     // packed rows per CTA (Gc * T)
+};
+
+constexpr int pow2ceil(int x)
+{
+    int p = 32;
+    while (p < x) p <<= 1;
+    return p;
+}
+
+template <int D, int N>
+struct TcLayout {
+    static constexpr int kFixed = N * D * 2 + N * 128 * 2 + 4096 + kOnesBytes;
+    static constexpr int kStagesFit = (227 * 1024 - 1024 - kFixed) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static constexpr int kQOff = 0;                                  // [D/64][N rows][128 B]
+    static constexpr int kRingOff = kQOff + N * D * 2;               // [stages][16 KB]
+    static constexpr int kPOff = kRingOff + kStages * kStageBytes;   // [2 key halves][N rows][128 B]
+    static constexpr int kOnesOff = kPOff + N * 128 * 2;             // bf16 ones [128 x 16] (row-sum MMA)
+    static constexpr int kBarOff = kOnesOff + kOnesBytes;
+    static constexpr int kNumBars = 2 * kStages + 6;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;          // tmem base, abort flag
+    static constexpr int kMOff = kMiscOff + 16;                      // float m_s[N]
+    static constexpr int kAOff = kMOff + N * 4;                      // float alpha_s[N]
+    static constexpr int kRedOff = kAOff + N * 4;                    // float red[4][N]
+    static constexpr int kLoOff = kRedOff + 4 * N * 4;               // int lo_s[N]
+    static constexpr int kHiOff = kLoOff + N * 4;                    // int hi_s[N]
+    static constexpr int kRowOff = kHiOff + N * 4;                   // int64 orow_s[N]
+    static constexpr int kPidOff = kRowOff + N * 8;                  // int pid_s[kMaxPids]
+    static constexpr int kTotal = kPidOff + kMaxPids * 4;
+    static constexpr int kAlloc = kTotal + 1024;
+    static constexpr int kTmemCols = pow2ceil(N * (2 + D / 128));
+    static_assert(kStages >= 3, "ring too shallow");
+    static_assert(N * (2 + D / 128) <= 512, "TMEM budget");
+    static_assert((N * D * 2) % 1024 == 0 && (N * 128) % 1024 == 0, "1024-byte swizzle atoms");
+};
+
+// ----------------------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: false on timeout (recorded) or when another warp aborted.
+__device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            raise_error(err, DFLASH_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Orders later uses of loaded registers after tcgen05.wait::ld.
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]));
+}
+
+__device__ __forceinline__ void named_bar_sync_128() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ bool named_bar_or_128(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
+// address, leading / stride byte offsets in 16-byte units, version 1 at bit
+// 46, layout type 2 = SWIZZLE_128B at bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Descriptor without swizzle (layout type 0): core matrices of 8 rows x 16 B.
+__device__ __forceinline__ uint64_t noswz_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B,
+// A/B major-ness (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, int a_mn, int b_mn)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+// ----------------------------------------------------------------------------- kernel
+
+template <int D, int N>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const AttnParams p, const TcExtra x)
+{
+    using Lay = TcLayout<D, N>;
+    constexpr int S = Lay::kStages;
+    constexpr int KC = D / 64;   // K stages per tile (64-dim chunks)
+    constexpr int VC = D / 128;  // O^T chunks (128-dim), V stages per 64-key half
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* q_s = smem + Lay::kQOff;
+    uint8_t* ring = smem + Lay::kRingOff;
+    uint8_t* p_s = smem + Lay::kPOff;
+    uint8_t* ones_s = smem + Lay::kOnesOff;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + S;
+    uint64_t* q_full = bars + 2 * S;
+    uint64_t* s_full = q_full + 1;
+    uint64_t* s_free = q_full + 2;
+    uint64_t* p_full = q_full + 3;
+    uint64_t* p_free = q_full + 4;
+    uint64_t* drain = q_full + 5;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
+    float* m_s = reinterpret_cast<float*>(smem + Lay::kMOff);
+    float* a_s = reinterpret_cast<float*>(smem + Lay::kAOff);
+    float* red = reinterpret_cast<float*>(smem + Lay::kRedOff);
+    int32_t* lo_s = reinterpret_cast<int32_t*>(smem + Lay::kLoOff);
+    int32_t* hi_s = reinterpret_cast<int32_t*>(smem + Lay::kHiOff);
+    int64_t* orow_s = reinterpret_cast<int64_t*>(smem + Lay::kRowOff);
+    int32_t* pid_s = reinterpret_cast<int32_t*>(smem + Lay::kPidOff);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int c_split = blockIdx.x;
+    const int g = blockIdx.y / x.n_rg;
+    const int rg = blockIdx.y % x.n_rg;
+    const int b = blockIdx.z;
+    const int T = p.T;
+    const int Psz = p.page_size;
+    const int R = x.R;
+    const int h0 = g * p.G + rg * x.Gc;
+
+    const int32_t L = __ldg(p.seq_lens + b);
+    const bool len_ok = seq_len_ok(p, L);
+    Chunk ch;
+    ch.kb = 0;
+    ch.ke = 0;
+    if (len_ok) ch = split_chunk(L, T, p.window, Psz, p.splits, c_split);
+    const int t0 = (ch.kb / Psz) * Psz;
+    const int ntiles = (ch.kb < ch.ke) ? (ch.ke - t0 + kTileKeys - 1) / kTileKeys : 0;
+
+    // ---------------------------------------------------------------- set-up
+    if (tid == 0) {
+        for (int i = 0; i < 2 * S + 6; ++i) {
+            uint64_t* bar = bars + i;
+            mbar_init(bar, (bar == s_free || bar == p_full) ? 128u : 1u);
+        }
+        *abort_flag = 0;
+        if (!len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (tid < N) {
+        int32_t lo = -(1 << 30), hi = (1 << 30);
+        int64_t orow = -1;
+        if (tid < R) {
+            const int i = tid / x.Gc;
+            const int hh = tid - i * x.Gc;
+            const KeyRange kr = row_range(L, T, i, p.causal, p.window);
+            lo = kr.lo;
+            hi = kr.hi;
+            orow = (int64_t)(b * T + i) * p.Hq + (h0 + hh);
+        }
+        lo_s[tid] = lo;
+        hi_s[tid] = hi;
+        orow_s[tid] = orow;
+        m_s[tid] = -INFINITY;
+        a_s[tid] = 1.f;
+    }
+    if (warp == kMmaWarp) {
+        // all-ones A operand of the row-sum MMA (bf16 1.0 = 0x3F80)
+        for (int idx = lane; idx < kOnesBytes / 16; idx += 32)
+            *reinterpret_cast<uint4*>(ones_s + idx * 16) = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        fence_proxy_async_smem();
+    }
+    if (warp == kProducerWarp) {
+        // zero the padding rows of Q (TMA writes rows [0, R) of every 64-dim chunk)
+        if (R < N) {
+            for (int idx = lane; idx < KC * (N - R) * 8; idx += 32) {
+                const int kc = idx / ((N - R) * 8);
+                const int rem = idx - kc * (N - R) * 8;
+                const int row = R + rem / 8;
+                const int c16 = rem % 8;
+                *reinterpret_cast<uint4*>(q_s + kc * N * 128 + row * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+        }
+        tmem_alloc(tmem_slot, Lay::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem_s = tmem;          // S^T: columns [0, N)
+    const uint32_t tmem_o = tmem + N;      // O^T chunk c: columns [N + c*N, N + (c+1)*N)
+    const uint32_t tmem_l = tmem + N + VC * N;  // row sums l (every lane holds all N), N columns
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer
+        const int pages_per_tile = kTileKeys / Psz;
+        const int first_page = t0 / Psz;
+        const int chunk_pages = ntiles * pages_per_tile;
+        int wbase = -kMaxPids;  // window of page ids held in pid_s: relative pages [wbase, wbase + kMaxPids)
+        auto load_window = [&](int base) {
+            for (int rel = lane; rel < kMaxPids; rel += 32) {
+                const int pr = base + rel;
+                int32_t id = p.num_pages;  // out-of-bounds coordinate: zero fill, no memory traffic
+                if (pr < chunk_pages && t0 + pr * Psz < ch.ke) {
+                    const int32_t v = __ldg(p.page_table + (int64_t)b * p.max_pages + first_page + pr);
+                    if (v >= 0 && v < p.num_pages)
+                        id = v;
+                    else
+                        raise_error(p.err, DFLASH_DEVERR_PAGE_ID);
+                }
+                pid_s[rel] = id;
+            }
+            __syncwarp();
+            wbase = base;
+        };
+        auto pid = [&](int rel) -> int32_t { return pid_s[rel - wbase]; };
+
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        uint32_t issued_parity[S];
+#pragma unroll
+        for (int s = 0; s < S; ++s) issued_parity[s] = 2;  // 2 = nothing outstanding
+        auto acquire = [&]() -> bool {
+            bool got = true;
+            if (lane == 0) got = wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.err);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            return got;
+        };
+        auto advance = [&]() {
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        };
+
+        if (ntiles > 0) {
+            if (lane == 0) {
+                mbar_expect_tx(q_full, (uint32_t)(R * 128 * KC));
+                for (int kc = 0; kc < KC; ++kc) tma_load_3d(q_s + kc * N * 128, &tm_q, q_full, kc * 64, h0, b * T);
+            }
+            for (int job = 0; job <= ntiles && ok; ++job) {
+                // K(job), then V(job - 1)
+                if (job < ntiles) {
+                    const int rel0 = job * pages_per_tile;
+                    const int wneed = job > 0 ? rel0 - pages_per_tile : rel0;
+                    if (rel0 + pages_per_tile > wbase + kMaxPids || wneed < wbase) load_window(wneed);
+                    for (int kc = 0; kc < KC && ok; ++kc) {
+                        ok = acquire();
+                        if (!ok) break;
+                        if (lane == 0) {
+                            uint8_t* dst = ring + stage * kStageBytes;
+                            mbar_expect_tx(full + stage, kStageBytes);
+                            for (int pg = 0; pg < pages_per_tile; ++pg)
+                                tma_load_4d(dst + pg * Psz * 128, &tm_k, full + stage, kc * 64, g, 0, pid(rel0 + pg));
+                            issued_parity[stage] = phase;
+                        }
+                        __syncwarp();
+                        advance();
+                    }
+                }
+                if (job >= 1 && ok) {
+                    const int jv = job - 1;
+                    const int rel0 = jv * pages_per_tile;
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        for (int c = 0; c < VC && ok; ++c) {
+                            ok = acquire();
+                            if (!ok) break;
+                            if (lane == 0) {
+                                uint8_t* dst = ring + stage * kStageBytes;
+                                mbar_expect_tx(full + stage, kStageBytes);
+                                const int ppg = 64 / Psz;
+                                for (int m = 0; m < 2; ++m)
+                                    for (int pg = 0; pg < ppg; ++pg)
+                                        tma_load_4d(dst + m * 8192 + pg * Psz * 128, &tm_v, full + stage,
+                                                    c * 128 + m * 64, g, 0, pid(rel0 + h * ppg + pg));
+                                issued_parity[stage] = phase;
+                            }
+                            __syncwarp();
+                            advance();
+                        }
+                    }
+                }
+            }
+        }
+        // Drain: make sure no TMA copy of ours is still landing when the CTA exits.
+        if (lane == 0 && !ok) {
+            for (int s = 0; s < S; ++s) {
+                if (issued_parity[s] > 1) continue;
+                const unsigned long long t_start = globaltimer();
+                while (!mbar_try_wait(full + s, issued_parity[s]) && globaltimer() - t_start < kTimeoutNs) {
+                }
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc_s = make_idesc(128, N, 0, 0);  // S^T = K . Q^T   (A K-major, B K-major)
+        constexpr uint32_t idesc_o = make_idesc(128, N, 1, 0);  // O^T += V^T . P^T (A MN-major, B K-major)
+        constexpr uint32_t idesc_l = make_idesc(128, N, 0, 0);  // l   += 1 . P^T   (A K-major, B K-major)
+        const uint32_t q_addr = smem_u32(q_s);
+        const uint32_t p_addr = smem_u32(p_s);
+        const uint32_t ring_addr = smem_u32(ring);
+        const uint32_t ones_addr = smem_u32(ones_s);
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        auto wait_lane0 = [&](uint64_t* bar, uint32_t par) -> bool {
+            bool got = true;
+            if (lane == 0) got = wait_bounded(bar, par, abort_flag, p.err);
+            got = __shfl_sync(0xffffffffu, got, 0);
+            return got;
+        };
+        auto advance = [&]() {
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        };
+        // PV of tile jj: O^T[c] += V^T(stage) . P^T(half h)
+        auto issue_pv = [&](int jj) -> bool {
+            if (!wait_lane0(p_full, (uint32_t)(jj & 1))) return false;
+            tc_fence_after();
+            const int tile_key0 = t0 + jj * kTileKeys;
+            for (int h = 0; h < 2; ++h) {
+                for (int c = 0; c < VC; ++c) {
+                    if (!wait_lane0(full + stage, phase)) return false;
+                    tc_fence_after();
+                    // zero V rows past seq_len inside the sequence's last, partial page
+                    const int key0 = tile_key0 + h * 64;
+                    const int zlo = L - key0;
+                    if (L % Psz != 0 && zlo > 0 && zlo < 64 && ch.ke == L) {
+                        const int zhi = min(64, ((L + Psz - 1) / Psz) * Psz - key0);
+                        uint8_t* st = ring + stage * kStageBytes;
+                        const int rows = zhi - zlo;
+                        for (int idx = lane; idx < rows * 2 * 8; idx += 32) {
+                            const int m = idx / (rows * 8);
+                            const int rem = idx - m * rows * 8;
+                            const int row = zlo + rem / 8;
+                            *reinterpret_cast<uint4*>(st + m * 8192 + row * 128 + (rem % 8) * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                    if (lane == 0) {
+                        const uint32_t st = ring_addr + stage * kStageBytes;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sw128_desc(st + kk * 2048, 8192, 1024);
+                            const uint64_t bdesc = sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024);
+                            tc_mma(tmem_o + c * N, a, bdesc, idesc_o, (jj > 0 || h > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(empty + stage);
+                    }
+                    __syncwarp();
+                    advance();
+                }
+                // l[r] += sum over this half's 64 keys of P^T[key][r]: ones[128 x 16] . P^T
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t a = noswz_desc(ones_addr, 2048, 128);
+                        const uint64_t bdesc = sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024);
+                        tc_mma(tmem_l, a, bdesc, idesc_l, (jj > 0 || h > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                __syncwarp();
+            }
+            if (lane == 0) tc_commit(p_free);
+            __syncwarp();
+            return true;
+        };
+
+        if (ntiles > 0) {
+            ok = wait_lane0(q_full, 0);
+            tc_fence_after();
+            for (int j = 0; j < ntiles && ok; ++j) {
+                if (j > 0) {
+                    ok = wait_lane0(s_free, (uint32_t)((j - 1) & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                for (int kc = 0; kc < KC && ok; ++kc) {
+                    ok = wait_lane0(full + stage, phase);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t st = ring_addr + stage * kStageBytes;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t a = sw128_desc(st + kk * 32, 16, 1024);
+                            const uint64_t bdesc = sw128_desc(q_addr + kc * N * 128 + kk * 32, 16, 1024);
+                            tc_mma(tmem_s, a, bdesc, idesc_s, (kc > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(empty + stage);
+                    }
+                    __syncwarp();
+                    advance();
+                }
+                if (!ok) break;
+                if (lane == 0) tc_commit(s_full);
+                __syncwarp();
+                if (j > 0) ok = issue_pv(j - 1);
+            }
+            if (ok) ok = issue_pv(ntiles - 1);
+        }
+        // Drain our MMAs before TMEM is released.
+        if (lane == 0) {
+            tc_commit(drain);
+            const unsigned long long t_start = globaltimer();
+            while (!mbar_try_wait(drain, 0) && globaltimer() - t_start < kTimeoutNs) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warps 0-3 (thread = key lane)
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const float sl2 = p.scale * kLog2e;
+        bool ok = true;
+        const bool plain = (p.causal == 0 && p.window == 0);
+        // P^T store address pieces for this key lane (K-major, 128-byte swizzle)
+        uint8_t* pcol = p_s + (tid >> 6) * (N * 128);
+        const int pchunk = (tid & 63) >> 3;
+        const int pbyte = (tid & 7) * 2;
+
+        // One thread waits on the mbarrier; the named barrier makes the outcome
+        // uniform across the 128 softmax threads (so none is left at a barrier).
+        auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool got = true;
+            if (tid == 0) got = wait_bounded(bar, parity, abort_flag, p.err);
+            return !named_bar_or_128(!got);
+        };
+        for (int j = 0; j < ntiles && ok; ++j) {
+            if (!group_wait(s_full, (uint32_t)(j & 1))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float s[N];
+#pragma unroll
+            for (int q16 = 0; q16 < N / 16; ++q16) {
+                uint32_t r16[16];
+                tmem_ld16(tmem_s + lane_base + q16 * 16, r16);
+                tmem_ld_wait();
+                reg_fence16(r16);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) s[q16 * 16 + u] = u2f(r16[u]);
+            }
+            tc_fence_before();
+            mbar_arrive(s_free);
+
+            const int key = t0 + j * kTileKeys + tid;
+            const bool kvalid = key >= ch.kb && key < ch.ke;
+            bool need = false;
+#pragma unroll
+            for (int r = 0; r < N; ++r) {
+                bool vis = kvalid;
+                if (!plain) vis = vis && key >= lo_s[r] && key <= hi_s[r];
+                s[r] = vis ? s[r] * sl2 : -INFINITY;
+                need = need || (s[r] > m_s[r] + kRescaleThresh);
+            }
+            need = named_bar_or_128(need);
+            if (need) {
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    float v = s[r];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+                    if ((r & 31) == lane) red[warp * N + r] = v;
+                }
+                named_bar_sync_128();
+                float my_m = 0.f, my_a = 1.f;
+#pragma unroll
+                for (int r = 0; r < N; ++r) {
+                    const float mo = m_s[r];
+                    const float mn = fmaxf(fmaxf(mo, fmaxf(red[r], red[N + r])), fmaxf(red[2 * N + r], red[3 * N + r]));
+                    const float al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
+                    if (r == tid) {
+                        my_m = mn;
+                        my_a = al;
+                    }
+                }
+                named_bar_sync_128();
+                if (tid < N) {
+                    m_s[tid] = my_m;
+                    a_s[tid] = my_a;
+                }
+                named_bar_sync_128();
+            }
+            // P^T buffer and O^T are free once the previous PV has completed
+            if (j > 0) {
+                if (!group_wait(p_free, (uint32_t)((j - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (need) {
+#pragma unroll 1
+                    for (int c = 0; c <= VC; ++c) {  // the VC O^T chunks, then the row sums
+#pragma unroll
+                        for (int q16 = 0; q16 < N / 16; ++q16) {
+                            uint32_t r16[16];
+                            const uint32_t ta = tmem_o + c * N + lane_base + q16 * 16;
+                            tmem_ld16(ta, r16);
+                            tmem_ld_wait();
+                            reg_fence16(r16);
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * a_s[q16 * 16 + u]);
+                            tmem_st16(ta, r16);
+                        }
+                    }
+                    tmem_st_wait();
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < N; ++r) {
+                const float pv = (s[r] == -INFINITY) ? 0.f : exp2f(s[r] - m_s[r]);
+                const __nv_bfloat16 pb = __float2bfloat16_rn(pv);
+                *reinterpret_cast<__nv_bfloat16*>(pcol + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) = pb;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(p_full);
+        }
+
+        // ---------------------------------------------------------------- epilogue
+        bool have_o = ok && ntiles > 0;
+        if (have_o) {
+            have_o = group_wait(p_free, (uint32_t)((ntiles - 1) & 1));
+            tc_fence_after();
+        }
+        const int64_t part_base = (int64_t)c_split * p.B * T * p.Hq;
+#pragma unroll 1
+        for (int q16 = 0; q16 < N / 16; ++q16) {
+            // row sums of rows q16*16 .. +15 (identical in every lane)
+            uint32_t l16[16];
+            if (have_o) {
+                tmem_ld16(tmem_l + lane_base + q16 * 16, l16);
+                tmem_ld_wait();
+                reg_fence16(l16);
+            } else {
+#pragma unroll
+                for (int u = 0; u < 16; ++u) l16[u] = 0u;
+            }
+            float inv[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int r = q16 * 16 + u;
+                const float tot = u2f(l16[u]);
+                inv[u] = tot > 0.f ? 1.f / tot : 0.f;
+                if (r == tid && r < R) {
+                    const float lse_v = tot > 0.f ? (m_s[r] + log2f(tot)) * kLn2 : -INFINITY;
+                    const int64_t orow = orow_s[r];
+                    if (p.splits == 1) {
+                        if (p.lse) p.lse[orow] = lse_v;
+                    } else {
+                        p.part_lse[part_base + orow] = lse_v;
+                    }
+                }
+            }
+#pragma unroll 1
+            for (int c = 0; c < VC; ++c) {
+                const int d = c * 128 + tid;
+                uint32_t r16[16];
+                if (have_o) {
+                    tmem_ld16(tmem_o + c * N + lane_base + q16 * 16, r16);
+                    tmem_ld_wait();
+                    reg_fence16(r16);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) r16[u] = 0u;
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int r = q16 * 16 + u;
+                    if (r < R) {
+                        const float v = u2f(r16[u]) * inv[u];
+                        const int64_t orow = orow_s[r];
+                        if (p.splits == 1)
+                            reinterpret_cast<__nv_bfloat16*>(p.out)[orow * D + d] = __float2bfloat16_rn(v);
+                        else
+                            p.part_out[(part_base + orow) * D + d] = v;
+                    }
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kProducerWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Lay::kTmemCols);
+    }
+}
+
+// ----------------------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Query heads per CTA: the largest divisor of G whose packed rows fit kMaxRows.
+int choose_gc(int G, int T)
+{
+    for (int gc = G; gc >= 1; --gc)
+        if (G % gc == 0 && gc * T <= kMaxRows) return gc;
+    return 0;
+}
+
+template <int D, int N>
+cudaError_t launch_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                      const TcExtra& x, cudaStream_t stream)
+{
+    using Lay = TcLayout<D, N>;
+    auto kern = tc_attn_kernel<D, N>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.splits, p.Hkv * x.n_rg, p.B);
+    kern<<<grid, kThreads, Lay::kAlloc, stream>>>(tq, tk, tv, p, x);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(int n, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                     const TcExtra& x, cudaStream_t stream)
+{
+    switch (n) {
+    case 16: return launch_dn<D, 16>(tq, tk, tv, p, x, stream);
+    case 32: return launch_dn<D, 32>(tq, tk, tv, p, x, stream);
+    case 48: return launch_dn<D, 48>(tq, tk, tv, p, x, stream);
+    case 64: return launch_dn<D, 64>(tq, tk, tv, p, x, stream);
+    case 80: return launch_dn<D, 80>(tq, tk, tv, p, x, stream);
+    }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+bool tc_supports(const AttnParams& p)
+{
+    if (p.dtype != DFLASH_BF16) return false;
+    if (p.D != 128 && p.D != 256 && p.D != 512) return false;
+    if (p.page_size != 16 && p.page_size != 32 && p.page_size != 64) return false;
+    if (choose_gc(p.G, p.T) == 0) return false;
+    if (p.sh % 8 || p.ss % 8 || p.sp % 8) return false;
+    return true;  // the tensor-map encoder is resolved from the driver at launch
+}
+
+int tc_ctas_per_split(const AttnParams& p)
+{
+    const int gc = choose_gc(p.G, p.T);
+    return gc > 0 ? p.B * p.Hkv * (p.G / gc) : 0;
+}
+
+cudaError_t launch_tc_attn(const AttnParams& p, cudaStream_t stream)
+{
+    if (!tc_supports(p)) return cudaErrorNotSupported;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    TcExtra x;
+    x.Gc = choose_gc(p.G, p.T);
+    x.n_rg = p.G / x.Gc;
+    x.R = x.Gc * p.T;
+    const int n = ((x.R + 15) / 16) * 16;
+
+    CUtensorMap tq, tk, tv;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)p.D, (cuuint64_t)p.Hq, (cuuint64_t)p.B * p.T};
+        const cuuint64_t strides[2] = {(cuuint64_t)p.D * 2, (cuuint64_t)p.Hq * p.D * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)x.Gc, (cuuint32_t)p.T};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.q), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.Hkv, (cuuint64_t)p.page_size,
+                                    (cuuint64_t)p.num_pages};
+        const cuuint64_t strides[3] = {(cuuint64_t)p.sh * 2, (cuuint64_t)p.ss * 2, (cuuint64_t)p.sp * 2};
+        const cuuint32_t box[4] = {64, 1, (cuuint32_t)p.page_size, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p.k), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        if (enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p.v), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e;
+    switch (p.D) {
+    case 128: e = launch_d<128>(n, tq, tk, tv, p, x, stream); break;
+    case 256: e = launch_d<256>(n, tq, tk, tv, p, x, stream); break;
+    case 512: e = launch_d<512>(n, tq, tk, tv, p, x, stream); break;
+    default: e = cudaErrorNotSupported;
+    }
+    if (e != cudaSuccess || p.splits == 1) return e;
+    return launch_combine(p.part_out, p.part_lse, p.splits, (int64_t)p.B * p.T * p.Hq, p.D, p.dtype, p.out, p.lse,
+                          stream);
+}
 
 }  // namespace dflash
