@@ -430,8 +430,8 @@ def main():
 
     tc = (args.kernel == "tc") or (args.kernel == "auto" and case.q.dtype == torch.bfloat16 and
                                    _tc_used(dfl, dims, case, splits_req))
-    kernel_name = "dflash_tc_attn" if tc else "dflash_simt_attn"
-    launches_per_step = 1 if (tc or splits == 1) else 2
+    kernel_name = "tc_attn_kernel" if tc else "simt_attn_kernel"
+    launches_per_step = 1 if splits == 1 else 2  # attention (+ split combine)
     peak, peak_kind = measured_peaks()
     traffic, traffic_note = traffic_from_profiles(kernel_name)
     achieved = kv / (ms_per_step * 1e-3) / 1e9

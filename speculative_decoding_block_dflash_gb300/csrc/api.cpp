@@ -180,8 +180,8 @@ int32_t plan_splits_impl(const dflash_dims* d, int32_t T, int32_t window, int32_
     // Longest union key range any request can have.
     int64_t span = max_len_of(d);
     if (window > 0) span = std::min<int64_t>(span, (int64_t)window + T - 1 + d->page_size);
-    // Keep at least 256 keys per chunk; aim for one wave over the SMs.
-    const int64_t max_by_len = std::max<int64_t>(1, span / 256);
+    // Keep at least 128 keys (one tensor-core tile) per chunk; aim for one wave over the SMs.
+    const int64_t max_by_len = std::max<int64_t>(1, span / 128);
     const int64_t units = work_units(d, T, kernel);
     const int64_t sms = device_sm_count();
     int64_t s = (sms + units - 1) / units;

@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ float m_sh, inv_sh, lse_sh;
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x;
+    // Launched as a programmatic dependent of the attention kernel: wait until
+    // that grid has completed and its partials are visible.
+    cudaGridDependencySynchronize();
 
     // max over chunks
     float m = -INFINITY;
@@ -93,9 +96,17 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, int32_t
                            int32_t D, int32_t out_dtype, void* out, float* lse, cudaStream_t stream)
 {
     if (rows <= 0) return cudaSuccess;
-    combine_kernel<<<dim3((unsigned)rows), kThreads, 0, stream>>>(part_out, part_lse, splits, rows, D,
-                                                                  out_dtype, out, lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, part_out, part_lse, splits, rows, D, out_dtype, out, lse);
 }
 
 }  // namespace dflash

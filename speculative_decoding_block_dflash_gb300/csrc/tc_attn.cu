@@ -12,30 +12,35 @@
 // page), and an fp32 O accumulator of 128 x 512 would fill all 512 TMEM
 // columns. So the kernel computes
 //     S^T [128 keys x N rows]    = K_tile [128 x D] . Q^T [D x N]        (M = 128 keys)
-//     O^T [D x N] (4 chunks)    += V_tile^T [D x 128] . P^T [128 x N]   (M = 128 dims)
-// with N = R rounded up to 16 (<= 80): TMEM holds S^T (N columns) and O^T
-// (D/128 * N columns), 400 columns at D = 512, N = 80.
+//     O^T [D x N] (D/128 chunks) += V_tile^T [D x 128] . P^T [128 x N]  (M = 128 dims)
+//     l   [128 x N]             += ones [128 x 128] . P^T              (row sums, every lane alike)
+// with N = R rounded up to 16 (<= 80): TMEM holds S^T, O^T and l, N * (2 + D/128)
+// columns (480 at D = 512, N = 80).
 //
-// Softmax (thread = one key lane of the tile): scores are masked by select
-// (non-causal rows see every key up to L-1, causal rows keys up to their own
-// position, a window W keeps the last W keys -- vLLM PR #43445 "Allow causal
-// DFlash"), the running row max m is shared by the 128 softmax threads
-// (cross-lane shuffle + shared-memory reduction) and only raised when a score
-// exceeds it by more than 2^8 in the exp2 domain (O^T and the per-thread row
-// sums are then rescaled by exp2(m_old - m_new)); P = exp2(s - m) is rounded
-// to bf16 and written to shared memory as the B operand of the PV MMA. The
-// row sum l is accumulated per key lane from the rounded P and reduced once
-// at the end.
+// Softmax (thread = one key lane of the tile, warps 0-3): S^T is read from TMEM
+// in 16-column groups in rolled loops (the code runs once or twice per SM per
+// call, so it is kept small for the instruction cache). Scores are masked by
+// select (non-causal rows see every key up to L-1, causal rows keys up to their
+// own position, a window W keeps the last W keys -- vLLM PR #43445 "Allow
+// causal DFlash"). The running row max m is shared by the 128 softmax threads
+// and only raised when a score exceeds it by more than 2^8 in the exp2 domain
+// (cross-lane shuffle + shared-memory reduction; O^T and l are then rescaled
+// by exp2(m_old - m_new) in TMEM). P = exp2(s - m) is rounded to bf16 and
+// written to shared memory as the B operand of the PV and row-sum MMAs.
 //
-// Warp roles (192 threads): warps 0-3 softmax + epilogue, warp 4 TMA
-// producer, warp 5 MMA issuer. Ring stages are 16 KB: a K stage is 128 keys x
-// 64 dims (K-major, 128-byte swizzle), a V stage 64 keys x 128 dims
-// (MN-major). One TMA box is one page's tokens of one KV head x 64 dims; the
-// page id comes from the page table (validated; out-of-range ids and pages
-// past the chunk are fetched at an out-of-bounds page coordinate, which the
-// TMA unit fills with zeros without touching memory). V rows of the last,
-// partial page past seq_len are zeroed in shared memory before the PV MMA so
-// garbage there can never reach the output.
+// Warp roles (288 threads): warps 0-3 softmax + epilogue, warps 4-7 TMA
+// producers, warp 8 MMA issuer. One warp's tensor copies are processed in
+// order, so a single producer warp caps a CTA near 26 GB/s with 2 KB boxes;
+// the ring stages are dealt round-robin to the four producer warps (stage i of
+// the sequence to warp i mod 4), each filling whole stages. Ring stages are
+// 16 KB: a K stage is 128 keys x 64 dims (K-major, 128-byte swizzle), a V
+// stage 64 keys x 128 dims (MN-major); per tile the order is K(j) then V(j).
+// One TMA box is one page's tokens of one KV head x 64 dims; the page id comes
+// from the page table (validated; out-of-range ids and pages past the chunk
+// are fetched at an out-of-bounds page coordinate, which the TMA unit fills
+// with zeros without touching memory). V rows of the last, partial page past
+// seq_len are zeroed in shared memory before the PV MMA so garbage there can
+// never reach the output.
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the kernel
 // records DFLASH_DEVERR_TIMEOUT, drains its own TMA copies and MMAs (bounded),
@@ -50,12 +55,13 @@
 namespace dflash {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 288;
+constexpr int kProducerWarp = 4;  // warps 4..7 issue TMA copies
+constexpr int kNumProducers = 4;
+constexpr int kMmaWarp = 8;
 constexpr int kTileKeys = 128;
 constexpr int kStageBytes = 16384;
-constexpr int kMaxPids = 512;
+constexpr int kMaxPids = 128;  // page ids held per producer warp (one window)
 constexpr int kMaxRows = 80;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -80,27 +86,28 @@ template <int D, int N>
 struct TcLayout {
     static constexpr int kFixed = N * D * 2 + N * 128 * 2 + 4096 + kOnesBytes;
     static constexpr int kStagesFit = (227 * 1024 - 1024 - kFixed) / kStageBytes;
-    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
     static constexpr int kQOff = 0;                                  // [D/64][N rows][128 B]
     static constexpr int kRingOff = kQOff + N * D * 2;               // [stages][16 KB]
     static constexpr int kPOff = kRingOff + kStages * kStageBytes;   // [2 key halves][N rows][128 B]
     static constexpr int kOnesOff = kPOff + N * 128 * 2;             // bf16 ones [128 x 16] (row-sum MMA)
     static constexpr int kBarOff = kOnesOff + kOnesBytes;
-    static constexpr int kNumBars = 2 * kStages + 6;
-    static constexpr int kMiscOff = kBarOff + kNumBars * 8;          // tmem base, abort flag
+    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;  // tmem base, abort flag
     static constexpr int kMOff = kMiscOff + 16;                      // float m_s[N]
     static constexpr int kAOff = kMOff + N * 4;                      // float alpha_s[N]
     static constexpr int kRedOff = kAOff + N * 4;                    // float red[4][N]
     static constexpr int kLoOff = kRedOff + 4 * N * 4;               // int lo_s[N]
     static constexpr int kHiOff = kLoOff + N * 4;                    // int hi_s[N]
     static constexpr int kRowOff = kHiOff + N * 4;                   // int64 orow_s[N]
-    static constexpr int kPidOff = kRowOff + N * 8;                  // int pid_s[kMaxPids]
-    static constexpr int kTotal = kPidOff + kMaxPids * 4;
+    static constexpr int kPidOff = kRowOff + N * 8;                  // int pid_s[4][kMaxPids]
+    static constexpr int kTotal = kPidOff + kNumProducers * kMaxPids * 4;
     static constexpr int kAlloc = kTotal + 1024;
     static constexpr int kTmemCols = pow2ceil(N * (2 + D / 128));
     static_assert(kStages >= 3, "ring too shallow");
     static_assert(N * (2 + D / 128) <= 512, "TMEM budget");
     static_assert((N * D * 2) % 1024 == 0 && (N * 128) % 1024 == 0, "1024-byte swizzle atoms");
+    static_assert(kTotal + 1024 <= 227 * 1024, "shared memory budget");
 };
 
 // ----------------------------------------------------------------------------- PTX wrappers
@@ -305,6 +312,28 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, int a_mn, int b_
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
+// 16 consecutive floats of a shared-memory row table into registers (four 16-byte loads).
+__device__ __forceinline__ void load_row16(const float* src, float (&v)[16])
+{
+    const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 t = s4[i];
+        v[4 * i + 0] = t.x;
+        v[4 * i + 1] = t.y;
+        v[4 * i + 2] = t.z;
+        v[4 * i + 3] = t.w;
+    }
+}
+
+// 2^x on the special-function unit (P only needs bf16 accuracy).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ----------------------------------------------------------------------------- kernel
 
 template <int D, int N>
@@ -315,7 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     using Lay = TcLayout<D, N>;
     constexpr int S = Lay::kStages;
     constexpr int KC = D / 64;   // K stages per tile (64-dim chunks)
-    constexpr int VC = D / 128;  // O^T chunks (128-dim), V stages per 64-key half
+    constexpr int VC = D / 128;  // O^T chunks (128 dims); V stages per 64-key half
+    constexpr int NQ = N / 16;   // 16-column groups of S^T / O^T / l
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -327,11 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full = bars;
     uint64_t* empty = bars + S;
     uint64_t* q_full = bars + 2 * S;
-    uint64_t* s_full = q_full + 1;
-    uint64_t* s_free = q_full + 2;
-    uint64_t* p_full = q_full + 3;
-    uint64_t* p_free = q_full + 4;
-    uint64_t* drain = q_full + 5;
+    uint64_t* s_full = q_full + 1;  // MMA -> softmax: S^T of the tile is in TMEM
+    uint64_t* p_full = q_full + 2;  // softmax -> MMA: P^T written (and S^T read)
+    uint64_t* p_free = q_full + 3;  // MMA -> softmax: PV of the tile done (P^T, O^T, l free)
+    uint64_t* drain = q_full + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
     float* m_s = reinterpret_cast<float*>(smem + Lay::kMOff);
@@ -362,156 +391,144 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (len_ok) ch = split_chunk(L, T, p.window, Psz, p.splits, c_split);
     const int t0 = (ch.kb / Psz) * Psz;
     const int ntiles = (ch.kb < ch.ke) ? (ch.ke - t0 + kTileKeys - 1) / kTileKeys : 0;
+    const int pages_per_tile = kTileKeys / Psz;
+    const int chunk_pages = ntiles * pages_per_tile;
+    const int first_page = t0 / Psz;
+
+    // Page ids of relative pages [base, base + kMaxPids) -> this producer warp's pid_w.
+    // Pages past the chunk and invalid ids map to the out-of-bounds coordinate num_pages.
+    const int pw = warp - kProducerWarp;
+    int32_t* pid_w = pid_s + (pw & 3) * kMaxPids;
+    auto load_window = [&](int base) {
+        for (int k = lane; k < kMaxPids; k += 32) {
+            const int pr = base + k;
+            int32_t id = p.num_pages;
+            if (pr < chunk_pages && t0 + pr * Psz < ch.ke) {
+                const int32_t v = __ldg(p.page_table + (int64_t)b * p.max_pages + first_page + pr);
+                if (v >= 0 && v < p.num_pages)
+                    id = v;
+                else
+                    raise_error(p.err, DFLASH_DEVERR_PAGE_ID);
+            }
+            pid_w[k] = id;
+        }
+        __syncwarp();
+    };
 
     // ---------------------------------------------------------------- set-up
     if (tid == 0) {
-        for (int i = 0; i < 2 * S + 6; ++i) {
+        for (int i = 0; i < 2 * S + 5; ++i) {
             uint64_t* bar = bars + i;
-            mbar_init(bar, (bar == s_free || bar == p_full) ? 128u : 1u);
+            mbar_init(bar, bar == p_full ? 128u : 1u);
         }
         *abort_flag = 0;
         if (!len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (tid < N) {
-        int32_t lo = -(1 << 30), hi = (1 << 30);
-        int64_t orow = -1;
-        if (tid < R) {
-            const int i = tid / x.Gc;
-            const int hh = tid - i * x.Gc;
-            const KeyRange kr = row_range(L, T, i, p.causal, p.window);
-            lo = kr.lo;
-            hi = kr.hi;
-            orow = (int64_t)(b * T + i) * p.Hq + (h0 + hh);
-        }
-        lo_s[tid] = lo;
-        hi_s[tid] = hi;
-        orow_s[tid] = orow;
-        m_s[tid] = -INFINITY;
-        a_s[tid] = 1.f;
-    }
-    if (warp == kMmaWarp) {
-        // all-ones A operand of the row-sum MMA (bf16 1.0 = 0x3F80)
+    if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
+        if (ntiles > 0) load_window(0);
+    } else if (warp == kMmaWarp) {
         for (int idx = lane; idx < kOnesBytes / 16; idx += 32)
-            *reinterpret_cast<uint4*>(ones_s + idx * 16) = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+            *reinterpret_cast<uint4*>(ones_s + idx * 16) =
+                make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // bf16 1.0
         fence_proxy_async_smem();
-    }
-    if (warp == kProducerWarp) {
-        // zero the padding rows of Q (TMA writes rows [0, R) of every 64-dim chunk)
-        if (R < N) {
-            for (int idx = lane; idx < KC * (N - R) * 8; idx += 32) {
-                const int kc = idx / ((N - R) * 8);
-                const int rem = idx - kc * (N - R) * 8;
-                const int row = R + rem / 8;
-                const int c16 = rem % 8;
-                *reinterpret_cast<uint4*>(q_s + kc * N * 128 + row * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-        }
         tmem_alloc(tmem_slot, Lay::kTmemCols);
         tmem_relinquish();
+    } else {
+        if (tid < N) {
+            int32_t lo = -(1 << 30), hi = (1 << 30);
+            int64_t orow = -1;
+            if (tid < R) {
+                const int i = tid / x.Gc;
+                const int hh = tid - i * x.Gc;
+                const KeyRange kr = row_range(L, T, i, p.causal, p.window);
+                lo = kr.lo;
+                hi = kr.hi;
+                orow = (int64_t)(b * T + i) * p.Hq + (h0 + hh);
+            }
+            lo_s[tid] = lo;
+            hi_s[tid] = hi;
+            orow_s[tid] = orow;
+            m_s[tid] = -INFINITY;
+            a_s[tid] = 1.f;
+        }
+        // zero the padding rows [R, N) of Q (the TMA writes rows [0, R) of every 64-dim chunk)
+        for (int idx = tid; idx < KC * (N - R) * 8; idx += 128) {
+            const int kc = idx / ((N - R) * 8);
+            const int rem = idx - kc * (N - R) * 8;
+            *reinterpret_cast<uint4*>(q_s + kc * N * 128 + (R + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // let a dependent split-combine grid start launching; it waits for our completion
+    cudaTriggerProgrammaticLaunchCompletion();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_s = tmem;          // S^T: columns [0, N)
-    const uint32_t tmem_o = tmem + N;      // O^T chunk c: columns [N + c*N, N + (c+1)*N)
-    const uint32_t tmem_l = tmem + N + VC * N;  // row sums l (every lane holds all N), N columns
+    const uint32_t tmem_s = tmem;               // S^T: columns [0, N)
+    const uint32_t tmem_o = tmem + N;           // O^T chunk c: columns [N + c*N, N + (c+1)*N)
+    const uint32_t tmem_l = tmem + N + VC * N;  // row sums (the same in every lane): N columns
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ TMA producer
-        const int pages_per_tile = kTileKeys / Psz;
-        const int first_page = t0 / Psz;
-        const int chunk_pages = ntiles * pages_per_tile;
-        int wbase = -kMaxPids;  // window of page ids held in pid_s: relative pages [wbase, wbase + kMaxPids)
-        auto load_window = [&](int base) {
-            for (int rel = lane; rel < kMaxPids; rel += 32) {
-                const int pr = base + rel;
-                int32_t id = p.num_pages;  // out-of-bounds coordinate: zero fill, no memory traffic
-                if (pr < chunk_pages && t0 + pr * Psz < ch.ke) {
-                    const int32_t v = __ldg(p.page_table + (int64_t)b * p.max_pages + first_page + pr);
-                    if (v >= 0 && v < p.num_pages)
-                        id = v;
-                    else
-                        raise_error(p.err, DFLASH_DEVERR_PAGE_ID);
-                }
-                pid_s[rel] = id;
-            }
-            __syncwarp();
-            wbase = base;
-        };
-        auto pid = [&](int rel) -> int32_t { return pid_s[rel - wbase]; };
-
+    if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
+        // ------------------------------------------------------------ TMA producers
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
+        int wbase = 0;
         uint32_t issued_parity[S];
 #pragma unroll
         for (int s = 0; s < S; ++s) issued_parity[s] = 2;  // 2 = nothing outstanding
-        auto acquire = [&]() -> bool {
-            bool got = true;
-            if (lane == 0) got = wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.err);
-            got = __shfl_sync(0xffffffffu, got, 0);
-            return got;
-        };
-        auto advance = [&]() {
-            if (++stage == S) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        };
-
         if (ntiles > 0) {
-            if (lane == 0) {
+            if (pw == 0 && lane == 0) {
                 mbar_expect_tx(q_full, (uint32_t)(R * 128 * KC));
                 for (int kc = 0; kc < KC; ++kc) tma_load_3d(q_s + kc * N * 128, &tm_q, q_full, kc * 64, h0, b * T);
             }
-            for (int job = 0; job <= ntiles && ok; ++job) {
-                // K(job), then V(job - 1)
-                if (job < ntiles) {
-                    const int rel0 = job * pages_per_tile;
-                    const int wneed = job > 0 ? rel0 - pages_per_tile : rel0;
-                    if (rel0 + pages_per_tile > wbase + kMaxPids || wneed < wbase) load_window(wneed);
-                    for (int kc = 0; kc < KC && ok; ++kc) {
-                        ok = acquire();
+            const int box = Psz * 128;  // bytes of one page x 64 dims
+            const int per_tile = KC + 2 * VC;
+            int seq = 0;  // index of the stage in the whole sequence; this warp fills seq = pw (mod 4)
+            for (int j = 0; j < ntiles && ok; ++j) {
+                const int rel0 = j * pages_per_tile;
+                // K(j): KC stages of 128 keys x 64 dims, then V(j): 2 x VC stages of 64 keys x 128 dims
+                for (int st = 0; st < per_tile && ok; ++st, ++seq) {
+                    if ((seq & 3) == pw) {
+                        if (rel0 + pages_per_tile > wbase + kMaxPids) {
+                            wbase = rel0;
+                            load_window(wbase);
+                        }
+                        if (lane == 0) ok = wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.err);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
                         if (!ok) break;
                         if (lane == 0) {
                             uint8_t* dst = ring + stage * kStageBytes;
                             mbar_expect_tx(full + stage, kStageBytes);
-                            for (int pg = 0; pg < pages_per_tile; ++pg)
-                                tma_load_4d(dst + pg * Psz * 128, &tm_k, full + stage, kc * 64, g, 0, pid(rel0 + pg));
+                            if (st < KC) {
+                                for (int pg = 0; pg < pages_per_tile; ++pg)
+                                    tma_load_4d(dst + pg * box, &tm_k, full + stage, st * 64, g, 0,
+                                                pid_w[rel0 + pg - wbase]);
+                            } else {
+                                const int h = (st - KC) / VC, c = (st - KC) % VC;
+                                const int ppg = 64 / Psz;  // pages per 64-key half
+                                for (int pg = 0; pg < ppg; ++pg) {
+                                    const int32_t page = pid_w[rel0 + h * ppg + pg - wbase];
+                                    for (int m = 0; m < 2; ++m)
+                                        tma_load_4d(dst + m * 8192 + pg * box, &tm_v, full + stage, c * 128 + m * 64,
+                                                    g, 0, page);
+                                }
+                            }
                             issued_parity[stage] = phase;
                         }
                         __syncwarp();
-                        advance();
                     }
-                }
-                if (job >= 1 && ok) {
-                    const int jv = job - 1;
-                    const int rel0 = jv * pages_per_tile;
-                    for (int h = 0; h < 2 && ok; ++h) {
-                        for (int c = 0; c < VC && ok; ++c) {
-                            ok = acquire();
-                            if (!ok) break;
-                            if (lane == 0) {
-                                uint8_t* dst = ring + stage * kStageBytes;
-                                mbar_expect_tx(full + stage, kStageBytes);
-                                const int ppg = 64 / Psz;
-                                for (int m = 0; m < 2; ++m)
-                                    for (int pg = 0; pg < ppg; ++pg)
-                                        tma_load_4d(dst + m * 8192 + pg * Psz * 128, &tm_v, full + stage,
-                                                    c * 128 + m * 64, g, 0, pid(rel0 + h * ppg + pg));
-                                issued_parity[stage] = phase;
-                            }
-                            __syncwarp();
-                            advance();
-                        }
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
             }
         }
-        // Drain: make sure no TMA copy of ours is still landing when the CTA exits.
+        // Drain: no TMA copy of ours may still be landing when the CTA exits.
         if (lane == 0 && !ok) {
             for (int s = 0; s < S; ++s) {
                 if (issued_parity[s] > 1) continue;
@@ -522,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc_s = make_idesc(128, N, 0, 0);  // S^T = K . Q^T   (A K-major, B K-major)
+        constexpr uint32_t idesc_s = make_idesc(128, N, 0, 0);  // S^T  = K . Q^T   (A K-major, B K-major)
         constexpr uint32_t idesc_o = make_idesc(128, N, 1, 0);  // O^T += V^T . P^T (A MN-major, B K-major)
         constexpr uint32_t idesc_l = make_idesc(128, N, 0, 0);  // l   += 1 . P^T   (A K-major, B K-major)
         const uint32_t q_addr = smem_u32(q_s);
@@ -535,8 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto wait_lane0 = [&](uint64_t* bar, uint32_t par) -> bool {
             bool got = true;
             if (lane == 0) got = wait_bounded(bar, par, abort_flag, p.err);
-            got = __shfl_sync(0xffffffffu, got, 0);
-            return got;
+            return __shfl_sync(0xffffffffu, got, 0);
         };
         auto advance = [&]() {
             if (++stage == S) {
@@ -544,27 +560,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 phase ^= 1u;
             }
         };
-        // PV of tile jj: O^T[c] += V^T(stage) . P^T(half h)
-        auto issue_pv = [&](int jj) -> bool {
-            if (!wait_lane0(p_full, (uint32_t)(jj & 1))) return false;
+        if (ntiles > 0) {
+            ok = wait_lane0(q_full, 0);
             tc_fence_after();
-            const int tile_key0 = t0 + jj * kTileKeys;
-            for (int h = 0; h < 2; ++h) {
-                for (int c = 0; c < VC; ++c) {
-                    if (!wait_lane0(full + stage, phase)) return false;
+        }
+        for (int j = 0; j < ntiles && ok; ++j) {
+            // S^T = K(j) . Q^T (the softmax of tile j-1 has read S^T: p_full(j-1) was waited for)
+            for (int kc = 0; kc < KC && ok; ++kc) {
+                ok = wait_lane0(full + stage, phase);
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t st = ring_addr + stage * kStageBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma(tmem_s, sw128_desc(st + kk * 32, 16, 1024),
+                               sw128_desc(q_addr + kc * N * 128 + kk * 32, 16, 1024), idesc_s,
+                               (kc > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(empty + stage);
+                }
+                __syncwarp();
+                advance();
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(s_full);
+            __syncwarp();
+            // O^T += V(j)^T . P^T, l += 1 . P^T
+            ok = wait_lane0(p_full, (uint32_t)(j & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const int tile_key0 = t0 + j * kTileKeys;
+            for (int h = 0; h < 2 && ok; ++h) {
+                for (int c = 0; c < VC && ok; ++c) {
+                    ok = wait_lane0(full + stage, phase);
+                    if (!ok) break;
                     tc_fence_after();
-                    // zero V rows past seq_len inside the sequence's last, partial page
+                    // V rows past seq_len in the sequence's last, partial page -> zero
                     const int key0 = tile_key0 + h * 64;
                     const int zlo = L - key0;
                     if (L % Psz != 0 && zlo > 0 && zlo < 64 && ch.ke == L) {
                         const int zhi = min(64, ((L + Psz - 1) / Psz) * Psz - key0);
                         uint8_t* st = ring + stage * kStageBytes;
                         const int rows = zhi - zlo;
-                        for (int idx = lane; idx < rows * 2 * 8; idx += 32) {
+                        for (int idx = lane; idx < rows * 16; idx += 32) {
                             const int m = idx / (rows * 8);
                             const int rem = idx - m * rows * 8;
-                            const int row = zlo + rem / 8;
-                            *reinterpret_cast<uint4*>(st + m * 8192 + row * 128 + (rem % 8) * 16) =
+                            *reinterpret_cast<uint4*>(st + m * 8192 + (zlo + rem / 8) * 128 + (rem % 8) * 16) =
                                 make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
@@ -573,64 +614,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         const uint32_t st = ring_addr + stage * kStageBytes;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = sw128_desc(st + kk * 2048, 8192, 1024);
-                            const uint64_t bdesc = sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024);
-                            tc_mma(tmem_o + c * N, a, bdesc, idesc_o, (jj > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma(tmem_o + c * N, sw128_desc(st + kk * 2048, 8192, 1024),
+                                   sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024), idesc_o,
+                                   (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
                         tc_commit(empty + stage);
                     }
                     __syncwarp();
                     advance();
                 }
-                // l[r] += sum over this half's 64 keys of P^T[key][r]: ones[128 x 16] . P^T
                 if (lane == 0) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = noswz_desc(ones_addr, 2048, 128);
-                        const uint64_t bdesc = sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024);
-                        tc_mma(tmem_l, a, bdesc, idesc_l, (jj > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma(tmem_l, noswz_desc(ones_addr, 2048, 128),
+                               sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024), idesc_l,
+                               (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
                 }
                 __syncwarp();
             }
+            if (!ok) break;
             if (lane == 0) tc_commit(p_free);
             __syncwarp();
-            return true;
-        };
-
-        if (ntiles > 0) {
-            ok = wait_lane0(q_full, 0);
-            tc_fence_after();
-            for (int j = 0; j < ntiles && ok; ++j) {
-                if (j > 0) {
-                    ok = wait_lane0(s_free, (uint32_t)((j - 1) & 1));
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                for (int kc = 0; kc < KC && ok; ++kc) {
-                    ok = wait_lane0(full + stage, phase);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t st = ring_addr + stage * kStageBytes;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a = sw128_desc(st + kk * 32, 16, 1024);
-                            const uint64_t bdesc = sw128_desc(q_addr + kc * N * 128 + kk * 32, 16, 1024);
-                            tc_mma(tmem_s, a, bdesc, idesc_s, (kc > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc_commit(empty + stage);
-                    }
-                    __syncwarp();
-                    advance();
-                }
-                if (!ok) break;
-                if (lane == 0) tc_commit(s_full);
-                __syncwarp();
-                if (j > 0) ok = issue_pv(j - 1);
-            }
-            if (ok) ok = issue_pv(ntiles - 1);
         }
         // Drain our MMAs before TMEM is released.
         if (lane == 0) {
@@ -644,13 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ softmax warps 0-3 (thread = key lane)
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float sl2 = p.scale * kLog2e;
-        bool ok = true;
         const bool plain = (p.causal == 0 && p.window == 0);
         // P^T store address pieces for this key lane (K-major, 128-byte swizzle)
         uint8_t* pcol = p_s + (tid >> 6) * (N * 128);
         const int pchunk = (tid & 63) >> 3;
         const int pbyte = (tid & 7) * 2;
-
+        bool ok = true;
         // One thread waits on the mbarrier; the named barrier makes the outcome
         // uniform across the 128 softmax threads (so none is left at a barrier).
         auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -658,64 +661,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid == 0) got = wait_bounded(bar, parity, abort_flag, p.err);
             return !named_bar_or_128(!got);
         };
+        auto load16 = [&](uint32_t taddr, uint32_t (&r16)[16]) {
+            tmem_ld16(taddr, r16);
+            tmem_ld_wait();
+            reg_fence16(r16);
+        };
+
         for (int j = 0; j < ntiles && ok; ++j) {
             if (!group_wait(s_full, (uint32_t)(j & 1))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float s[N];
-#pragma unroll
-            for (int q16 = 0; q16 < N / 16; ++q16) {
-                uint32_t r16[16];
-                tmem_ld16(tmem_s + lane_base + q16 * 16, r16);
-                tmem_ld_wait();
-                reg_fence16(r16);
-#pragma unroll
-                for (int u = 0; u < 16; ++u) s[q16 * 16 + u] = u2f(r16[u]);
-            }
-            tc_fence_before();
-            mbar_arrive(s_free);
-
             const int key = t0 + j * kTileKeys + tid;
             const bool kvalid = key >= ch.kb && key < ch.ke;
-            bool need = false;
-#pragma unroll
-            for (int r = 0; r < N; ++r) {
+            // masked, log2-scaled score of column col from raw S^T bits
+            auto score = [&](uint32_t raw, int col) -> float {
                 bool vis = kvalid;
-                if (!plain) vis = vis && key >= lo_s[r] && key <= hi_s[r];
-                s[r] = vis ? s[r] * sl2 : -INFINITY;
-                need = need || (s[r] > m_s[r] + kRescaleThresh);
+                if (!plain) vis = vis && key >= lo_s[col] && key <= hi_s[col];
+                return vis ? u2f(raw) * sl2 : -INFINITY;
+            };
+            // pass 1: does any score exceed the running max by more than the threshold?
+            bool need = false;
+#pragma unroll 1
+            for (int q = 0; q < NQ; ++q) {
+                float mv[16];
+                load_row16(m_s + q * 16, mv);
+                uint32_t r16[16];
+                load16(tmem_s + lane_base + q * 16, r16);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) need |= score(r16[u], q * 16 + u) > mv[u] + kRescaleThresh;
             }
             need = named_bar_or_128(need);
             if (need) {
+                // new row maxima: max over the 128 key lanes (shuffles, then across the 4 warps)
+#pragma unroll 1
+                for (int q = 0; q < NQ; ++q) {
+                    uint32_t r16[16];
+                    load16(tmem_s + lane_base + q * 16, r16);
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    float v = s[r];
+                    for (int u = 0; u < 16; ++u) {
+                        float v = score(r16[u], q * 16 + u);
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-                    if ((r & 31) == lane) red[warp * N + r] = v;
-                }
-                named_bar_sync_128();
-                float my_m = 0.f, my_a = 1.f;
-#pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    const float mo = m_s[r];
-                    const float mn = fmaxf(fmaxf(mo, fmaxf(red[r], red[N + r])), fmaxf(red[2 * N + r], red[3 * N + r]));
-                    const float al = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
-                    if (r == tid) {
-                        my_m = mn;
-                        my_a = al;
+                        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+                        if (((q * 16 + u) & 31) == lane) red[warp * N + q * 16 + u] = v;
                     }
                 }
                 named_bar_sync_128();
                 if (tid < N) {
-                    m_s[tid] = my_m;
-                    a_s[tid] = my_a;
+                    const float mo = m_s[tid];
+                    const float mn =
+                        fmaxf(fmaxf(mo, fmaxf(red[tid], red[N + tid])), fmaxf(red[2 * N + tid], red[3 * N + tid]));
+                    m_s[tid] = mn;
+                    a_s[tid] = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
                 }
                 named_bar_sync_128();
             }
-            // P^T buffer and O^T are free once the previous PV has completed
+            // P^T, O^T and l are free once the previous tile's PV has completed
             if (j > 0) {
                 if (!group_wait(p_free, (uint32_t)((j - 1) & 1))) {
                     ok = false;
@@ -724,27 +726,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if (need) {
 #pragma unroll 1
-                    for (int c = 0; c <= VC; ++c) {  // the VC O^T chunks, then the row sums
+                    for (int cq = 0; cq < (VC + 1) * NQ; ++cq) {  // O^T chunks, then the row sums
+                        const int c = cq / NQ, q = cq % NQ;
+                        uint32_t r16[16];
+                        const uint32_t ta = tmem_o + c * N + lane_base + q * 16;
+                        load16(ta, r16);
+                        float av[16];
+                        load_row16(a_s + q * 16, av);
 #pragma unroll
-                        for (int q16 = 0; q16 < N / 16; ++q16) {
-                            uint32_t r16[16];
-                            const uint32_t ta = tmem_o + c * N + lane_base + q16 * 16;
-                            tmem_ld16(ta, r16);
-                            tmem_ld_wait();
-                            reg_fence16(r16);
-#pragma unroll
-                            for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * a_s[q16 * 16 + u]);
-                            tmem_st16(ta, r16);
-                        }
+                        for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * av[u]);
+                        tmem_st16(ta, r16);
                     }
                     tmem_st_wait();
                 }
             }
+            // pass 2: P = exp2(s - m), bf16, into P^T[col][key]
+#pragma unroll 1
+            for (int q = 0; q < NQ; ++q) {
+                // row maxima into registers first: the P^T stores below must not be ordered
+                // against these loads (both are shared-memory accesses the compiler cannot separate)
+                float mv[16];
+                load_row16(m_s + q * 16, mv);
+                uint32_t r16[16];
+                load16(tmem_s + lane_base + q * 16, r16);
+                __nv_bfloat16 pb[16];
 #pragma unroll
-            for (int r = 0; r < N; ++r) {
-                const float pv = (s[r] == -INFINITY) ? 0.f : exp2f(s[r] - m_s[r]);
-                const __nv_bfloat16 pb = __float2bfloat16_rn(pv);
-                *reinterpret_cast<__nv_bfloat16*>(pcol + r * 128 + ((pchunk ^ (r & 7)) << 4) + pbyte) = pb;
+                for (int u = 0; u < 16; ++u) {
+                    const float sc = score(r16[u], q * 16 + u);
+                    pb[u] = __float2bfloat16_rn((sc == -INFINITY) ? 0.f : ex2(sc - mv[u]));
+                }
+                uint8_t* prow = pcol + q * 16 * 128 + pbyte;
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    *reinterpret_cast<__nv_bfloat16*>(prow + u * 128 + ((pchunk ^ (u & 7)) << 4)) = pb[u];
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -758,14 +772,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
         }
         const int64_t part_base = (int64_t)c_split * p.B * T * p.Hq;
+        const bool final_out = (p.splits == 1);
 #pragma unroll 1
-        for (int q16 = 0; q16 < N / 16; ++q16) {
-            // row sums of rows q16*16 .. +15 (identical in every lane)
+        for (int q = 0; q < NQ; ++q) {
             uint32_t l16[16];
             if (have_o) {
-                tmem_ld16(tmem_l + lane_base + q16 * 16, l16);
-                tmem_ld_wait();
-                reg_fence16(l16);
+                load16(tmem_l + lane_base + q * 16, l16);
             } else {
 #pragma unroll
                 for (int u = 0; u < 16; ++u) l16[u] = 0u;
@@ -773,17 +785,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             float inv[16];
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
-                const int r = q16 * 16 + u;
                 const float tot = u2f(l16[u]);
-                inv[u] = tot > 0.f ? 1.f / tot : 0.f;
-                if (r == tid && r < R) {
-                    const float lse_v = tot > 0.f ? (m_s[r] + log2f(tot)) * kLn2 : -INFINITY;
-                    const int64_t orow = orow_s[r];
-                    if (p.splits == 1) {
-                        if (p.lse) p.lse[orow] = lse_v;
-                    } else {
-                        p.part_lse[part_base + orow] = lse_v;
-                    }
+                inv[u] = tot > 0.f ? __frcp_rn(tot) : 0.f;
+            }
+            const int my = tid - q * 16;
+            if (my >= 0 && my < 16 && tid < R) {
+                float tot = 0.f;
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    if (u == my) tot = u2f(l16[u]);
+                const float lse_v = tot > 0.f ? (m_s[tid] + __log2f(tot)) * kLn2 : -INFINITY;
+                if (final_out) {
+                    if (p.lse) p.lse[orow_s[tid]] = lse_v;
+                } else {
+                    p.part_lse[part_base + orow_s[tid]] = lse_v;
                 }
             }
 #pragma unroll 1
@@ -791,24 +806,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int d = c * 128 + tid;
                 uint32_t r16[16];
                 if (have_o) {
-                    tmem_ld16(tmem_o + c * N + lane_base + q16 * 16, r16);
-                    tmem_ld_wait();
-                    reg_fence16(r16);
+                    load16(tmem_o + c * N + lane_base + q * 16, r16);
                 } else {
 #pragma unroll
                     for (int u = 0; u < 16; ++u) r16[u] = 0u;
                 }
+                if (final_out) {
+                    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + d;
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int r = q16 * 16 + u;
-                    if (r < R) {
-                        const float v = u2f(r16[u]) * inv[u];
-                        const int64_t orow = orow_s[r];
-                        if (p.splits == 1)
-                            reinterpret_cast<__nv_bfloat16*>(p.out)[orow * D + d] = __float2bfloat16_rn(v);
-                        else
-                            p.part_out[(part_base + orow) * D + d] = v;
-                    }
+                    for (int u = 0; u < 16; ++u)
+                        if (q * 16 + u < R) o[orow_s[q * 16 + u] * D] = __float2bfloat16_rn(u2f(r16[u]) * inv[u]);
+                } else {
+                    float* o = p.part_out + part_base * D + d;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        if (q * 16 + u < R) o[orow_s[q * 16 + u] * D] = u2f(r16[u]) * inv[u];
                 }
             }
         }
@@ -817,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == kProducerWarp) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, Lay::kTmemCols);
     }

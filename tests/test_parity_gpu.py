@@ -136,6 +136,16 @@ def test_gqa8_head_dims(kernel, D, T):
     check_full(case, out, lse)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("page_size", [8, 32, 64, 128])
+def test_page_sizes(kernel, page_size):
+    case = workloads.make_custom("pages", 2, 9, 16, 2, 256, [900, 2100], page_size=page_size, causal=True,
+                                 window=300, seed=23 + page_size, device="cuda")
+    maybe_skip(case, kernel)
+    out, lse = run(case, kernel=kernel, num_splits=3)
+    check_full(case, out, lse)
+
+
 @pytest.mark.parametrize("T", [1, 2, 33, 64])
 def test_block_len_extremes_simt(T):
     case = workloads.make_custom("blk", 2, T, 4, 1, 64, [T, T + 200], causal=True, seed=13 + T, device="cuda")
