@@ -208,6 +208,37 @@ DFLASH_API const char* dflash_status_string(dflash_status status);
 /* Detail of the last failing call on the calling thread ("" if none). */
 DFLASH_API const char* dflash_last_error_message(void);
 
+/*
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate device memory: code that runs while a CUDA graph is
+ * being captured, inside a custom allocator, or in a runtime that owns all
+ * device memory and forbids cudaMalloc. dflash_block_attn needs a caller-made
+ * workspace whenever it splits the keys; this variant keeps that scratch (the
+ * error word, counters and split partials) in a fixed array of
+ * DFLASH_NOALLOC_SCRATCH_BYTES bytes inside the library's device image,
+ * reserved on each GPU when the library's device code is loaded there and
+ * held until the process exits. It allocates nothing.
+ *
+ * Arguments as in dflash_block_attn, with num_splits (0 = auto), kernel (a
+ * dflash_kernel value) and stream (cudaStream_t or NULL) passed directly.
+ * A plan whose workspace would exceed the array returns DFLASH_ERR_WORKSPACE
+ * (request fewer splits). The first call on a device resolves the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture. Every call clears the error word and
+ * counters on `stream`, then reuses the array, which keeps the last call's
+ * contents: calls that can overlap on the GPU (different streams, or
+ * different host threads on the same device) race on it and must be ordered
+ * by the caller. Device-side check bits land in the array's error word and are
+ * not reported by this entry point (the checks still keep every access in
+ * bounds).
+ */
+#define DFLASH_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+DFLASH_API dflash_status dflash_block_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                                   const int32_t* page_table, const int32_t* seq_lens,
+                                                   const dflash_dims* dims, int32_t block_len, int32_t causal,
+                                                   int32_t window, float scale, void* out, float* lse,
+                                                   int32_t num_splits, int32_t kernel, void* stream);
+
 /* DFLASH_ABI_VERSION of the loaded library. */
 DFLASH_API int32_t dflash_abi_version(void);
 

@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     Opts,
     abi_version,
     block_attn,
+    block_attn_noalloc,
     load_library,
     make_dims,
     plan_splits,

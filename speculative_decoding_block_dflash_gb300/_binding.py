@@ -30,6 +30,7 @@ DEVERR_PAGE_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
 
 EXPORTED = (
     "dflash_block_attn",
+    "dflash_block_attn_noalloc",
     "dflash_split_combine",
     "dflash_plan_splits",
     "dflash_workspace_bytes",
@@ -91,6 +92,8 @@ def load_library(path: Optional[str] = None):
         dims_p, opts_p = ctypes.POINTER(Dims), ctypes.POINTER(Opts)
         lib.dflash_block_attn.restype = ctypes.c_int
         lib.dflash_block_attn.argtypes = [vp, vp, vp, vp, vp, dims_p, i32, i32, i32, f32, vp, vp, opts_p]
+        lib.dflash_block_attn_noalloc.restype = ctypes.c_int
+        lib.dflash_block_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, dims_p, i32, i32, i32, f32, vp, vp, i32, i32, vp]
         lib.dflash_split_combine.restype = ctypes.c_int
         lib.dflash_split_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
         lib.dflash_plan_splits.restype = i32
@@ -221,6 +224,31 @@ def block_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pa
                                seq_lens.data_ptr(), ctypes.byref(dims), int(block_len), int(bool(causal)),
                                int(window), float(scale), out.data_ptr(),
                                lse.data_ptr() if lse is not None else None, ctypes.byref(opts))
+    _check(st)
+    return out, lse
+
+
+def block_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
+                       seq_lens: torch.Tensor, block_len: int, causal: bool = False, window: int = 0,
+                       scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                       lse: Optional[torch.Tensor] = None, num_splits: int = 0, kernel: str = "auto",
+                       max_seq_len: Optional[int] = None, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """dflash_block_attn_noalloc: the same attention with the library's own fixed
+    scratch instead of a workspace, for callers that cannot allocate device memory.
+    out/lse are allocated here only when not given."""
+    lib = load_library()
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    dims = make_dims(q, k_cache, page_table, block_len, max_seq_len)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[2])
+    if out is None:
+        out = torch.empty_like(q)
+    st = lib.dflash_block_attn_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), page_table.data_ptr(),
+                                       seq_lens.data_ptr(), ctypes.byref(dims), int(block_len), int(bool(causal)),
+                                       int(window), float(scale), out.data_ptr(),
+                                       lse.data_ptr() if lse is not None else None, int(num_splits),
+                                       KERNELS[kernel], _stream_handle(stream))
     _check(st)
     return out, lse
 

@@ -91,6 +91,17 @@ int g_sm_count[64] = {0};
 
 }  // namespace
 
+dflash_status report_error(dflash_status s, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
 int device_sm_count()
 {
     int dev = 0;

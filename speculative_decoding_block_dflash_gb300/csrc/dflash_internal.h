@@ -53,4 +53,7 @@ cudaError_t launch_tc_attn(const AttnParams& p, cudaStream_t stream);
 // SM count of the current device (cached per device).
 int device_sm_count();
 
+// Records the text returned by dflash_last_error_message() and returns s.
+dflash_status report_error(dflash_status s, const char* fmt, ...);
+
 }  // namespace dflash
