@@ -91,14 +91,19 @@ typedef enum dflash_dtype {
     DFLASH_FP32 = 1  /* q, k_cache, v_cache, out in float32 */
 } dflash_dtype;
 
-/* Which kernel computes the attention. AUTO picks the tensor-core (tcgen05)
-   kernel for bf16 and the fp32 SIMT kernel for fp32. SIMT forces the CUDA-core
-   kernel (any dtype); TC forces the tensor-core kernel (bf16 only; returns
-   DFLASH_ERR_UNSUPPORTED for shapes it does not cover). */
+/* Which kernel computes the attention. AUTO picks the single-CTA tensor-core
+   (tcgen05) kernel for bf16 where it covers the shape, else the SIMT kernel.
+   SIMT forces the CUDA-core kernel (any dtype). TC forces the single-CTA
+   tensor-core kernel and TC_PAIR the operand-split tensor-core kernel (a
+   2-CTA cluster: one CTA streams K and runs the softmax, the other streams V
+   and accumulates the output); both are bf16 only and return
+   DFLASH_ERR_UNSUPPORTED for shapes they do not cover (head_dim 128/256/512,
+   page size 16/32/64). All kernels compute the same definition. */
 typedef enum dflash_kernel {
     DFLASH_KERNEL_AUTO = 0,
     DFLASH_KERNEL_SIMT = 1,
-    DFLASH_KERNEL_TC = 2
+    DFLASH_KERNEL_TC = 2,
+    DFLASH_KERNEL_TC_PAIR = 3
 } dflash_kernel;
 
 /* Device-side error bits accumulated (bitwise OR) in the workspace error word. */
@@ -172,7 +177,8 @@ DFLASH_API dflash_status dflash_block_attn(const void* q, const void* k_cache, c
  *   partial_out  device, float32 [num_splits, num_rows, head_dim] contiguous.
  *   partial_lse  device, float32 [num_splits, num_rows]; -inf marks an empty chunk.
  *   num_splits   1 .. DFLASH_MAX_SPLITS; num_rows >= 1; head_dim multiple of 4, <= 512.
- *   out          device, [num_rows, head_dim] of out_dtype (written); a row whose
+ *   out          device, [num_rows, head_dim] of out_dtype (written; 16-byte aligned for
+ *                float32, 8-byte aligned for bfloat16); a row whose
  *                chunks are all empty gets zeros.
  *   lse          device, float32 [num_rows] (written) or NULL; -inf for all-empty rows.
  *   stream       cudaStream_t or NULL.

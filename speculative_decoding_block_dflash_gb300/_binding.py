@@ -24,7 +24,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_CHECK, ERR_WORKSPACE 
 # dflash_dtype
 BF16, FP32 = 0, 1
 # dflash_kernel
-KERNELS = {"auto": 0, "simt": 1, "tc": 2}
+KERNELS = {"auto": 0, "simt": 1, "tc": 2, "tc_pair": 3}
 # device error bits
 DEVERR_PAGE_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
 

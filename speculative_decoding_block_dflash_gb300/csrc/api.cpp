@@ -165,8 +165,13 @@ int choose_kernel(const dflash_dims* d, int32_t T, int32_t window, int32_t reque
         if (d->dtype != DFLASH_BF16 || !tc_supports(p)) return -DFLASH_ERR_UNSUPPORTED;
         return DFLASH_KERNEL_TC;
     }
+    if (requested == DFLASH_KERNEL_TC_PAIR) {
+        if (d->dtype != DFLASH_BF16 || !tc_pair_supports(p)) return -DFLASH_ERR_UNSUPPORTED;
+        return DFLASH_KERNEL_TC_PAIR;
+    }
     if (requested != DFLASH_KERNEL_AUTO) return -DFLASH_ERR_INVALID_ARG;
     if (d->dtype == DFLASH_BF16 && tc_supports(p)) return DFLASH_KERNEL_TC;
+    if (d->dtype == DFLASH_BF16 && tc_pair_supports(p)) return DFLASH_KERNEL_TC_PAIR;
     return DFLASH_KERNEL_SIMT;
 }
 
@@ -180,6 +185,14 @@ int64_t work_units(const dflash_dims* d, int32_t T, int kernel)
         p.Hkv = d->num_kv_heads;
         p.G = d->num_q_heads / d->num_kv_heads;
         return tc_ctas_per_split(p);
+    }
+    if (kernel == DFLASH_KERNEL_TC_PAIR) {
+        AttnParams p{};
+        p.B = d->batch;
+        p.T = T;
+        p.Hkv = d->num_kv_heads;
+        p.G = d->num_q_heads / d->num_kv_heads;
+        return tc_pair_ctas_per_split(p);
     }
     return (int64_t)d->batch * d->num_q_heads * ((T + 15) / 16);
 }
@@ -316,9 +329,11 @@ dflash_status dflash_block_attn(const void* q, const void* k_cache, const void* 
     p.dtype = dims->dtype;
 
     cudaStream_t stream = opts ? static_cast<cudaStream_t>(opts->stream) : nullptr;
-    cudaError_t e = (kernel == DFLASH_KERNEL_TC) ? launch_tc_attn(p, stream) : launch_simt_attn(p, stream);
+    cudaError_t e = (kernel == DFLASH_KERNEL_TC)        ? launch_tc_attn(p, stream)
+                    : (kernel == DFLASH_KERNEL_TC_PAIR) ? launch_tc_pair_attn(p, stream)
+                                                        : launch_simt_attn(p, stream);
     if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
-    if (splits > 1 && kernel != DFLASH_KERNEL_TC) {
+    if (splits > 1 && kernel == DFLASH_KERNEL_SIMT) {
         e = launch_combine(p.part_out, p.part_lse, splits, (int64_t)p.B * p.T * p.Hq, p.D, p.dtype, out, lse, stream);
         if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     }
@@ -339,7 +354,8 @@ dflash_status dflash_split_combine(const float* partial_out, const float* partia
         return fail(DFLASH_ERR_INVALID_ARG, "head_dim %d must be a multiple of 4 in [4, 512]", head_dim);
     if (out_dtype != DFLASH_BF16 && out_dtype != DFLASH_FP32)
         return fail(DFLASH_ERR_INVALID_ARG, "out_dtype %d invalid", (int)out_dtype);
-    if (!aligned(partial_out, 16) || !aligned(partial_lse, 4) || !aligned(out, 8) || (lse && !aligned(lse, 4)))
+    if (!aligned(partial_out, 16) || !aligned(partial_lse, 4) || !aligned(out, out_dtype == DFLASH_FP32 ? 16 : 8) ||
+        (lse && !aligned(lse, 4)))
         return fail(DFLASH_ERR_INVALID_ARG, "misaligned pointer");
     cudaError_t e = launch_combine(partial_out, partial_lse, num_splits, num_rows, head_dim, out_dtype, out, lse,
                                    static_cast<cudaStream_t>(stream));

@@ -6,7 +6,9 @@
 //
 // One CTA per output row (query row x head); 128 threads, each owning four
 // consecutive head-dim elements (float4 loads, D <= 512). The chunk weights
-// are computed once per CTA into shared memory.
+// are computed once per CTA into shared memory; the partial rows of all chunks
+// are then loaded eight at a time so the L2 latency is paid once per eight
+// chunks rather than once per chunk.
 #include <cmath>
 
 #include "dflash_device.cuh"
@@ -69,12 +71,29 @@ __global__ void __launch_bounds__(kThreads)
 
     const int d0 = tid * 4;
     if (d0 < D) {
+        // all chunks' loads in flight at once (8 per round), then the weighted sum;
+        // empty chunks carry weight 0 and zero partials
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (inv > 0.f) {
-            for (int c = 0; c < S; ++c) {
+            const float* base = part_out + row * D + d0;
+            const int64_t cstride = rows * D;
+            int c = 0;
+            for (; c + 8 <= S; c += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = __ldg(reinterpret_cast<const float4*>(base + (c + k) * cstride));
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float w = w_s[c + k];
+                    acc.x = fmaf(w, v[k].x, acc.x);
+                    acc.y = fmaf(w, v[k].y, acc.y);
+                    acc.z = fmaf(w, v[k].z, acc.z);
+                    acc.w = fmaf(w, v[k].w, acc.w);
+                }
+            }
+            for (; c < S; ++c) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(base + c * cstride));
                 const float w = w_s[c];
-                if (w == 0.f) continue;
-                const float4 v = *reinterpret_cast<const float4*>(part_out + ((int64_t)c * rows + row) * D + d0);
                 acc.x = fmaf(w, v.x, acc.x);
                 acc.y = fmaf(w, v.y, acc.y);
                 acc.z = fmaf(w, v.z, acc.z);
@@ -82,10 +101,17 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
         const int64_t o = row * D + d0;
-        store_elem(out, o + 0, acc.x * inv, out_dtype);
-        store_elem(out, o + 1, acc.y * inv, out_dtype);
-        store_elem(out, o + 2, acc.z * inv, out_dtype);
-        store_elem(out, o + 3, acc.w * inv, out_dtype);
+        if (out_dtype == DFLASH_BF16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + o) = pk;
+        } else {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + o) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        }
     }
     if (tid == 0 && lse) lse[row] = lse_sh;
 }

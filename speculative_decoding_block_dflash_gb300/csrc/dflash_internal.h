@@ -50,6 +50,11 @@ bool tc_supports(const AttnParams& p);
 int tc_ctas_per_split(const AttnParams& p);  // CTAs per split chunk (B * Hkv * row groups)
 cudaError_t launch_tc_attn(const AttnParams& p, cudaStream_t stream);
 
+// Operand-split tensor-core kernel (2-CTA cluster: one CTA streams K, the other V).
+bool tc_pair_supports(const AttnParams& p);
+int tc_pair_ctas_per_split(const AttnParams& p);  // CTAs per split chunk (2 * B * Hkv * row groups)
+cudaError_t launch_tc_pair_attn(const AttnParams& p, cudaStream_t stream);
+
 // SM count of the current device (cached per device).
 int device_sm_count();
 

@@ -31,10 +31,10 @@ def _built():
     dfl.load_library()
 
 
-def _tc_available(case):
+def _tc_available(case, kernel="tc"):
     dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
     try:
-        dfl.plan_splits(dims, case.block_len, case.window, 0, "tc")
+        dfl.plan_splits(dims, case.block_len, case.window, 0, kernel)
         return True
     except dfl.DflashError:
         return False
@@ -97,11 +97,11 @@ def check_sampled(case, out, lse, per_request=6):
     check_close(lse[idx, hh], ref_l, ta, tr, f"{case.name} sampled lse")
 
 
-KERNELS = ["simt", "tc"]
+KERNELS = ["simt", "tc", "tc_pair"]
 
 
 def maybe_skip(case, kernel):
-    if kernel == "tc" and (case.q.dtype != torch.bfloat16 or not _tc_available(case)):
+    if kernel.startswith("tc") and (case.q.dtype != torch.bfloat16 or not _tc_available(case, kernel)):
         pytest.skip("tensor-core kernel does not cover this case")
 
 
