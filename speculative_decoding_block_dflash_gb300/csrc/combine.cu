@@ -4,11 +4,12 @@
 //   m = max_c lse_c, w_c = exp(lse_c - m), out = sum_c w_c o_c / sum_c w_c,
 //   lse = m + log(sum_c w_c); chunks with lse_c = -inf weigh nothing.
 //
-// One CTA per output row (query row x head); 128 threads, each owning four
-// consecutive head-dim elements (float4 loads, D <= 512). The chunk weights
-// are computed once per CTA into shared memory; the partial rows of all chunks
-// are then loaded eight at a time so the L2 latency is paid once per eight
-// chunks rather than once per chunk.
+// One CTA per output row (query row x head), 512 threads. D/4 threads cover
+// one partial row with float4 loads (D <= 512), so the CTA holds 512 / (D/4)
+// such groups; group g sums the chunks c = g, g + groups, ... and the groups
+// meet in shared memory. The chunk weights are computed once per CTA; each
+// thread keeps eight partial-row loads in flight, so at D = 512 a 32-chunk
+// combine costs one L2 round trip instead of eight.
 #include <cmath>
 
 #include "dflash_device.cuh"
@@ -16,7 +17,7 @@
 namespace dflash {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 512;
 
 __global__ void __launch_bounds__(kThreads)
     combine_kernel(const float* __restrict__ part_out, const float* __restrict__ part_lse, int32_t S,
@@ -26,6 +27,7 @@ __global__ void __launch_bounds__(kThreads)
     __shared__ float w_s[DFLASH_MAX_SPLITS];
     __shared__ float red[kThreads / 32];
     __shared__ float m_sh, inv_sh, lse_sh;
+    __shared__ float4 acc_s[kThreads];
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x;
     // Launched as a programmatic dependent of the attention kernel: wait until
@@ -69,36 +71,43 @@ __global__ void __launch_bounds__(kThreads)
     __syncthreads();
     const float inv = inv_sh;
 
-    const int d0 = tid * 4;
-    if (d0 < D) {
-        // all chunks' loads in flight at once (8 per round), then the weighted sum;
-        // empty chunks carry weight 0 and zero partials
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (inv > 0.f) {
-            const float* base = part_out + row * D + d0;
-            const int64_t cstride = rows * D;
-            int c = 0;
-            for (; c + 8 <= S; c += 8) {
-                float4 v[8];
+    const int lanes = D / 4;              // threads per partial row
+    const int groups = kThreads / lanes;  // chunk groups
+    const int gi = tid / lanes;
+    const int d0 = (tid - gi * lanes) * 4;
+    // empty chunks carry weight 0 and zero partials
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (inv > 0.f && gi < groups) {
+        const float* base = part_out + row * D + d0;
+        const int64_t cstride = rows * D;
+        for (int c0 = gi; c0 < S; c0 += 8 * groups) {
+            float4 v[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = __ldg(reinterpret_cast<const float4*>(base + (c + k) * cstride));
+            for (int k = 0; k < 8; ++k) {
+                const int c = c0 + k * groups;
+                v[k] = c < S ? __ldg(reinterpret_cast<const float4*>(base + c * cstride))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float w = w_s[c + k];
-                    acc.x = fmaf(w, v[k].x, acc.x);
-                    acc.y = fmaf(w, v[k].y, acc.y);
-                    acc.z = fmaf(w, v[k].z, acc.z);
-                    acc.w = fmaf(w, v[k].w, acc.w);
-                }
+            for (int k = 0; k < 8; ++k) {
+                const int c = c0 + k * groups;
+                const float w = c < S ? w_s[c] : 0.f;
+                acc.x = fmaf(w, v[k].x, acc.x);
+                acc.y = fmaf(w, v[k].y, acc.y);
+                acc.z = fmaf(w, v[k].z, acc.z);
+                acc.w = fmaf(w, v[k].w, acc.w);
             }
-            for (; c < S; ++c) {
-                const float4 v = __ldg(reinterpret_cast<const float4*>(base + c * cstride));
-                const float w = w_s[c];
-                acc.x = fmaf(w, v.x, acc.x);
-                acc.y = fmaf(w, v.y, acc.y);
-                acc.z = fmaf(w, v.z, acc.z);
-                acc.w = fmaf(w, v.w, acc.w);
-            }
+        }
+    }
+    acc_s[tid] = acc;
+    __syncthreads();
+    if (tid < lanes) {
+        for (int g = 1; g < groups; ++g) {
+            const float4 o = acc_s[g * lanes + tid];
+            acc.x += o.x;
+            acc.y += o.y;
+            acc.z += o.z;
+            acc.w += o.w;
         }
         const int64_t o = row * D + d0;
         if (out_dtype == DFLASH_BF16) {

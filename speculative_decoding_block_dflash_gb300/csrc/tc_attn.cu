@@ -11,36 +11,49 @@
 // Transposed formulation. head_dim reaches 512 ("head_size <= 512", same
 // page), and an fp32 O accumulator of 128 x 512 would fill all 512 TMEM
 // columns. So the kernel computes
-//     S^T [128 keys x N rows]    = K_tile [128 x D] . Q^T [D x N]        (M = 128 keys)
+//     S^T [128 keys x N rows]     = K_tile [128 x D] . Q^T [D x N]        (M = 128 keys)
 //     O^T [D x N] (D/128 chunks) += V_tile^T [D x 128] . P^T [128 x N]  (M = 128 dims)
-//     l   [128 x N]             += ones [128 x 128] . P^T              (row sums, every lane alike)
-// with N = R rounded up to 16 (<= 80): TMEM holds S^T, O^T and l, N * (2 + D/128)
-// columns (480 at D = 512, N = 80).
+//     l^T [128 x 16]             += P [128 rows x 128] . ones [128 x 16] (lane r = row r's sum)
+// with N = R rounded up to 16 (<= 80). The row-sum MMA reads P as a 128-row
+// operand (rows >= N only feed unused lanes), so l takes 16 TMEM columns and
+// S^T fits twice: TMEM holds two S^T buffers, O^T and l^T, 2N + (D/128) N + 16
+// columns (496 at D = 512, N = 80).
+//
+// Pipeline. The ring is filled in the order the MMA warp consumes it, K(0) K(1)
+// V(0) K(2) V(1) ... V(n-1): S(j+1) is computed into the other S^T buffer while
+// the softmax of tile j runs, and the TMA copies only wait for a softmax when
+// the ring is full of V(j) stages.
 //
 // Softmax (thread = one key lane of the tile, warps 0-3): S^T is read from TMEM
-// in 16-column groups in rolled loops (the code runs once or twice per SM per
-// call, so it is kept small for the instruction cache). Scores are masked by
-// select (non-causal rows see every key up to L-1, causal rows keys up to their
-// own position, a window W keeps the last W keys -- vLLM PR #43445 "Allow
-// causal DFlash"). The running row max m is shared by the 128 softmax threads
-// and only raised when a score exceeds it by more than 2^8 in the exp2 domain
-// (cross-lane shuffle + shared-memory reduction; O^T and l are then rescaled
-// by exp2(m_old - m_new) in TMEM). P = exp2(s - m) is rounded to bf16 and
-// written to shared memory as the B operand of the PV and row-sum MMAs.
+// in 16-column groups in rolled loops; this code runs once or twice per SM per
+// call, so it is kept small, and a dry run over fully masked scores executes it
+// once while the first K tile is still in flight so that the first real tile
+// does not stall on instruction fetches. Scores are masked by select
+// (non-causal rows see every key up to L-1, causal rows keys up to their own
+// position, a window W keeps the last W keys -- vLLM PR #43445 "Allow causal
+// DFlash"). The running row max m is shared by the 128 softmax threads and only
+// raised when a score exceeds it by more than 2^8 in the exp2 domain (a
+// transposing shuffle reduction leaves each lane with one column's maximum over
+// its warp, then the four warps meet in shared memory; O^T and l^T are then
+// rescaled by exp2(m_old - m_new) in TMEM). P = exp2(s - m) is rounded to bf16
+// and written to shared memory as the operand of the PV and row-sum MMAs.
 //
-// Warp roles (288 threads): warps 0-3 softmax + epilogue, warps 4-7 TMA
-// producers, warp 8 MMA issuer. One warp's tensor copies are processed in
-// order, so a single producer warp caps a CTA near 26 GB/s with 2 KB boxes;
-// the ring stages are dealt round-robin to the four producer warps (stage i of
-// the sequence to warp i mod 4), each filling whole stages. Ring stages are
-// 16 KB: a K stage is 128 keys x 64 dims (K-major, 128-byte swizzle), a V
-// stage 64 keys x 128 dims (MN-major); per tile the order is K(j) then V(j).
-// One TMA box is one page's tokens of one KV head x 64 dims; the page id comes
-// from the page table (validated; out-of-range ids and pages past the chunk
-// are fetched at an out-of-bounds page coordinate, which the TMA unit fills
-// with zeros without touching memory). V rows of the last, partial page past
-// seq_len are zeroed in shared memory before the PV MMA so garbage there can
-// never reach the output.
+// Warp roles (288 threads): warps 0-3 softmax, warps 4-7 TMA producers, warp 8
+// MMA issuer; warps 0-7 share the epilogue. One warp's tensor copies are
+// processed in order, so a single producer warp caps a CTA near 26 GB/s with
+// 2 KB boxes; the ring stages are dealt round-robin to the four producer warps
+// (stage i of the sequence to warp i mod 4), each filling whole stages. Ring
+// stages are 16 KB: a K stage is 128 keys x 64 dims (K-major, 128-byte
+// swizzle), a V stage 64 keys x 128 dims (MN-major). One TMA box is one page's
+// tokens of one KV head x 64 dims; the page id comes from the page table
+// (validated; out-of-range ids and pages past the chunk are fetched at an
+// out-of-bounds page coordinate, which the TMA unit fills with zeros without
+// touching memory). V rows of the last, partial page past seq_len are zeroed in
+// shared memory before the PV MMA so garbage there can never reach the output.
+//
+// Epilogue: the output tile is normalised by 1/l, assembled row-major in the
+// freed Q / P / ring shared memory by eight warps and written with bulk
+// asynchronous copies, one per block position (its Gc head rows are contiguous).
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the kernel
 // records DFLASH_DEVERR_TIMEOUT, drains its own TMA copies and MMAs (bounded),
@@ -89,30 +102,71 @@ struct TcLayout {
     static constexpr int kFixed = N * D * 2 + N * 128 * 2 + 4096 + kOnesBytes;
     static constexpr int kStagesFit = (227 * 1024 - 1024 - kFixed) / kStageBytes;
     static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
-    static constexpr int kQOff = 0;                                  // [D/64][N rows][128 B]
-    static constexpr int kRingOff = kQOff + N * D * 2;               // [stages][16 KB]
-    static constexpr int kPOff = kRingOff + kStages * kStageBytes;   // [2 key halves][N rows][128 B]
-    static constexpr int kOnesOff = kPOff + N * 128 * 2;             // bf16 ones [128 x 16] (row-sum MMA)
+    static constexpr int kQOff = 0;                                     // [D/64][N rows][128 B]
+    static constexpr int kPOff = kQOff + N * D * 2;                     // [2 key halves][N rows][128 B]
+    static constexpr int kRingOff = kPOff + N * 128 * 2;                // [stages][16 KB]
+    static constexpr int kOnesOff = kRingOff + kStages * kStageBytes;   // bf16 ones [16 x 64] (row-sum MMA)
     static constexpr int kBarOff = kOnesOff + kOnesBytes;
-    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kNumBars = 2 * kStages + 6;
     static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;  // tmem base, abort flag
-    static constexpr int kMOff = kMiscOff + 16;                      // float m_s[N]
-    static constexpr int kAOff = kMOff + N * 4;                      // float alpha_s[N]
-    static constexpr int kRedOff = kAOff + N * 4;                    // float red[4][N]
-    static constexpr int kLoOff = kRedOff + 4 * N * 4;               // int lo_s[N]
-    static constexpr int kHiOff = kLoOff + N * 4;                    // int hi_s[N]
-    static constexpr int kRowOff = kHiOff + N * 4;                   // int64 orow_s[N]
-    static constexpr int kPidOff = kRowOff + N * 8;                  // int pid_s[4][kMaxPids]
+    static constexpr int kMOff = kMiscOff + 16;                         // float m_s[N]
+    static constexpr int kAOff = kMOff + N * 4;                         // float alpha_s[N] (1/l at the end)
+    static constexpr int kRedOff = kAOff + N * 4;                       // float red[4][N]
+    static constexpr int kLoOff = kRedOff + 4 * N * 4;                  // int lo_s[N]
+    static constexpr int kHiOff = kLoOff + N * 4;                       // int hi_s[N]
+    static constexpr int kRowOff = kHiOff + N * 4;                      // int64 orow_s[N]
+    static constexpr int kPidOff = kRowOff + N * 8;                     // int pid_s[4][kMaxPids]
     static constexpr int kTotal = kPidOff + kNumProducers * kMaxPids * 4;
     static constexpr int kAlloc = kTotal + 1024;
-    static constexpr int kTmemCols = pow2ceil(N * (2 + D / 128));
+    static constexpr int kTmemUsed = 2 * N + (D / 128) * N + 16;        // S^T x 2, O^T, l^T
+    static constexpr int kTmemCols = pow2ceil(kTmemUsed);
     static_assert(kStages >= 3, "ring too shallow");
-    static_assert(N * (2 + D / 128) <= 512, "TMEM budget");
+    static_assert(kOnesOff - kQOff >= N * D * 4, "output tile staging (Q, P and the ring)");
+    static_assert(kPOff + N * 128 + 128 * 128 <= kOnesOff, "128-row P operand of the row-sum MMA");
+    static_assert(kTmemUsed <= 512, "TMEM budget");
     static_assert((N * D * 2) % 1024 == 0 && (N * 128) % 1024 == 0, "1024-byte swizzle atoms");
     static_assert(kTotal + 1024 <= 227 * 1024, "shared memory budget");
 };
 
 // ----------------------------------------------------------------------------- kernel
+
+// Column maxima over a warp: v holds 16 consecutive columns of this lane's row.
+// Each step swaps half of the live columns with the partner lane and keeps the
+// maximum of the half it owns; after four steps lane l holds the maximum over
+// its 16-lane half of column l mod 16, and one exchange across the halves
+// completes it: 16 shuffles for 16 columns instead of 80 (one butterfly each).
+__device__ __forceinline__ float transpose_max16(float (&v)[16], int lane)
+{
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+        }
+    }
+    return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 16));
+}
+
+// The k-th unit (0 <= k < 2n) of the ring sequence K(0) K(1) V(0) K(2) V(1) ...
+// K(n-1) V(n-2) V(n-1): whether it is a K tile, and which tile. K(j+1) is loaded
+// ahead of V(j) so S(j+1) can be computed while the softmax of tile j runs.
+__device__ __forceinline__ void ring_unit(int k, int n, bool& is_k, int& tile)
+{
+    if (k == 0) {
+        is_k = true;
+        tile = 0;
+    } else if (k & 1) {
+        const int m = (k + 1) >> 1;
+        is_k = m < n;
+        tile = is_k ? m : n - 1;
+    } else {
+        is_k = false;
+        tile = (k - 2) >> 1;
+    }
+}
 
 template <int D, int N>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -123,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int S = Lay::kStages;
     constexpr int KC = D / 64;   // K stages per tile (64-dim chunks)
     constexpr int VC = D / 128;  // O^T chunks (128 dims); V stages per 64-key half
-    constexpr int NQ = N / 16;   // 16-column groups of S^T / O^T / l
+    constexpr int NQ = N / 16;   // 16-column groups of S^T / O^T
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -135,10 +189,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full = bars;
     uint64_t* empty = bars + S;
     uint64_t* q_full = bars + 2 * S;
-    uint64_t* s_full = q_full + 1;  // MMA -> softmax: S^T of the tile is in TMEM
-    uint64_t* p_full = q_full + 2;  // softmax -> MMA: P^T written (and S^T read)
-    uint64_t* p_free = q_full + 3;  // MMA -> softmax: PV of the tile done (P^T, O^T, l free)
-    uint64_t* drain = q_full + 4;
+    uint64_t* s_full = q_full + 1;  // [2] MMA -> softmax: S^T of the tile is in TMEM buffer j mod 2
+    uint64_t* p_full = q_full + 3;  // softmax -> MMA: P^T written and S^T buffer read
+    uint64_t* p_free = q_full + 4;  // MMA -> softmax: PV of the tile done (P^T, O^T and l free)
+    uint64_t* drain = q_full + 5;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
     float* m_s = reinterpret_cast<float*>(smem + Lay::kMOff);
@@ -195,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------------- set-up
     if (tid == 0) {
-        for (int i = 0; i < 2 * S + 5; ++i) {
+        for (int i = 0; i < Lay::kNumBars; ++i) {
             uint64_t* bar = bars + i;
             mbar_init(bar, bar == p_full ? 128u : 1u);
         }
@@ -245,9 +299,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // let a dependent split-combine grid start launching; it waits for our completion
     cudaTriggerProgrammaticLaunchCompletion();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_s = tmem;               // S^T: columns [0, N)
-    const uint32_t tmem_o = tmem + N;           // O^T chunk c: columns [N + c*N, N + (c+1)*N)
-    const uint32_t tmem_l = tmem + N + VC * N;  // row sums (the same in every lane): N columns
+    const uint32_t tmem_s = tmem;                   // S^T buffers: columns [0, N) and [N, 2N)
+    const uint32_t tmem_o = tmem + 2 * N;           // O^T chunk c: columns [2N + cN, 2N + (c+1)N)
+    const uint32_t tmem_l = tmem + 2 * N + VC * N;  // l^T: lane r holds row r's sum (16 equal columns)
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    bool role_ok = true;
+
+    auto load16 = [&](uint32_t taddr, uint32_t (&r16)[16]) {
+        tmem_ld16(taddr, r16);
+        tmem_ld_wait();
+        reg_fence16(r16);
+    };
 
     if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
         // ------------------------------------------------------------ TMA producers
@@ -264,15 +326,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kc = 0; kc < KC; ++kc) tma_load_3d(q_s + kc * N * 128, &tm_q, q_full, kc * 64, h0, b * T);
             }
             const int box = Psz * 128;  // bytes of one page x 64 dims
-            const int per_tile = KC + 2 * VC;
-            int seq = 0;  // index of the stage in the whole sequence; this warp fills seq = pw (mod 4)
-            for (int j = 0; j < ntiles && ok; ++j) {
-                const int rel0 = j * pages_per_tile;
-                // K(j): KC stages of 128 keys x 64 dims, then V(j): 2 x VC stages of 64 keys x 128 dims
-                for (int st = 0; st < per_tile && ok; ++st, ++seq) {
+            int seq = 0;                // index of the stage in the whole sequence; this warp fills seq = pw (mod 4)
+            for (int k = 0; k < 2 * ntiles && ok; ++k) {
+                bool is_k;
+                int tile;
+                ring_unit(k, ntiles, is_k, tile);
+                const int rel0 = tile * pages_per_tile;
+                const int n_st = is_k ? KC : 2 * VC;
+                // K: KC stages of 128 keys x 64 dims; V: 2 x VC stages of 64 keys x 128 dims
+                for (int sq = 0; sq < n_st && ok; ++sq, ++seq) {
                     if ((seq & 3) == pw) {
-                        if (rel0 + pages_per_tile > wbase + kMaxPids) {
-                            wbase = rel0;
+                        if (rel0 < wbase || rel0 + pages_per_tile > wbase + kMaxPids) {
+                            wbase = (tile > 0 ? tile - 1 : 0) * pages_per_tile;
                             load_window(wbase);
                         }
                         if (lane == 0) ok = wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.err);
@@ -281,12 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0) {
                             uint8_t* dst = ring + stage * kStageBytes;
                             mbar_expect_tx(full + stage, kStageBytes);
-                            if (st < KC) {
+                            if (is_k) {
                                 for (int pg = 0; pg < pages_per_tile; ++pg)
-                                    tma_load_4d(dst + pg * box, &tm_k, full + stage, st * 64, g, 0,
+                                    tma_load_4d(dst + pg * box, &tm_k, full + stage, sq * 64, g, 0,
                                                 pid_w[rel0 + pg - wbase]);
                             } else {
-                                const int h = (st - KC) / VC, c = (st - KC) % VC;
+                                const int h = sq / VC, c = sq % VC;
                                 const int ppg = 64 / Psz;  // pages per 64-key half
                                 for (int pg = 0; pg < ppg; ++pg) {
                                     const int32_t page = pid_w[rel0 + h * ppg + pg - wbase];
@@ -306,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        // Drain: no TMA copy of ours may still be landing when the CTA exits.
+        // Drain: no TMA copy of ours may still be landing when the ring is reused or the CTA exits.
         if (lane == 0 && !ok) {
             for (int s = 0; s < S; ++s) {
                 if (issued_parity[s] > 1) continue;
@@ -315,11 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        __syncwarp();
+        role_ok = ok;
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc_s = make_idesc(128, N, 0, 0);  // S^T  = K . Q^T   (A K-major, B K-major)
-        constexpr uint32_t idesc_o = make_idesc(128, N, 1, 0);  // O^T += V^T . P^T (A MN-major, B K-major)
-        constexpr uint32_t idesc_l = make_idesc(128, N, 0, 0);  // l   += 1 . P^T   (A K-major, B K-major)
+        constexpr uint32_t idesc_s = make_idesc(128, N, 0, 0);   // S^T  = K . Q^T   (A K-major, B K-major)
+        constexpr uint32_t idesc_o = make_idesc(128, N, 1, 0);   // O^T += V^T . P^T (A MN-major, B K-major)
+        constexpr uint32_t idesc_l = make_idesc(128, 16, 0, 0);  // l^T += P . 1     (A K-major, B K-major)
         const uint32_t q_addr = smem_u32(q_s);
         const uint32_t p_addr = smem_u32(p_s);
         const uint32_t ring_addr = smem_u32(ring);
@@ -342,28 +409,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_lane0(q_full, 0);
             tc_fence_after();
         }
-        for (int j = 0; j < ntiles && ok; ++j) {
-            // S^T = K(j) . Q^T (the softmax of tile j-1 has read S^T: p_full(j-1) was waited for)
-            for (int kc = 0; kc < KC && ok; ++kc) {
-                ok = wait_lane0(full + stage, phase);
-                if (!ok) break;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t st = ring_addr + stage * kStageBytes;
+        for (int k = 0; k < 2 * ntiles && ok; ++k) {
+            bool is_k;
+            int j;
+            ring_unit(k, ntiles, is_k, j);
+            if (is_k) {
+                // S^T(j) = K(j) . Q^T into buffer j mod 2, whose previous tile j - 2 the
+                // softmax has finished with (its p_full was waited for by the V(j-2) unit)
+                const uint32_t sb = tmem_s + (uint32_t)(j & 1) * N;
+                for (int kc = 0; kc < KC && ok; ++kc) {
+                    ok = wait_lane0(full + stage, phase);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t st = ring_addr + stage * kStageBytes;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc_mma(tmem_s, sw128_desc(st + kk * 32, 16, 1024),
-                               sw128_desc(q_addr + kc * N * 128 + kk * 32, 16, 1024), idesc_s,
-                               (kc > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(empty + stage);
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc_mma(sb, sw128_desc(st + kk * 32, 16, 1024),
+                                   sw128_desc(q_addr + kc * N * 128 + kk * 32, 16, 1024), idesc_s,
+                                   (kc > 0 || kk > 0) ? 1u : 0u);
+                        tc_commit(empty + stage);
+                    }
+                    __syncwarp();
+                    advance();
                 }
+                if (!ok) break;
+                if (lane == 0) tc_commit(s_full + (j & 1));
                 __syncwarp();
-                advance();
+                continue;
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(s_full);
-            __syncwarp();
-            // O^T += V(j)^T . P^T, l += 1 . P^T
+            // O^T += V(j)^T . P^T and l^T += P . 1 once the softmax has written P(j)
             ok = wait_lane0(p_full, (uint32_t)(j & 1));
             if (!ok) break;
             tc_fence_after();
@@ -401,11 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     advance();
                 }
+                // Row sums: P read as a 128-row A operand (rows >= N fall on the next shared
+                // memory region and only produce unused TMEM lanes) times a 64 x 16 block of ones.
                 if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma(tmem_l, noswz_desc(ones_addr, 2048, 128),
-                               sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024), idesc_l,
+                        tc_mma(tmem_l, sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024),
+                               sw128_desc(ones_addr + kk * 32, 16, 1024), idesc_l,
                                (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
                 }
                 __syncwarp();
@@ -424,7 +501,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warps 0-3 (thread = key lane)
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const float sl2 = p.scale * kLog2e;
         const bool plain = (p.causal == 0 && p.window == 0);
         // P^T store address pieces for this key lane (K-major, 128-byte swizzle)
@@ -439,20 +515,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tid == 0) got = wait_bounded(bar, parity, abort_flag, p.err);
             return !named_bar_or_128(!got);
         };
-        auto load16 = [&](uint32_t taddr, uint32_t (&r16)[16]) {
-            tmem_ld16(taddr, r16);
-            tmem_ld_wait();
-            reg_fence16(r16);
-        };
 
-        for (int j = 0; j < ntiles && ok; ++j) {
-            if (!group_wait(s_full, (uint32_t)(j & 1))) {
-                ok = false;
-                break;
+        // Iteration j = -1 is a dry run over fully masked scores while the first K tile is
+        // in flight: it executes the instructions of a real tile, the row-max path
+        // included, without touching a barrier, so the first real tile does not wait on
+        // instruction fetches from a memory system busy with K/V traffic. It reads the
+        // O^T columns (not written before p_full) and leaves zeros in P^T (not read before
+        // p_full), m = -inf and alpha = 0.
+        for (int j = (ntiles > 0 ? -1 : 0); j < ntiles && ok; ++j) {
+            const bool dry = j < 0;
+            const uint32_t sb = (dry ? tmem_o : tmem_s + (uint32_t)(j & 1) * N) + lane_base;
+            if (!dry) {
+                if (!group_wait(s_full + (j & 1), (uint32_t)((j >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
             }
-            tc_fence_after();
             const int key = t0 + j * kTileKeys + tid;
-            const bool kvalid = key >= ch.kb && key < ch.ke;
+            const bool kvalid = !dry && key >= ch.kb && key < ch.ke;
             // masked, log2-scaled score of column col from raw S^T bits
             auto score = [&](uint32_t raw, int col) -> float {
                 bool vis = kvalid;
@@ -466,24 +547,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float mv[16];
                 load_row16(m_s + q * 16, mv);
                 uint32_t r16[16];
-                load16(tmem_s + lane_base + q * 16, r16);
+                load16(sb + q * 16, r16);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) need |= score(r16[u], q * 16 + u) > mv[u] + kRescaleThresh;
             }
-            need = named_bar_or_128(need);
+            need = named_bar_or_128(need || dry);
             if (need) {
-                // new row maxima: max over the 128 key lanes (shuffles, then across the 4 warps)
+                // new row maxima: each warp's column maxima (transposing shuffle reduction,
+                // one column per lane), then the maximum over the 4 warps
 #pragma unroll 1
                 for (int q = 0; q < NQ; ++q) {
                     uint32_t r16[16];
-                    load16(tmem_s + lane_base + q * 16, r16);
+                    load16(sb + q * 16, r16);
+                    float v[16];
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        float v = score(r16[u], q * 16 + u);
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-                        if (((q * 16 + u) & 31) == lane) red[warp * N + q * 16 + u] = v;
-                    }
+                    for (int u = 0; u < 16; ++u) v[u] = score(r16[u], q * 16 + u);
+                    const float mx = transpose_max16(v, lane);
+                    if (lane < 16) red[warp * N + q * 16 + lane] = mx;
                 }
                 named_bar_sync_128();
                 if (tid < N) {
@@ -504,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if (need) {
 #pragma unroll 1
-                    for (int cq = 0; cq < (VC + 1) * NQ; ++cq) {  // O^T chunks, then the row sums
+                    for (int cq = 0; cq < VC * NQ; ++cq) {
                         const int c = cq / NQ, q = cq % NQ;
                         uint32_t r16[16];
                         const uint32_t ta = tmem_o + c * N + lane_base + q * 16;
@@ -514,6 +594,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * av[u]);
                         tmem_st16(ta, r16);
+                    }
+                    {
+                        // l^T: this thread's lane is row tid
+                        uint32_t r16[16];
+                        load16(tmem_l + lane_base, r16);
+                        const float a = tid < N ? a_s[tid] : 1.f;
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * a);
+                        tmem_st16(tmem_l + lane_base, r16);
                     }
                     tmem_st_wait();
                 }
@@ -526,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float mv[16];
                 load_row16(m_s + q * 16, mv);
                 uint32_t r16[16];
-                load16(tmem_s + lane_base + q * 16, r16);
+                load16(sb + q * 16, r16);
                 __nv_bfloat16 pb[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
@@ -538,46 +627,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = 0; u < 16; ++u)
                     *reinterpret_cast<__nv_bfloat16*>(prow + u * 128 + ((pchunk ^ (u & 7)) << 4)) = pb[u];
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(p_full);
+            if (!dry) {
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(p_full);
+            }
         }
+        bool good = ok && ntiles > 0;
+        if (good) good = group_wait(p_free, (uint32_t)((ntiles - 1) & 1));
+        role_ok = good;
+    }
 
-        // ---------------------------------------------------------------- epilogue
-        bool have_o = ok && ntiles > 0;
-        if (have_o) {
-            have_o = group_wait(p_free, (uint32_t)((ntiles - 1) & 1));
-            tc_fence_after();
-        }
+    // ---------------------------------------------------------------- epilogue (warps 0-7)
+    // Softmax warps 0-3 and the producer warps 4-7 (idle by now) share the read-out: TMEM
+    // lanes 32 (w mod 4) .. +31 are open to warp w, so warps w and w + 4 take alternate
+    // 128-dim chunks of O^T. The output tile (R rows x D, bf16 for the final output,
+    // fp32 for a split's partial) is assembled row-major over Q, P and the ring (all
+    // free once the last PV has completed) and written with bulk asynchronous copies:
+    // for each block position i the Gc heads' rows are contiguous in global memory.
+    if (warp < 8) {
+        const bool have_o = !named_bar_or_256(!role_ok) && ntiles > 0;
+        tc_fence_after();
         const int64_t part_base = (int64_t)c_split * p.B * T * p.Hq;
         const bool final_out = (p.splits == 1);
-        __nv_bfloat16* __restrict__ out_bf = reinterpret_cast<__nv_bfloat16*>(p.out);
-        float* __restrict__ part_out = p.part_out;
-#pragma unroll 1
-        for (int q = 0; q < NQ; ++q) {
-            // output row offsets of these 16 columns into registers before any global store
-            int64_t orow[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) orow[u] = orow_s[q * 16 + u];
+        if (warp < 4) {
+            // row tid's sum sits in TMEM lane tid of l^T
             uint32_t l16[16];
             if (have_o) {
-                load16(tmem_l + lane_base + q * 16, l16);
+                load16(tmem_l + lane_base, l16);
             } else {
 #pragma unroll
                 for (int u = 0; u < 16; ++u) l16[u] = 0u;
             }
-            float inv[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const float tot = u2f(l16[u]);
-                inv[u] = tot > 0.f ? __frcp_rn(tot) : 0.f;
-            }
-            const int my = tid - q * 16;
-            if (my >= 0 && my < 16 && tid < R) {
-                float tot = 0.f;
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    if (u == my) tot = u2f(l16[u]);
+            const float tot = u2f(l16[0]);
+            if (tid < N) a_s[tid] = tot > 0.f ? 1.f / tot : 0.f;
+            if (tid < R) {
                 const float lse_v = tot > 0.f ? (m_s[tid] + __log2f(tot)) * kLn2 : -INFINITY;
                 if (final_out) {
                     if (p.lse) p.lse[orow_s[tid]] = lse_v;
@@ -585,9 +669,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.part_lse[part_base + orow_s[tid]] = lse_v;
                 }
             }
+        }
+        named_bar_sync_256();
+        uint8_t* tile_o = smem + Lay::kQOff;
+        float* tile_f = reinterpret_cast<float*>(tile_o);
+        __nv_bfloat16* tile_b = reinterpret_cast<__nv_bfloat16*>(tile_o);
+        const int dl = (warp & 3) * 32 + lane;  // dim within a 128-dim chunk = TMEM lane
 #pragma unroll 1
-            for (int c = 0; c < VC; ++c) {
-                const int d = c * 128 + tid;
+        for (int c = warp >> 2; c < VC; c += 2) {
+#pragma unroll 1
+            for (int q = 0; q < NQ; ++q) {
+                float iv[16];
+                load_row16(a_s + q * 16, iv);
                 uint32_t r16[16];
                 if (have_o) {
                     load16(tmem_o + c * N + lane_base + q * 16, r16);
@@ -595,16 +688,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 16; ++u) r16[u] = 0u;
                 }
+                const int d = c * 128 + dl;
                 if (final_out) {
 #pragma unroll
                     for (int u = 0; u < 16; ++u)
-                        if (q * 16 + u < R) out_bf[orow[u] * D + d] = __float2bfloat16_rn(u2f(r16[u]) * inv[u]);
+                        if (q * 16 + u < R) tile_b[(q * 16 + u) * D + d] = __float2bfloat16_rn(u2f(r16[u]) * iv[u]);
                 } else {
 #pragma unroll
                     for (int u = 0; u < 16; ++u)
-                        if (q * 16 + u < R) part_out[(part_base + orow[u]) * D + d] = u2f(r16[u]) * inv[u];
+                        if (q * 16 + u < R) tile_f[(q * 16 + u) * D + d] = u2f(r16[u]) * iv[u];
                 }
             }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync_256();
+        if (tid == 0) {
+            const uint32_t esz = final_out ? 2u : 4u;
+            const uint32_t run = (uint32_t)x.Gc * D * esz;  // bytes of one block position's Gc rows
+            for (int i = 0; i < T; ++i) {
+                const int64_t row0 = (int64_t)(b * T + i) * p.Hq + h0;
+                void* dst = final_out ? static_cast<void*>(static_cast<__nv_bfloat16*>(p.out) + row0 * D)
+                                      : static_cast<void*>(p.part_out + (part_base + row0) * D);
+                bulk_store_global(dst, tile_o + (size_t)i * run, run);
+            }
+            bulk_commit_group();
+            bulk_wait_read_0();  // the tile must stay in shared memory until the copies have read it
         }
     }
 

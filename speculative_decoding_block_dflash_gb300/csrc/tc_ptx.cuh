@@ -181,6 +181,23 @@ __device__ __forceinline__ bool named_bar_or_128(bool pred)
     return r != 0;
 }
 
+// Named barrier 2 over warps 0-7 (256 threads).
+__device__ __forceinline__ void named_bar_sync_256() { asm volatile("bar.sync 2, 256;" ::: "memory"); }
+
+__device__ __forceinline__ bool named_bar_or_256(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 2, 256, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
 // address, leading / stride byte offsets in 16-byte units, version 1 at bit
 // 46, layout type 2 = SWIZZLE_128B at bits 61-63).
@@ -276,6 +293,18 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
 }
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this CTA's
+// shared memory to global memory, tracked by this thread's bulk async-groups.
+__device__ __forceinline__ void bulk_store_global(void* gdst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Wait until every committed bulk group of this thread has completed (writes performed).
+__device__ __forceinline__ void bulk_wait_all_0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Wait until at most one (resp. zero) committed bulk groups of this thread still read their source.
 __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
