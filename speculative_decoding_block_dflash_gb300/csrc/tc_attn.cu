@@ -107,7 +107,7 @@ struct TcLayout {
     static constexpr int kRingOff = kPOff + N * 128 * 2;                // [stages][16 KB]
     static constexpr int kOnesOff = kRingOff + kStages * kStageBytes;   // bf16 ones [16 x 64] (row-sum MMA)
     static constexpr int kBarOff = kOnesOff + kOnesBytes;
-    static constexpr int kNumBars = 2 * kStages + 6;
+    static constexpr int kNumBars = 2 * kStages + 5;
     static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;  // tmem base, abort flag
     static constexpr int kMOff = kMiscOff + 16;                         // float m_s[N]
     static constexpr int kAOff = kMOff + N * 4;                         // float alpha_s[N] (1/l at the end)
@@ -188,11 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
     uint64_t* full = bars;
     uint64_t* empty = bars + S;
-    uint64_t* q_full = bars + 2 * S;
-    uint64_t* s_full = q_full + 1;  // [2] MMA -> softmax: S^T of the tile is in TMEM buffer j mod 2
-    uint64_t* p_full = q_full + 3;  // softmax -> MMA: P^T written and S^T buffer read
-    uint64_t* p_free = q_full + 4;  // MMA -> softmax: PV of the tile done (P^T, O^T and l free)
-    uint64_t* drain = q_full + 5;
+    uint64_t* s_full = bars + 2 * S;  // [2] MMA -> softmax: S^T of the tile is in TMEM buffer j mod 2
+    uint64_t* p_full = s_full + 2;    // softmax -> MMA: P^T written and S^T buffer read
+    uint64_t* p_free = s_full + 3;    // MMA -> softmax: PV of the tile done (P^T, O^T and l free)
+    uint64_t* drain = s_full + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
     float* m_s = reinterpret_cast<float*>(smem + Lay::kMOff);
@@ -321,10 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < S; ++s) issued_parity[s] = 2;  // 2 = nothing outstanding
         if (ntiles > 0) {
-            if (pw == 0 && lane == 0) {
-                mbar_expect_tx(q_full, (uint32_t)(R * 128 * KC));
-                for (int kc = 0; kc < KC; ++kc) tma_load_3d(q_s + kc * N * 128, &tm_q, q_full, kc * 64, h0, b * T);
-            }
             const int box = Psz * 128;  // bytes of one page x 64 dims
             int seq = 0;                // index of the stage in the whole sequence; this warp fills seq = pw (mod 4)
             for (int k = 0; k < 2 * ntiles && ok; ++k) {
@@ -345,7 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!ok) break;
                         if (lane == 0) {
                             uint8_t* dst = ring + stage * kStageBytes;
-                            mbar_expect_tx(full + stage, kStageBytes);
+                            // The Q tile rides on the first stage's barrier: the MMA warp's first
+                            // wait covers it. (A separate barrier completed by the tensor-copy unit
+                            // and waited on ahead of the ring made every later K/V copy of the CTA
+                            // land about twice as late.)
+                            const bool with_q = (seq == 0);
+                            mbar_expect_tx(full + stage, kStageBytes + (with_q ? (uint32_t)(R * 128 * KC) : 0u));
+                            if (with_q)
+                                for (int kc = 0; kc < KC; ++kc)
+                                    tma_load_3d(q_s + kc * N * 128, &tm_q, full + stage, kc * 64, h0, b * T);
                             if (is_k) {
                                 for (int pg = 0; pg < pages_per_tile; ++pg)
                                     tma_load_4d(dst + pg * box, &tm_k, full + stage, sq * 64, g, 0,
@@ -405,10 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 phase ^= 1u;
             }
         };
-        if (ntiles > 0) {
-            ok = wait_lane0(q_full, 0);
-            tc_fence_after();
-        }
         for (int k = 0; k < 2 * ntiles && ok; ++k) {
             bool is_k;
             int j;
