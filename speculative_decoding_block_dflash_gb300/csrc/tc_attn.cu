@@ -99,15 +99,16 @@ constexpr int pow2ceil(int x)
 
 template <int D, int N>
 struct TcLayout {
-    static constexpr int kFixed = N * D * 2 + N * 128 * 2 + 4096 + kOnesBytes;
+    static constexpr int kPBytes = N * 128 * 2;                         // one P^T buffer: 2 key halves
+    static constexpr int kFixed = N * D * 2 + 2 * kPBytes + 4096 + kOnesBytes;
     static constexpr int kStagesFit = (227 * 1024 - 1024 - kFixed) / kStageBytes;
     static constexpr int kStages = kStagesFit > 12 ? 12 : kStagesFit;
     static constexpr int kQOff = 0;                                     // [D/64][N rows][128 B]
-    static constexpr int kPOff = kQOff + N * D * 2;                     // [2 key halves][N rows][128 B]
-    static constexpr int kRingOff = kPOff + N * 128 * 2;                // [stages][16 KB]
+    static constexpr int kPOff = kQOff + N * D * 2;                     // [2 buffers][2 key halves][N rows][128 B]
+    static constexpr int kRingOff = kPOff + 2 * kPBytes;                // [stages][16 KB]
     static constexpr int kOnesOff = kRingOff + kStages * kStageBytes;   // bf16 ones [16 x 64] (row-sum MMA)
     static constexpr int kBarOff = kOnesOff + kOnesBytes;
-    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kNumBars = 2 * kStages + 6;
     static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;  // tmem base, abort flag
     static constexpr int kMOff = kMiscOff + 16;                         // float m_s[N]
     static constexpr int kAOff = kMOff + N * 4;                         // float alpha_s[N] (1/l at the end)
@@ -122,7 +123,7 @@ struct TcLayout {
     static constexpr int kTmemCols = pow2ceil(kTmemUsed);
     static_assert(kStages >= 3, "ring too shallow");
     static_assert(kOnesOff - kQOff >= N * D * 4, "output tile staging (Q, P and the ring)");
-    static_assert(kPOff + N * 128 + 128 * 128 <= kOnesOff, "128-row P operand of the row-sum MMA");
+    static_assert(kPOff + kPBytes + N * 128 + 128 * 128 <= kOnesOff, "128-row P operand of the row-sum MMA");
     static_assert(kTmemUsed <= 512, "TMEM budget");
     static_assert((N * D * 2) % 1024 == 0 && (N * 128) % 1024 == 0, "1024-byte swizzle atoms");
     static_assert(kTotal + 1024 <= 227 * 1024, "shared memory budget");
@@ -190,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty = bars + S;
     uint64_t* s_full = bars + 2 * S;  // [2] MMA -> softmax: S^T of the tile is in TMEM buffer j mod 2
     uint64_t* p_full = s_full + 2;    // softmax -> MMA: P^T written and S^T buffer read
-    uint64_t* p_free = s_full + 3;    // MMA -> softmax: PV of the tile done (P^T, O^T and l free)
-    uint64_t* drain = s_full + 4;
+    uint64_t* p_free = s_full + 3;    // [2] MMA -> softmax: PV of the tile done (P^T buffer j mod 2 free)
+    uint64_t* drain = s_full + 5;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
     float* m_s = reinterpret_cast<float*>(smem + Lay::kMOff);
@@ -442,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             const int tile_key0 = t0 + j * kTileKeys;
+            const uint32_t pb_addr = p_addr + (uint32_t)(j & 1) * Lay::kPBytes;
             for (int h = 0; h < 2 && ok; ++h) {
                 for (int c = 0; c < VC && ok; ++c) {
                     ok = wait_lane0(full + stage, phase);
@@ -468,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma(tmem_o + c * N, sw128_desc(st + kk * 2048, 8192, 1024),
-                                   sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024), idesc_o,
+                                   sw128_desc(pb_addr + h * N * 128 + kk * 32, 16, 1024), idesc_o,
                                    (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
                         tc_commit(empty + stage);
                     }
@@ -480,14 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma(tmem_l, sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024),
+                        tc_mma(tmem_l, sw128_desc(pb_addr + h * N * 128 + kk * 32, 16, 1024),
                                sw128_desc(ones_addr + kk * 32, 16, 1024), idesc_l,
                                (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
                 }
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(p_free);
+            if (lane == 0) tc_commit(p_free + (j & 1));
             __syncwarp();
         }
         // Drain our MMAs before TMEM is released.
@@ -503,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sl2 = p.scale * kLog2e;
         const bool plain = (p.causal == 0 && p.window == 0);
         // P^T store address pieces for this key lane (K-major, 128-byte swizzle)
-        uint8_t* pcol = p_s + (tid >> 6) * (N * 128);
+        uint8_t* pcol0 = p_s + (tid >> 6) * (N * 128);
         const int pchunk = (tid & 63) >> 3;
         const int pbyte = (tid & 7) * 2;
         bool ok = true;
@@ -574,14 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 named_bar_sync_128();
             }
-            // P^T, O^T and l are free once the previous tile's PV has completed
-            if (j > 0) {
-                if (!group_wait(p_free, (uint32_t)((j - 1) & 1))) {
+            // O^T and l^T hold tile j-1 once its PV has completed: only a rescale waits for it.
+            // P^T buffer j mod 2 is free once PV(j-2) has completed. (p_free[b] completes once
+            // per two tiles and every phase is waited for in order.)
+            if (j > 0 && need) {
+                if (!group_wait(p_free + ((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                if (need) {
+                {
 #pragma unroll 1
                     for (int cq = 0; cq < VC * NQ; ++cq) {
                         const int c = cq / NQ, q = cq % NQ;
@@ -606,7 +610,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                 }
             }
-            // pass 2: P = exp2(s - m), bf16, into P^T[col][key]
+            if (j > 1) {
+                if (!group_wait(p_free + (j & 1), (uint32_t)(((j - 2) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            // pass 2: P = exp2(s - m), bf16, into P^T buffer j mod 2 [col][key]
+            uint8_t* pcol = pcol0 + (j & 1) * Lay::kPBytes;
 #pragma unroll 1
             for (int q = 0; q < NQ; ++q) {
                 // row maxima into registers first: the P^T stores below must not be ordered
@@ -633,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         bool good = ok && ntiles > 0;
-        if (good) good = group_wait(p_free, (uint32_t)((ntiles - 1) & 1));
+        if (good) good = group_wait(p_free + ((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1));
         role_ok = good;
     }
 
