@@ -36,7 +36,10 @@
 // transposing shuffle reduction leaves each lane with one column's maximum over
 // its warp, then the four warps meet in shared memory; O^T and l^T are then
 // rescaled by exp2(m_old - m_new) in TMEM). P = exp2(s - m) is rounded to bf16
-// and written to shared memory as the operand of the PV and row-sum MMAs.
+// pairs and written to shared memory as the operand of the PV and row-sum MMAs,
+// MN-major with a 32-byte swizzle so that a key lane's 16 rows of a group are two
+// 16-byte stores. P^T has two buffers: the softmax of tile j+1 writes while
+// PV(j) still reads.
 //
 // Warp roles (288 threads): warps 0-3 softmax, warps 4-7 TMA producers, warp 8
 // MMA issuer; warps 0-7 share the epilogue. One warp's tensor copies are
@@ -389,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t idesc_s = make_idesc(128, N, 0, 0);   // S^T  = K . Q^T   (A K-major, B K-major)
-        constexpr uint32_t idesc_o = make_idesc(128, N, 1, 0);   // O^T += V^T . P^T (A MN-major, B K-major)
-        constexpr uint32_t idesc_l = make_idesc(128, 16, 0, 0);  // l^T += P . 1     (A K-major, B K-major)
+        constexpr uint32_t idesc_o = make_idesc(128, N, 1, 1);   // O^T += V^T . P^T (A MN-major, B MN-major)
+        constexpr uint32_t idesc_l = make_idesc(128, 16, 1, 0);  // l^T += P . 1     (A MN-major, B K-major)
         const uint32_t q_addr = smem_u32(q_s);
         const uint32_t p_addr = smem_u32(p_s);
         const uint32_t ring_addr = smem_u32(ring);
@@ -470,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma(tmem_o + c * N, sw128_desc(st + kk * 2048, 8192, 1024),
-                                   sw128_desc(pb_addr + h * N * 128 + kk * 32, 16, 1024), idesc_o,
+                                   sw32_desc(pb_addr + h * N * 128 + kk * 512, 2048, 256), idesc_o,
                                    (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
                         tc_commit(empty + stage);
                     }
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        tc_mma(tmem_l, sw128_desc(pb_addr + h * N * 128 + kk * 32, 16, 1024),
+                        tc_mma(tmem_l, sw32_desc(pb_addr + h * N * 128 + kk * 512, 2048, 256),
                                sw128_desc(ones_addr + kk * 32, 16, 1024), idesc_l,
                                (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -504,10 +507,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ softmax warps 0-3 (thread = key lane)
         const float sl2 = p.scale * kLog2e;
         const bool plain = (p.causal == 0 && p.window == 0);
-        // P^T store address pieces for this key lane (K-major, 128-byte swizzle)
-        uint8_t* pcol0 = p_s + (tid >> 6) * (N * 128);
-        const int pchunk = (tid & 63) >> 3;
-        const int pbyte = (tid & 7) * 2;
+        // P^T is MN-major with a 32-byte swizzle: per key half, 16-row groups (atoms) of
+        // 2048 B = 8 key groups x (8 keys x 32 B); this key lane owns one 32-byte row of
+        // every atom, the two 16-byte halves swapped for keys 4-7 of a group.
+        const int pr = tid & 7;
+        uint8_t* prow0 = p_s + (tid >> 6) * (N * 128) + ((tid & 63) >> 3) * 256 + pr * 32;
+        const int pswz0 = (0 ^ (pr >> 2)) << 4;
+        const int pswz1 = (1 ^ (pr >> 2)) << 4;
         bool ok = true;
         // One thread waits on the mbarrier; the named barrier makes the outcome
         // uniform across the 128 softmax threads (so none is left at a barrier).
@@ -617,8 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
             }
-            // pass 2: P = exp2(s - m), bf16, into P^T buffer j mod 2 [col][key]
-            uint8_t* pcol = pcol0 + (j & 1) * Lay::kPBytes;
+            // pass 2: P = exp2(s - m), bf16 pairs, into P^T buffer j mod 2
+            uint8_t* prow = prow0 + (j & 1) * Lay::kPBytes;
 #pragma unroll 1
             for (int q = 0; q < NQ; ++q) {
                 // row maxima into registers first: the P^T stores below must not be ordered
@@ -627,16 +633,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_row16(m_s + q * 16, mv);
                 uint32_t r16[16];
                 load16(sb + q * 16, r16);
-                __nv_bfloat16 pb[16];
+                uint32_t pk[8];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float sc = score(r16[u], q * 16 + u);
-                    pb[u] = __float2bfloat16_rn((sc == -INFINITY) ? 0.f : ex2(sc - mv[u]));
+                for (int u = 0; u < 8; ++u) {
+                    const float s0 = score(r16[2 * u], q * 16 + 2 * u);
+                    const float s1 = score(r16[2 * u + 1], q * 16 + 2 * u + 1);
+                    const float e0 = (s0 == -INFINITY) ? 0.f : ex2(s0 - mv[2 * u]);
+                    const float e1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - mv[2 * u + 1]);
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+                    pk[u] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
-                uint8_t* prow = pcol + q * 16 * 128 + pbyte;
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    *reinterpret_cast<__nv_bfloat16*>(prow + u * 128 + ((pchunk ^ (u & 7)) << 4)) = pb[u];
+                uint8_t* dst = prow + q * 2048;
+                *reinterpret_cast<uint4*>(dst + pswz0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(dst + pswz1) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
             if (!dry) {
                 fence_proxy_async_smem();

@@ -212,6 +212,19 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// Shared-memory matrix descriptor, 32-byte swizzle (layout type 6): atoms of 8 rows x 32 B
+// in which the two 16-byte halves of rows 4-7 are swapped.
+__device__ __forceinline__ uint64_t sw32_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)6 << 61;
+    return d;
+}
+
 // Descriptor without swizzle (layout type 0): core matrices of 8 rows x 16 B.
 __device__ __forceinline__ uint64_t noswz_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
 {
