@@ -111,7 +111,11 @@ struct TcLayout {
     static constexpr int kRingOff = kPOff + 2 * kPBytes;                // [stages][16 KB]
     static constexpr int kOnesOff = kRingOff + kStages * kStageBytes;   // bf16 ones [16 x 64] (row-sum MMA)
     static constexpr int kBarOff = kOnesOff + kOnesBytes;
-    static constexpr int kNumBars = 2 * kStages + 6;
+    // Stages of the first K tile that do not fit the ring borrow the P^T buffers, which
+    // are not written before the first softmax (it starts after those stages are consumed).
+    static constexpr int kExtraWant = D / 64 - kStages;
+    static constexpr int kExtra = (kPBytes < kStageBytes || kExtraWant <= 0) ? 0 : (kExtraWant > 2 ? 2 : kExtraWant);
+    static constexpr int kNumBars = 2 * kStages + 6 + kExtra;
     static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;  // tmem base, abort flag
     static constexpr int kMOff = kMiscOff + 16;                         // float m_s[N]
     static constexpr int kAOff = kMOff + N * 4;                         // float alpha_s[N] (1/l at the end)
@@ -172,6 +176,31 @@ __device__ __forceinline__ void ring_unit(int k, int n, bool& is_k, int& tile)
     }
 }
 
+// Buffer and phase of the stage with sequence number seq: stages S .. S+E-1 (the tail of the
+// first K tile) go to the E extra slots, used once; every other stage cycles through the
+// S ring slots.
+struct RingSlot {
+    int idx;
+    uint32_t phase;
+    bool extra;
+};
+
+__device__ __forceinline__ RingSlot ring_slot(int seq, int S, int E)
+{
+    RingSlot r;
+    if (seq >= S && seq < S + E) {
+        r.idx = seq - S;
+        r.phase = 0;
+        r.extra = true;
+    } else {
+        const int q = seq < S ? seq : seq - E;
+        r.idx = q % S;
+        r.phase = (uint32_t)((q / S) & 1);
+        r.extra = false;
+    }
+    return r;
+}
+
 template <int D, int N>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -196,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_full = s_full + 2;    // softmax -> MMA: P^T written and S^T buffer read
     uint64_t* p_free = s_full + 3;    // [2] MMA -> softmax: PV of the tile done (P^T buffer j mod 2 free)
     uint64_t* drain = s_full + 5;
+    uint64_t* xfull = s_full + 6;     // [kExtra] TMA -> MMA: extra stage landed (used once)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
     float* m_s = reinterpret_cast<float*>(smem + Lay::kMOff);
@@ -316,11 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
         // ------------------------------------------------------------ TMA producers
-        int stage = 0;
-        uint32_t phase = 0;
+        constexpr int E = Lay::kExtra;
         bool ok = true;
         int wbase = 0;
         uint32_t issued_parity[S];
+        uint32_t issued_extra = 0;
 #pragma unroll
         for (int s = 0; s < S; ++s) issued_parity[s] = 2;  // 2 = nothing outstanding
         if (ntiles > 0) {
@@ -339,23 +369,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                             wbase = (tile > 0 ? tile - 1 : 0) * pages_per_tile;
                             load_window(wbase);
                         }
-                        if (lane == 0) ok = wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.err);
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok) break;
+                        const RingSlot sl = ring_slot(seq, S, E);
+                        uint64_t* fb = sl.extra ? xfull + sl.idx : full + sl.idx;
+                        if (!sl.extra) {
+                            if (lane == 0) ok = wait_bounded(empty + sl.idx, sl.phase ^ 1u, abort_flag, p.err);
+                            ok = __shfl_sync(0xffffffffu, ok, 0);
+                            if (!ok) break;
+                        }
                         if (lane == 0) {
-                            uint8_t* dst = ring + stage * kStageBytes;
+                            uint8_t* dst = sl.extra ? p_s + sl.idx * Lay::kPBytes : ring + sl.idx * kStageBytes;
                             // The Q tile rides on the first stage's barrier: the MMA warp's first
                             // wait covers it. (A separate barrier completed by the tensor-copy unit
                             // and waited on ahead of the ring made every later K/V copy of the CTA
                             // land about twice as late.)
                             const bool with_q = (seq == 0);
-                            mbar_expect_tx(full + stage, kStageBytes + (with_q ? (uint32_t)(R * 128 * KC) : 0u));
+                            mbar_expect_tx(fb, kStageBytes + (with_q ? (uint32_t)(R * 128 * KC) : 0u));
                             if (with_q)
                                 for (int kc = 0; kc < KC; ++kc)
-                                    tma_load_3d(q_s + kc * N * 128, &tm_q, full + stage, kc * 64, h0, b * T);
+                                    tma_load_3d(q_s + kc * N * 128, &tm_q, fb, kc * 64, h0, b * T);
                             if (is_k) {
                                 for (int pg = 0; pg < pages_per_tile; ++pg)
-                                    tma_load_4d(dst + pg * box, &tm_k, full + stage, sq * 64, g, 0,
+                                    tma_load_4d(dst + pg * box, &tm_k, fb, sq * 64, g, 0,
                                                 pid_w[rel0 + pg - wbase]);
                             } else {
                                 const int h = sq / VC, c = sq % VC;
@@ -363,17 +397,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int pg = 0; pg < ppg; ++pg) {
                                     const int32_t page = pid_w[rel0 + h * ppg + pg - wbase];
                                     for (int m = 0; m < 2; ++m)
-                                        tma_load_4d(dst + m * 8192 + pg * box, &tm_v, full + stage, c * 128 + m * 64,
+                                        tma_load_4d(dst + m * 8192 + pg * box, &tm_v, fb, c * 128 + m * 64,
                                                     g, 0, page);
                                 }
                             }
-                            issued_parity[stage] = phase;
+                            if (sl.extra)
+                                issued_extra |= 1u << sl.idx;
+                            else
+                                issued_parity[sl.idx] = sl.phase;
                         }
                         __syncwarp();
-                    }
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
                     }
                 }
             }
@@ -384,6 +417,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (issued_parity[s] > 1) continue;
                 const unsigned long long t_start = globaltimer();
                 while (!mbar_try_wait(full + s, issued_parity[s]) && globaltimer() - t_start < kTimeoutNs) {
+                }
+            }
+            for (int e = 0; e < E; ++e) {
+                if (!(issued_extra & (1u << e))) continue;
+                const unsigned long long t_start = globaltimer();
+                while (!mbar_try_wait(xfull + e, 0) && globaltimer() - t_start < kTimeoutNs) {
                 }
             }
         }
@@ -398,19 +437,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t p_addr = smem_u32(p_s);
         const uint32_t ring_addr = smem_u32(ring);
         const uint32_t ones_addr = smem_u32(ones_s);
-        int stage = 0;
-        uint32_t phase = 0;
+        constexpr int E = Lay::kExtra;
+        int mseq = 0;  // sequence number of the next ring stage
         bool ok = true;
         auto wait_lane0 = [&](uint64_t* bar, uint32_t par) -> bool {
             bool got = true;
             if (lane == 0) got = wait_bounded(bar, par, abort_flag, p.err);
             return __shfl_sync(0xffffffffu, got, 0);
         };
-        auto advance = [&]() {
-            if (++stage == S) {
-                stage = 0;
-                phase ^= 1u;
-            }
+        // wait for the next stage; its shared address (and whether it is an extra slot)
+        auto next_stage = [&](uint32_t& addr, RingSlot& sl) -> bool {
+            sl = ring_slot(mseq, S, E);
+            const bool got = wait_lane0(sl.extra ? xfull + sl.idx : full + sl.idx, sl.phase);
+            addr = sl.extra ? p_addr + sl.idx * Lay::kPBytes : ring_addr + sl.idx * kStageBytes;
+            return got;
+        };
+        auto release = [&](const RingSlot& sl) {
+            if (lane == 0 && !sl.extra) tc_commit(empty + sl.idx);
+            __syncwarp();
+            ++mseq;
         };
         for (int k = 0; k < 2 * ntiles && ok; ++k) {
             bool is_k;
@@ -421,20 +466,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // softmax has finished with (its p_full was waited for by the V(j-2) unit)
                 const uint32_t sb = tmem_s + (uint32_t)(j & 1) * N;
                 for (int kc = 0; kc < KC && ok; ++kc) {
-                    ok = wait_lane0(full + stage, phase);
+                    uint32_t st;
+                    RingSlot sl;
+                    ok = next_stage(st, sl);
                     if (!ok) break;
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t st = ring_addr + stage * kStageBytes;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma(sb, sw128_desc(st + kk * 32, 16, 1024),
                                    sw128_desc(q_addr + kc * N * 128 + kk * 32, 16, 1024), idesc_s,
                                    (kc > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(empty + stage);
                     }
-                    __syncwarp();
-                    advance();
+                    release(sl);
                 }
                 if (!ok) break;
                 if (lane == 0) tc_commit(s_full + (j & 1));
@@ -449,7 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t pb_addr = p_addr + (uint32_t)(j & 1) * Lay::kPBytes;
             for (int h = 0; h < 2 && ok; ++h) {
                 for (int c = 0; c < VC && ok; ++c) {
-                    ok = wait_lane0(full + stage, phase);
+                    uint32_t st_addr;
+                    RingSlot sl;
+                    ok = next_stage(st_addr, sl);
                     if (!ok) break;
                     tc_fence_after();
                     // V rows past seq_len in the sequence's last, partial page -> zero
@@ -457,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int zlo = L - key0;
                     if (L % Psz != 0 && zlo > 0 && zlo < 64 && ch.ke == L) {
                         const int zhi = min(64, ((L + Psz - 1) / Psz) * Psz - key0);
-                        uint8_t* st = ring + stage * kStageBytes;
+                        uint8_t* st = smem + (st_addr - smem_u32(smem));
                         const int rows = zhi - zlo;
                         for (int idx = lane; idx < rows * 16; idx += 32) {
                             const int m = idx / (rows * 8);
@@ -469,16 +515,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                     }
                     if (lane == 0) {
-                        const uint32_t st = ring_addr + stage * kStageBytes;
+                        const uint32_t st = st_addr;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             tc_mma(tmem_o + c * N, sw128_desc(st + kk * 2048, 8192, 1024),
                                    sw32_desc(pb_addr + h * N * 128 + kk * 512, 2048, 256), idesc_o,
                                    (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(empty + stage);
                     }
-                    __syncwarp();
-                    advance();
+                    release(sl);
                 }
                 // Row sums: P read as a 128-row A operand (rows >= N fall on the next shared
                 // memory region and only produce unused TMEM lanes) times a 64 x 16 block of ones.
@@ -525,10 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // Iteration j = -1 is a dry run over fully masked scores while the first K tile is
         // in flight: it executes the instructions of a real tile, the row-max path
-        // included, without touching a barrier, so the first real tile does not wait on
-        // instruction fetches from a memory system busy with K/V traffic. It reads the
-        // O^T columns (not written before p_full) and leaves zeros in P^T (not read before
-        // p_full), m = -inf and alpha = 0.
+        // included, without touching a barrier or P^T (whose buffers may hold the first
+        // tile's extra K stages), so the first real tile does not wait on instruction
+        // fetches from a memory system busy with K/V traffic. It reads the O^T columns
+        // (not written before p_full) and leaves m = -inf and alpha = 0.
         for (int j = (ntiles > 0 ? -1 : 0); j < ntiles && ok; ++j) {
             const bool dry = j < 0;
             const uint32_t sb = (dry ? tmem_o : tmem_s + (uint32_t)(j & 1) * N) + lane_base;
@@ -643,9 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
                     pk[u] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
-                uint8_t* dst = prow + q * 2048;
-                *reinterpret_cast<uint4*>(dst + pswz0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4*>(dst + pswz1) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                if (!dry) {
+                    uint8_t* dst = prow + q * 2048;
+                    *reinterpret_cast<uint4*>(dst + pswz0) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4*>(dst + pswz1) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
             }
             if (!dry) {
                 fence_proxy_async_smem();
