@@ -196,7 +196,10 @@ DFLASH_API int32_t dflash_plan_splits(const dflash_dims* dims, int32_t block_len
 
 /* Workspace bytes a call with these sizes and split count needs (split count
    as returned by dflash_plan_splits). Layout, each part 256-byte aligned: the
-   error word (256 bytes), B*Hq int32 counters, then -- only when splits > 1 --
+   error word (256 bytes), an 8 KB counter block (the arrival counters of the
+   tensor-core kernel's in-kernel split combine; fixed size, zero between
+   calls, left non-zero only after a device timeout), then -- only when
+   splits > 1 --
    partial lse float32 [splits, B*T, Hq] and partial out float32
    [splits, B*T, Hq, D]. Returns 0 for invalid dims. */
 DFLASH_API size_t dflash_workspace_bytes(const dflash_dims* dims, int32_t block_len, int32_t num_splits);

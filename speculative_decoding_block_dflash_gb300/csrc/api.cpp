@@ -123,7 +123,7 @@ WorkspaceLayout workspace_layout(int32_t B, int32_t T, int32_t Hq, int32_t D, in
     WorkspaceLayout w;
     w.err_off = 0;
     w.counters_off = 256;
-    size_t off = w.counters_off + round_up(sizeof(int32_t) * (size_t)B * Hq, 256);
+    size_t off = w.counters_off + DFLASH_COUNTER_BYTES;
     w.part_lse_off = off;
     w.part_out_off = off;
     if (splits > 1) {

@@ -33,7 +33,12 @@ struct AttnParams {
     int32_t dtype;        // dflash_dtype
 };
 
-// Workspace carve-up (offsets in bytes from the workspace base).
+// Workspace carve-up (offsets in bytes from the workspace base). The counter block has a
+// fixed size, so a workspace zeroed once stays valid for calls of any size: two int32
+// counters per (request, row group) of an in-kernel split combine, which only runs when the
+// whole grid is resident (at most a few hundred groups).
+constexpr size_t DFLASH_COUNTER_BYTES = 8192;
+constexpr int DFLASH_MAX_COMBINE_GROUPS = (int)(DFLASH_COUNTER_BYTES / 8);
 struct WorkspaceLayout {
     size_t err_off, counters_off, part_lse_off, part_out_off, total;
 };

@@ -88,10 +88,18 @@ constexpr float kRescaleThresh = 8.0f;
 constexpr int kOnesBytes = 4096;
 
 struct TcExtra {
-    int32_t Gc;    // query heads per CTA
-    int32_t n_rg;  // row groups per KV head (G / Gc)
-    int32_t R;     // packed rows per CTA (Gc * T)
+    int32_t Gc;     // query heads per CTA
+    int32_t n_rg;   // row groups per KV head (G / Gc)
+    int32_t R;      // packed rows per CTA (Gc * T)
+    int32_t fused;  // 1: the split CTAs of a row group combine their partials in this kernel
 };
+
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* ptr)
+{
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
 
 constexpr int pow2ceil(int x)
 {
@@ -778,7 +786,118 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_store_global(dst, tile_o + (size_t)i * run, run);
             }
             bulk_commit_group();
-            bulk_wait_read_0();  // the tile must stay in shared memory until the copies have read it
+            if (x.fused)
+                bulk_wait_all_0();   // the partial must be in global memory before the arrival below
+            else
+                bulk_wait_read_0();  // the tile must stay in shared memory until the copies have read it
+        }
+
+        if (x.fused) {
+            // ------------------------------------------------------------ split combine
+            // The splits CTAs of this (request, row group) are co-resident (cooperative
+            // launch). Each publishes its partial (the bulk copy above, the lse stores
+            // before it), arrives on the group's counter and waits for all of them; then
+            // each combines a slice of the group's R x D outputs:
+            //   m = max_c lse_c, w_c = exp(lse_c - m), out = sum_c w_c o_c / sum_c w_c,
+            //   lse = m + log(sum_c w_c)
+            // The last CTA to finish resets the two counters to zero for the next call.
+            __threadfence();
+            named_bar_sync_256();
+            int32_t* cnt = p.counters + 2 * (b * gridDim.y + blockIdx.y);
+            bool arrived = true;
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __threadfence();
+                atomicAdd(cnt, 1);
+                const unsigned long long t_start = globaltimer();
+                while (ld_acquire_gpu(cnt) < p.splits) {
+                    if (globaltimer() - t_start > kTimeoutNs) {
+                        raise_error(p.err, DFLASH_DEVERR_TIMEOUT);
+                        arrived = false;
+                        break;
+                    }
+                }
+            }
+            arrived = !named_bar_or_256(!arrived);
+            if (arrived) {
+                const int64_t nrow_all = (int64_t)p.B * T * p.Hq;  // rows of one split's partial
+                const int total = R * D;
+                const int per = ((total + p.splits - 1) / p.splits + 3) & ~3;
+                const int e0 = c_split * per;
+                const int e1 = min(total, e0 + per);
+                if (e0 < e1) {
+                    const int r0 = e0 / D;
+                    const int nr = (e1 - 1) / D - r0 + 1;
+                    float* w_sm = reinterpret_cast<float*>(smem + Lay::kQOff);  // [nr][splits] weights
+                    float* r_sm = w_sm + nr * p.splits;                          // [nr][2]: 1/sum, lse
+                    for (int rr = warp; rr < nr; rr += 8) {
+                        const int64_t orow = orow_s[r0 + rr];
+                        float m = -INFINITY;
+                        for (int c = lane; c < p.splits; c += 32) m = fmaxf(m, __ldcg(p.part_lse + (int64_t)c * nrow_all + orow));
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                        float tot = 0.f;
+                        for (int c = lane; c < p.splits; c += 32) {
+                            const float l = __ldcg(p.part_lse + (int64_t)c * nrow_all + orow);
+                            const float w = (l == -INFINITY) ? 0.f : expf(l - m);
+                            w_sm[rr * p.splits + c] = w;
+                            tot += w;
+                        }
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+                        if (lane == 0) {
+                            const bool empty_row = (m == -INFINITY) || !(tot > 0.f);
+                            r_sm[2 * rr] = empty_row ? 0.f : 1.f / tot;
+                            r_sm[2 * rr + 1] = empty_row ? -INFINITY : m + logf(tot);
+                        }
+                    }
+                    named_bar_sync_256();
+                    for (int e = e0 + tid * 4; e < e1; e += 256 * 4) {
+                        const int r = e / D, d = e - r * D, rr = r - r0;
+                        const float inv = r_sm[2 * rr];
+                        const int64_t orow = orow_s[r];
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (inv > 0.f) {
+                            const float* base = p.part_out + orow * D + d;
+                            const int64_t cstride = nrow_all * D;
+                            for (int c0 = 0; c0 < p.splits; c0 += 16) {
+                                float4 v[16];
+#pragma unroll
+                                for (int k = 0; k < 16; ++k)
+                                    v[k] = c0 + k < p.splits
+                                               ? __ldcg(reinterpret_cast<const float4*>(base + (c0 + k) * cstride))
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                                for (int k = 0; k < 16; ++k) {
+                                    const float w = c0 + k < p.splits ? w_sm[rr * p.splits + c0 + k] : 0.f;
+                                    acc.x = fmaf(w, v[k].x, acc.x);
+                                    acc.y = fmaf(w, v[k].y, acc.y);
+                                    acc.z = fmaf(w, v[k].z, acc.z);
+                                    acc.w = fmaf(w, v[k].w, acc.w);
+                                }
+                            }
+                        }
+                        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+                        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+                        uint2 pk;
+                        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow * D + d) = pk;
+                    }
+                    // a row's lse is written by the CTA whose slice holds the row's first element
+                    for (int rr = tid; rr < nr; rr += 256)
+                        if ((r0 + rr) * D >= e0 && p.lse) p.lse[orow_s[r0 + rr]] = r_sm[2 * rr + 1];
+                }
+            }
+            named_bar_sync_256();
+            if (tid == 0 && arrived) {
+                __threadfence();
+                if (atomicAdd(cnt + 1, 1) == p.splits - 1) {
+                    // every CTA of the group has passed the arrival wait and read its slice
+                    atomicExch(cnt, 0);
+                    atomicExch(cnt + 1, 0);
+                }
+            }
         }
     }
 
@@ -822,27 +941,56 @@ int choose_gc(int G, int T)
 
 template <int D, int N>
 cudaError_t launch_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                      const TcExtra& x, cudaStream_t stream)
+                      const TcExtra& x, cudaStream_t stream, bool* combined)
 {
     using Lay = TcLayout<D, N>;
     auto kern = tc_attn_kernel<D, N>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
     if (e != cudaSuccess) return e;
     dim3 grid(p.splits, p.Hkv * x.n_rg, p.B);
-    kern<<<grid, kThreads, Lay::kAlloc, stream>>>(tq, tk, tv, p, x);
-    return cudaGetLastError();
+    TcExtra xx = x;
+    bool coop = false;
+    if (p.splits > 1 && p.counters) {
+        // fused combine: every CTA of the grid must be resident at once
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Lay::kAlloc) == cudaSuccess &&
+            (int64_t)grid.x * grid.y * grid.z <= (int64_t)per_sm * device_sm_count() &&
+            (int64_t)grid.y * grid.z <= DFLASH_MAX_COMBINE_GROUPS)
+            coop = true;
+    }
+    xx.fused = coop ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Lay::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = coop ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p, xx);
+    if (coop && e == cudaErrorCooperativeLaunchTooLarge) {
+        (void)cudaGetLastError();  // not resident after all: plain launch, separate combine
+        coop = false;
+        xx.fused = 0;
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p, xx);
+    }
+    *combined = (e == cudaSuccess) && coop;
+    return e;
 }
 
 template <int D>
 cudaError_t launch_d(int n, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                     const TcExtra& x, cudaStream_t stream)
+                     const TcExtra& x, cudaStream_t stream, bool* combined)
 {
     switch (n) {
-    case 16: return launch_dn<D, 16>(tq, tk, tv, p, x, stream);
-    case 32: return launch_dn<D, 32>(tq, tk, tv, p, x, stream);
-    case 48: return launch_dn<D, 48>(tq, tk, tv, p, x, stream);
-    case 64: return launch_dn<D, 64>(tq, tk, tv, p, x, stream);
-    case 80: return launch_dn<D, 80>(tq, tk, tv, p, x, stream);
+    case 16: return launch_dn<D, 16>(tq, tk, tv, p, x, stream, combined);
+    case 32: return launch_dn<D, 32>(tq, tk, tv, p, x, stream, combined);
+    case 48: return launch_dn<D, 48>(tq, tk, tv, p, x, stream, combined);
+    case 64: return launch_dn<D, 64>(tq, tk, tv, p, x, stream, combined);
+    case 80: return launch_dn<D, 80>(tq, tk, tv, p, x, stream, combined);
     }
     return cudaErrorNotSupported;
 }
@@ -871,6 +1019,7 @@ cudaError_t launch_tc_attn(const AttnParams& p, cudaStream_t stream)
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     TcExtra x;
+    x.fused = 0;
     x.Gc = choose_gc(p.G, p.T);
     x.n_rg = p.G / x.Gc;
     x.R = x.Gc * p.T;
@@ -903,13 +1052,14 @@ cudaError_t launch_tc_attn(const AttnParams& p, cudaStream_t stream)
             return cudaErrorInvalidValue;
     }
     cudaError_t e;
+    bool combined = false;
     switch (p.D) {
-    case 128: e = launch_d<128>(n, tq, tk, tv, p, x, stream); break;
-    case 256: e = launch_d<256>(n, tq, tk, tv, p, x, stream); break;
-    case 512: e = launch_d<512>(n, tq, tk, tv, p, x, stream); break;
+    case 128: e = launch_d<128>(n, tq, tk, tv, p, x, stream, &combined); break;
+    case 256: e = launch_d<256>(n, tq, tk, tv, p, x, stream, &combined); break;
+    case 512: e = launch_d<512>(n, tq, tk, tv, p, x, stream, &combined); break;
     default: e = cudaErrorNotSupported;
     }
-    if (e != cudaSuccess || p.splits == 1) return e;
+    if (e != cudaSuccess || p.splits == 1 || combined) return e;
     return launch_combine(p.part_out, p.part_lse, p.splits, (int64_t)p.B * p.T * p.Hq, p.D, p.dtype, p.out, p.lse,
                           stream);
 }

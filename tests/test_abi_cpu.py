@@ -74,12 +74,12 @@ def test_workspace_layout(lib):
     d = good_dims()
     T = 9
     n1 = lib.dflash_workspace_bytes(ctypes.byref(d), T, 1)
-    assert n1 == 256 + 256  # error word + 2*32 int32 counters (rounded)
+    assert n1 == 256 + 8192  # error word + fixed counter block
     S = 16
     rows = 2 * T * 32
     n = lib.dflash_workspace_bytes(ctypes.byref(d), T, S)
     rnd = lambda x: (x + 255) // 256 * 256
-    assert n == 512 + rnd(4 * rows * S) + rnd(4 * rows * S * 512)
+    assert n == 256 + 8192 + rnd(4 * rows * S) + rnd(4 * rows * S * 512)
     assert lib.dflash_workspace_bytes(ctypes.byref(d), T, 0) == 0
     assert lib.dflash_workspace_bytes(ctypes.byref(good_dims(head_dim=520)), T, 1) == 0
 
