@@ -431,7 +431,9 @@ def main():
     tc = (args.kernel == "tc") or (args.kernel == "auto" and case.q.dtype == torch.bfloat16 and
                                    _tc_used(dfl, dims, case, splits_req))
     kernel_name = "tc_attn_kernel" if tc else "simt_attn_kernel"
-    launches_per_step = 1 if splits == 1 else 2  # attention (+ split combine)
+    # attention, plus the split combine unless the tensor-core kernel combines in-kernel
+    # (it does whenever its whole grid is resident: one CTA per SM)
+    launches_per_step = 1 if splits == 1 or (tc and _tc_ctas(case, splits) <= _sm_count(dev)) else 2
     peak, peak_kind = measured_peaks()
     traffic, traffic_note = traffic_from_profiles(kernel_name)
     achieved = kv / (ms_per_step * 1e-3) / 1e9
@@ -487,6 +489,18 @@ def main():
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def _tc_ctas(case, splits):
+    """CTAs of the tensor-core grid: splits x KV heads x row groups x requests (row groups: the
+    largest divisor of G whose G/rg query heads x T rows fit one 80-row tile)."""
+    G = case.num_q_heads // case.num_kv_heads
+    gc = max(d for d in range(1, G + 1) if G % d == 0 and d * case.block_len <= 80)
+    return splits * case.num_kv_heads * (G // gc) * case.batch
+
+
+def _sm_count(dev):
+    return torch.cuda.get_device_properties(dev).multi_processor_count
 
 
 def _tc_used(dfl, dims, case, splits_req):
