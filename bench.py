@@ -327,7 +327,7 @@ def main():
     def call(layer, stream=None):
         dfl.block_attn(case.q, case.k_cache, case.v_cache, case.page_tables[layer], case.seq_lens,
                        case.block_len, causal=case.causal, window=case.window, scale=case.scale, out=out,
-                       lse=lse, num_splits=splits, kernel=args.kernel, workspace=ws, stream=stream)
+                       lse=lse, num_splits=splits_req, kernel=args.kernel, workspace=ws, stream=stream)
 
     # one CUDA graph per layer (captured on a side stream after an eager warm-up)
     side = torch.cuda.Stream(device=dev)
@@ -406,7 +406,7 @@ def main():
         pt_d.copy_(pts_h[k % layers], non_blocking=True)
         sl_d.copy_(sl_h, non_blocking=True)
         dfl.block_attn(q_d, case.k_cache, case.v_cache, pt_d, sl_d, case.block_len, causal=case.causal,
-                       window=case.window, scale=case.scale, out=out, lse=lse, num_splits=splits,
+                       window=case.window, scale=case.scale, out=out, lse=lse, num_splits=splits_req,
                        kernel=args.kernel, workspace=ws)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
@@ -433,7 +433,7 @@ def main():
     kernel_name = "tc_attn_kernel" if tc else "simt_attn_kernel"
     # attention, plus the split combine unless the tensor-core kernel combines in-kernel
     # (it does whenever its whole grid is resident: one CTA per SM)
-    launches_per_step = 1 if splits == 1 or (tc and _tc_ctas(case, splits) <= _sm_count(dev)) else 2
+    launches_per_step = 1 if splits == 1 or (tc and _tc_ctas(case, splits, splits_req) <= _sm_count(dev)) else 2
     peak, peak_kind = measured_peaks()
     traffic, traffic_note = traffic_from_profiles(kernel_name)
     achieved = kv / (ms_per_step * 1e-3) / 1e9
@@ -491,12 +491,15 @@ def main():
         dist.destroy_process_group()
 
 
-def _tc_ctas(case, splits):
-    """CTAs of the tensor-core grid: splits x KV heads x row groups x requests (row groups: the
-    largest divisor of G whose G/rg query heads x T rows fit one 80-row tile)."""
+def _tc_ctas(case, splits, splits_req):
+    """CTAs of the tensor-core grid: chunk slots x KV heads x row groups, times the requests
+    unless the auto plan deals its slots over the requests by length (row groups: the largest
+    divisor of G whose G/rg query heads x T rows fit one 80-row tile)."""
     G = case.num_q_heads // case.num_kv_heads
     gc = max(d for d in range(1, G + 1) if G % d == 0 and d * case.block_len <= 80)
-    return splits * case.num_kv_heads * (G // gc) * case.batch
+    per = splits * case.num_kv_heads * (G // gc)
+    balanced = splits_req <= 0 and case.batch > 1 and splits >= case.batch
+    return per if balanced else per * case.batch
 
 
 def _sm_count(dev):

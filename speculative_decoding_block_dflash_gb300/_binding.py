@@ -215,7 +215,7 @@ def block_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pa
     if workspace is None:
         workspace = workspace_for(q.device, need)
     opts = Opts()
-    opts.num_splits = splits
+    opts.num_splits = num_splits  # the caller's request: the library re-plans the same count (0 = auto)
     opts.kernel = KERNELS[kernel]
     opts.workspace = workspace.data_ptr()
     opts.workspace_bytes = workspace.numel() * workspace.element_size()

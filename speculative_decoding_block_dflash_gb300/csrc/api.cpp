@@ -201,20 +201,55 @@ int32_t plan_splits_impl(const dflash_dims* d, int32_t T, int32_t window, int32_
 {
     if (requested > 0) return requested > DFLASH_MAX_SPLITS ? -DFLASH_ERR_INVALID_ARG : requested;
     if (requested < 0) return -DFLASH_ERR_INVALID_ARG;
+    // Several requests on the tensor-core path: one wave of chunk slots dealt to the requests
+    // in proportion to their key spans (the kernel reads seq_lens), so a long request does
+    // not leave most SMs idle while its equal-count chunks finish.
+    const int32_t bal = balanced_slots(d, T, window, kernel);
+    if (bal > 0) return bal;
     // Longest union key range any request can have.
     int64_t span = max_len_of(d);
     if (window > 0) span = std::min<int64_t>(span, (int64_t)window + T - 1 + d->page_size);
-    // Keep at least 128 keys (one tensor-core tile) per chunk; aim for one wave over the SMs.
+    // Keep at least 128 keys (one tensor-core tile) per chunk; fill at most one wave over the
+    // SMs (a partial second wave would cost a whole extra round of the longest chunks).
     const int64_t max_by_len = std::max<int64_t>(1, span / 128);
     const int64_t units = work_units(d, T, kernel);
     const int64_t sms = device_sm_count();
-    int64_t s = (sms + units - 1) / units;
+    int64_t s = sms / units;
     s = std::min<int64_t>(s, max_by_len);
     s = std::min<int64_t>(s, DFLASH_MAX_SPLITS);
     return (int32_t)std::max<int64_t>(1, s);
 }
 
 }  // namespace
+
+namespace dflash {
+
+int32_t balanced_slots(const dflash_dims* d, int32_t T, int32_t window, int kernel)
+{
+    if (kernel != DFLASH_KERNEL_TC || d->batch < 2) return 0;
+    AttnParams p{};
+    p.B = 1;
+    p.T = T;
+    p.Hkv = d->num_kv_heads;
+    p.G = d->num_q_heads / d->num_kv_heads;
+    const int64_t per_req = tc_ctas_per_split(p);  // CTAs of one (request, chunk)
+    if (per_req <= 0) return 0;
+    if ((int64_t)d->batch * per_req > DFLASH_MAX_COMBINE_GROUPS) return 0;
+    int64_t span = max_len_of(d);
+    if (window > 0) span = std::min<int64_t>(span, (int64_t)window + T - 1 + d->page_size);
+    int64_t c = device_sm_count() / per_req;                            // one wave
+    c = std::min<int64_t>(c, (int64_t)d->batch * std::max<int64_t>(1, span / 128));  // >= a tile each
+    c = std::min<int64_t>(c, DFLASH_MAX_SPLITS);
+    if (c < d->batch || c < 2) return 0;
+    return (int32_t)c;
+}
+
+int resolve_kernel(const dflash_dims* d, int32_t T, int32_t window, int32_t requested)
+{
+    return choose_kernel(d, T, window, requested);
+}
+
+}  // namespace dflash
 
 extern "C" {
 
@@ -284,7 +319,10 @@ dflash_status dflash_block_attn(const void* q, const void* k_cache, const void* 
     const int32_t splits = plan_splits_impl(dims, block_len, window, requested, kernel);
     if (splits < 1) return fail(DFLASH_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", requested, DFLASH_MAX_SPLITS);
 
-    const WorkspaceLayout wl = workspace_layout(dims->batch, block_len, dims->num_q_heads, dims->head_dim, splits);
+    // Length-balanced plan: partials are [slot][T][Hq][D], so the layout is sized for one request.
+    const bool balanced = requested == 0 && splits > 1 && balanced_slots(dims, block_len, window, kernel) == splits;
+    const WorkspaceLayout wl =
+        workspace_layout(balanced ? 1 : dims->batch, block_len, dims->num_q_heads, dims->head_dim, splits);
     void* ws = opts ? opts->workspace : nullptr;
     const size_t ws_bytes = opts ? opts->workspace_bytes : 0;
     if (ws) {
@@ -327,6 +365,7 @@ dflash_status dflash_block_attn(const void* q, const void* k_cache, const void* 
     p.scale = scale;
     p.splits = splits;
     p.dtype = dims->dtype;
+    p.balanced = balanced ? 1 : 0;
 
     cudaStream_t stream = opts ? static_cast<cudaStream_t>(opts->stream) : nullptr;
     cudaError_t e = (kernel == DFLASH_KERNEL_TC)        ? launch_tc_attn(p, stream)

@@ -29,8 +29,10 @@ struct AttnParams {
     int64_t sp, ss, sh;   // K/V element strides: page, slot, head
     int32_t causal, window;
     float scale;
-    int32_t splits;
+    int32_t splits;       // uniform: chunks per request; balanced: chunk slots in total
     int32_t dtype;        // dflash_dtype
+    int32_t balanced;     // 1: the tensor-core kernel deals its `splits` slots to the requests in
+                          // proportion to their key spans (partials laid out [slot][T][Hq][D])
 };
 
 // Workspace carve-up (offsets in bytes from the workspace base). The counter block has a
@@ -43,6 +45,12 @@ struct WorkspaceLayout {
     size_t err_off, counters_off, part_lse_off, part_out_off, total;
 };
 WorkspaceLayout workspace_layout(int32_t B, int32_t T, int32_t Hq, int32_t D, int32_t splits);
+
+// Slots of the tensor-core kernel's length-balanced split plan for these sizes (auto split
+// count, B > 1, whole grid resident), or 0 when the plan is uniform.
+int32_t balanced_slots(const dflash_dims* d, int32_t T, int32_t window, int kernel);
+// Kernel a selector resolves to for these sizes (a dflash_kernel value), or -status.
+int resolve_kernel(const dflash_dims* d, int32_t T, int32_t window, int32_t requested);
 
 // Kernel launchers (return cudaSuccess or the launch error).
 cudaError_t launch_simt_attn(const AttnParams& p, cudaStream_t stream);

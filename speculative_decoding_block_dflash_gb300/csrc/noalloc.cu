@@ -59,7 +59,10 @@ extern "C" DFLASH_API dflash_status dflash_block_attn_noalloc(
         return dflash_block_attn(q, k_cache, v_cache, page_table, seq_lens, dims, block_len, causal, window, scale,
                                  out, lse, &o);
     }
-    const size_t need = dflash_workspace_bytes(dims, block_len, splits);
+    const int kres = resolve_kernel(dims, block_len, window, kernel);
+    const bool balanced = num_splits == 0 && splits > 1 && balanced_slots(dims, block_len, window, kres) == splits;
+    const size_t need =
+        workspace_layout(balanced ? 1 : dims->batch, block_len, dims->num_q_heads, dims->head_dim, splits).total;
     if (need > (size_t)DFLASH_NOALLOC_SCRATCH_BYTES)
         return report_error(DFLASH_ERR_WORKSPACE,
                             "dflash_block_attn_noalloc: %d splits need %zu bytes of scratch, more than the %u bytes "
@@ -69,11 +72,12 @@ extern "C" DFLASH_API dflash_status dflash_block_attn_noalloc(
     cudaError_t e = scratch_address(&ws);
     if (e != cudaSuccess) return report_error(DFLASH_ERR_CUDA, "resolving the scratch address: %s", cudaGetErrorString(e));
     // the error word and the counters must start at zero; the rest is overwritten before it is read
-    const WorkspaceLayout wl = workspace_layout(dims->batch, block_len, dims->num_q_heads, dims->head_dim, splits);
+    const WorkspaceLayout wl =
+        workspace_layout(balanced ? 1 : dims->batch, block_len, dims->num_q_heads, dims->head_dim, splits);
     e = cudaMemsetAsync(ws, 0, wl.part_lse_off, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return report_error(DFLASH_ERR_CUDA, "clearing the scratch header: %s", cudaGetErrorString(e));
     dflash_opts o{};
-    o.num_splits = splits;
+    o.num_splits = num_splits;  // the same request re-plans to the same split count and layout
     o.kernel = kernel;
     o.workspace = ws;
     o.workspace_bytes = DFLASH_NOALLOC_SCRATCH_BYTES;

@@ -209,6 +209,46 @@ __device__ __forceinline__ RingSlot ring_slot(int seq, int S, int E)
     return r;
 }
 
+// Length-balanced plan: the splits chunk slots of a row group are dealt to the B requests in
+// proportion to their key spans (every request gets at least one): request b gets
+// 1 + e(b+1) - e(b) slots with e(k) = round((splits - B) * span(0..k) / span(all)). Slot
+// `slot` is chunk c of n of request b, whose chunks start at slot `first`.
+struct ReqChunk {
+    int32_t b, c, n, first;
+};
+
+__device__ inline int64_t key_span(const AttnParams& p, int32_t b)
+{
+    int32_t L = __ldg(p.seq_lens + b);
+    if (L < 0) L = 0;
+    if (L > p.max_seq_len) L = p.max_seq_len;
+    int32_t lo = 0;
+    if (p.window > 0) {
+        lo = L - p.T - p.window + 1;
+        if (lo < 0) lo = 0;
+    }
+    const int64_t n = (int64_t)L - (lo / p.page_size) * p.page_size;
+    return n > 0 ? n : 1;
+}
+
+__device__ inline ReqChunk balanced_chunk(const AttnParams& p, int32_t slot)
+{
+    int64_t total = 0;
+    for (int32_t b = 0; b < p.B; ++b) total += key_span(p, b);
+    const int64_t extra = p.splits - p.B;
+    int64_t pref = 0;
+    int32_t first = 0, e0 = 0;
+    for (int32_t b = 0; b < p.B; ++b) {
+        pref += key_span(p, b);
+        const int32_t e1 = (int32_t)((2 * extra * pref + total) / (2 * total));
+        const int32_t n = 1 + e1 - e0;
+        if (slot < first + n) return ReqChunk{b, slot - first, n, first};
+        first += n;
+        e0 = e1;
+    }
+    return ReqChunk{p.B - 1, 0, 1, first};
+}
+
 template <int D, int N>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -247,10 +287,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int c_split = blockIdx.x;
+    // (request, chunk of its n_split chunks); partial rows of chunk k sit at
+    // (slot0 + k) * rstride + rbias + output row
+    int b, c_split, n_split, slot0;
+    int64_t rstride, rbias;
+    if (p.balanced) {
+        const ReqChunk rc = balanced_chunk(p, blockIdx.x);
+        b = rc.b;
+        c_split = rc.c;
+        n_split = rc.n;
+        slot0 = rc.first;
+        rstride = (int64_t)p.T * p.Hq;
+        rbias = -(int64_t)b * p.T * p.Hq;
+    } else {
+        b = blockIdx.z;
+        c_split = blockIdx.x;
+        n_split = p.splits;
+        slot0 = 0;
+        rstride = (int64_t)p.B * p.T * p.Hq;
+        rbias = 0;
+    }
     const int g = blockIdx.y / x.n_rg;
     const int rg = blockIdx.y % x.n_rg;
-    const int b = blockIdx.z;
     const int T = p.T;
     const int Psz = p.page_size;
     const int R = x.R;
@@ -261,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Chunk ch;
     ch.kb = 0;
     ch.ke = 0;
-    if (len_ok) ch = split_chunk(L, T, p.window, Psz, p.splits, c_split);
+    if (len_ok) ch = split_chunk(L, T, p.window, Psz, n_split, c_split);
     const int t0 = (ch.kb / Psz) * Psz;
     const int ntiles = (ch.kb < ch.ke) ? (ch.ke - t0 + kTileKeys - 1) / kTileKeys : 0;
     const int pages_per_tile = kTileKeys / Psz;
@@ -722,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < 8) {
         const bool have_o = !named_bar_or_256(!role_ok) && ntiles > 0;
         tc_fence_after();
-        const int64_t part_base = (int64_t)c_split * p.B * T * p.Hq;
+        const int64_t part_base = (slot0 + c_split) * rstride + rbias;
         const bool final_out = (p.splits == 1);
         if (warp < 4) {
             // row tid's sum sits in TMEM lane tid of l^T
@@ -810,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence();
                 atomicAdd(cnt, 1);
                 const unsigned long long t_start = globaltimer();
-                while (ld_acquire_gpu(cnt) < p.splits) {
+                while (ld_acquire_gpu(cnt) < n_split) {
                     if (globaltimer() - t_start > kTimeoutNs) {
                         raise_error(p.err, DFLASH_DEVERR_TIMEOUT);
                         arrived = false;
@@ -820,27 +878,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             arrived = !named_bar_or_256(!arrived);
             if (arrived) {
-                const int64_t nrow_all = (int64_t)p.B * T * p.Hq;  // rows of one split's partial
                 const int total = R * D;
-                const int per = ((total + p.splits - 1) / p.splits + 3) & ~3;
+                const int per = ((total + n_split - 1) / n_split + 3) & ~3;
                 const int e0 = c_split * per;
                 const int e1 = min(total, e0 + per);
                 if (e0 < e1) {
                     const int r0 = e0 / D;
                     const int nr = (e1 - 1) / D - r0 + 1;
                     float* w_sm = reinterpret_cast<float*>(smem + Lay::kQOff);  // [nr][splits] weights
-                    float* r_sm = w_sm + nr * p.splits;                          // [nr][2]: 1/sum, lse
+                    float* r_sm = w_sm + nr * n_split;                           // [nr][2]: 1/sum, lse
                     for (int rr = warp; rr < nr; rr += 8) {
                         const int64_t orow = orow_s[r0 + rr];
                         float m = -INFINITY;
-                        for (int c = lane; c < p.splits; c += 32) m = fmaxf(m, __ldcg(p.part_lse + (int64_t)c * nrow_all + orow));
+                        const float* lse_row = p.part_lse + slot0 * rstride + rbias + orow;
+                        for (int c = lane; c < n_split; c += 32) m = fmaxf(m, __ldcg(lse_row + c * rstride));
 #pragma unroll
                         for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
                         float tot = 0.f;
-                        for (int c = lane; c < p.splits; c += 32) {
-                            const float l = __ldcg(p.part_lse + (int64_t)c * nrow_all + orow);
+                        for (int c = lane; c < n_split; c += 32) {
+                            const float l = __ldcg(lse_row + c * rstride);
                             const float w = (l == -INFINITY) ? 0.f : expf(l - m);
-                            w_sm[rr * p.splits + c] = w;
+                            w_sm[rr * n_split + c] = w;
                             tot += w;
                         }
 #pragma unroll
@@ -858,18 +916,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int64_t orow = orow_s[r];
                         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                         if (inv > 0.f) {
-                            const float* base = p.part_out + orow * D + d;
-                            const int64_t cstride = nrow_all * D;
-                            for (int c0 = 0; c0 < p.splits; c0 += 16) {
+                            const float* base = p.part_out + (slot0 * rstride + rbias + orow) * D + d;
+                            const int64_t cstride = rstride * D;
+                            for (int c0 = 0; c0 < n_split; c0 += 16) {
                                 float4 v[16];
 #pragma unroll
                                 for (int k = 0; k < 16; ++k)
-                                    v[k] = c0 + k < p.splits
+                                    v[k] = c0 + k < n_split
                                                ? __ldcg(reinterpret_cast<const float4*>(base + (c0 + k) * cstride))
                                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                                 for (int k = 0; k < 16; ++k) {
-                                    const float w = c0 + k < p.splits ? w_sm[rr * p.splits + c0 + k] : 0.f;
+                                    const float w = c0 + k < n_split ? w_sm[rr * n_split + c0 + k] : 0.f;
                                     acc.x = fmaf(w, v[k].x, acc.x);
                                     acc.y = fmaf(w, v[k].y, acc.y);
                                     acc.z = fmaf(w, v[k].z, acc.z);
@@ -892,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync_256();
             if (tid == 0 && arrived) {
                 __threadfence();
-                if (atomicAdd(cnt + 1, 1) == p.splits - 1) {
+                if (atomicAdd(cnt + 1, 1) == n_split - 1) {
                     // every CTA of the group has passed the arrival wait and read its slice
                     atomicExch(cnt, 0);
                     atomicExch(cnt + 1, 0);
@@ -947,9 +1005,10 @@ cudaError_t launch_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     auto kern = tc_attn_kernel<D, N>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.splits, p.Hkv * x.n_rg, p.B);
+    dim3 grid(p.splits, p.Hkv * x.n_rg, p.balanced ? 1 : p.B);
     TcExtra xx = x;
     bool coop = false;
+    if (p.balanced && !p.counters) return cudaErrorInvalidValue;  // the balanced plan combines in-kernel
     if (p.splits > 1 && p.counters) {
         // fused combine: every CTA of the grid must be resident at once
         int per_sm = 0;
@@ -958,6 +1017,7 @@ cudaError_t launch_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
             (int64_t)grid.y * grid.z <= DFLASH_MAX_COMBINE_GROUPS)
             coop = true;
     }
+    if (p.balanced && !coop) return cudaErrorInvalidConfiguration;  // its partials need the in-kernel combine
     xx.fused = coop ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -970,7 +1030,7 @@ cudaError_t launch_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     cfg.attrs = attr;
     cfg.numAttrs = coop ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p, xx);
-    if (coop && e == cudaErrorCooperativeLaunchTooLarge) {
+    if (coop && e == cudaErrorCooperativeLaunchTooLarge && !p.balanced) {
         (void)cudaGetLastError();  // not resident after all: plain launch, separate combine
         coop = false;
         xx.fused = 0;

@@ -92,8 +92,10 @@ def test_plan_splits_explicit_and_invalid(lib):
     assert lib.dflash_plan_splits(ctypes.byref(good_dims(head_dim=72)), 9, 0, 0, 0) == -B.ERR_UNSUPPORTED
     auto = lib.dflash_plan_splits(ctypes.byref(d), 9, 0, 0, 0)
     assert 1 <= auto <= 256
-    # a sliding window bounds the useful split count by its span
-    assert lib.dflash_plan_splits(ctypes.byref(d), 9, 256, 0, 0) <= 2
+    # a sliding window bounds the useful split count by its span (per request: the
+    # length-balanced plan deals its slots over the batch's requests)
+    assert lib.dflash_plan_splits(ctypes.byref(d), 9, 256, 0, 0) <= 2 * d.batch
+    assert lib.dflash_plan_splits(ctypes.byref(good_dims(batch=1)), 9, 256, 0, 0) <= 2
 
 
 def test_head_dim_512_accepted_and_above_rejected(lib):

@@ -263,6 +263,25 @@ def test_split_counts_agree(kernel):
         torch.testing.assert_close(lse, lref, atol=1e-3, rtol=1e-3)
 
 
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (False, 2048)])
+def test_length_balanced_plan(causal, window):
+    # Very different lengths under the auto plan: the tensor-core kernel deals one wave of
+    # chunk slots to the requests by key span and combines in-kernel.
+    case = workloads.make_custom("balanced", 4, 9, 32, 4, 512, [64, 9000, 1500, 300], causal=causal,
+                                 window=window, seed=31, device="cuda")
+    maybe_skip(case, "tc")
+    dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
+    slots = dfl.plan_splits(dims, case.block_len, case.window, 0, "tc")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert case.batch <= slots <= sms // case.num_kv_heads  # one wave of 4-CTA slots
+    out, lse = run(case, kernel="tc", num_splits=0)
+    check_full(case, out, lse)
+    # the same call with the uniform plan of as many chunks agrees
+    uni, luni = run(case, kernel="tc", num_splits=slots)
+    torch.testing.assert_close(out.float(), uni.float(), atol=1e-2, rtol=1e-2)
+    torch.testing.assert_close(lse, luni, atol=1e-3, rtol=1e-3)
+
+
 def test_window_covering_everything_equals_global():
     case = workloads.make_custom("wg", 2, 9, 8, 2, 128, [300, 500], seed=19, device="cuda")
     a, la = run(case)

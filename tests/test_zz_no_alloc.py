@@ -76,6 +76,16 @@ def test_noalloc_unsplit_and_auto_plan():
         _close(lse, ref_l, 1e-2)
 
 
+def test_noalloc_length_balanced_auto_plan():
+    # B > 1 with the auto plan takes the length-balanced layout, which fits the scratch
+    case = workloads.make_custom("noalloc_bal", 4, 9, 32, 4, 512, [64, 9000, 1500, 300], seed=74,
+                                 device="cuda")
+    ref_o, ref_l = _reference(case, 0, "auto")
+    out, lse = _noalloc(case, 0, "auto")
+    _close(out, ref_o, 1e-2)
+    _close(lse, ref_l, 1e-2)
+
+
 def test_noalloc_rejects_plans_beyond_its_scratch():
     lib = dfl.load_library()
     case = workloads.make_custom("noalloc_big", 8, 16, 32, 4, 512, [4096] * 8, seed=73, device="cuda")
