@@ -248,6 +248,39 @@ DFLASH_API dflash_status dflash_block_attn_noalloc(const void* q, const void* k_
                                                    int32_t window, float scale, void* out, float* lse,
                                                    int32_t num_splits, int32_t kernel, void* stream);
 
+/*
+ * Longest-prefix acceptance: the verify step after the target has scored a drafted
+ * block. The pages describe the loop as guess a block, verify it in parallel, accept the
+ * longest correct prefix, repeat (kenforever1 "dflash-gemma4-31b-notes", relation
+ * diagram steps 3-4).
+ *
+ * A block is [x_0, d_1, ..., d_K] with K = block_len - 1 drafted tokens. For request b and
+ * block position j the target token is t_j = argmax_v logits[b, j, v] (the smallest index
+ * among equal maxima; logits must be finite). Draft d_i is correct when d_i == t_{i-1}.
+ *   accepted_len[b] = the largest a in [0, K] with d_i == t_{i-1} for all i <= a
+ *   next_token[b]   = t_a  (the target's token at the first mismatch, or after the block)
+ *   target_argmax[b, j] = t_j when target_argmax is not NULL
+ *
+ *   logits        device, [batch, block_len, vocab] of dtype (bf16 or fp32), row j of request
+ *                 b at (b * block_len + j) * row_stride elements, row_stride >= vocab; aligned
+ *                 to its element size (rows are read with 16-byte loads between their
+ *                 16-byte boundaries).
+ *   draft         device int32 [batch, block_len - 1] (may be NULL when block_len == 1).
+ *   accepted_len, next_token   device int32 [batch], written.
+ *   target_argmax device int32 [batch, block_len] or NULL.
+ *   workspace     device, 256-byte aligned, dflash_accept_workspace_bytes() long, zeroed once
+ *                 before its first use; the call leaves it zeroed (it holds one 64-bit key
+ *                 per row and one arrival counter per request).
+ * Limits: batch * block_len <= 65535, 1 <= vocab < 2^31. Invalid arguments are reported
+ * before any launch. Asynchronous on `stream`; calls that share a workspace must not overlap.
+ */
+DFLASH_API size_t dflash_accept_workspace_bytes(int32_t batch, int32_t block_len);
+DFLASH_API dflash_status dflash_accept_prefix(const void* logits, dflash_dtype dtype, int32_t batch,
+                                              int32_t block_len, int32_t vocab, int64_t row_stride,
+                                              const int32_t* draft, int32_t* accepted_len, int32_t* next_token,
+                                              int32_t* target_argmax, void* workspace, size_t workspace_bytes,
+                                              void* stream);
+
 /* DFLASH_ABI_VERSION of the loaded library. */
 DFLASH_API int32_t dflash_abi_version(void);
 

@@ -16,6 +16,8 @@ from ._binding import (  # noqa: F401
     Dims,
     Opts,
     abi_version,
+    accept_prefix,
+    accept_workspace_bytes,
     block_attn,
     block_attn_noalloc,
     load_library,

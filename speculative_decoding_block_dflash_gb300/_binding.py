@@ -38,6 +38,8 @@ EXPORTED = (
     "dflash_status_string",
     "dflash_last_error_message",
     "dflash_abi_version",
+    "dflash_accept_prefix",
+    "dflash_accept_workspace_bytes",
 )
 
 
@@ -108,6 +110,10 @@ def load_library(path: Optional[str] = None):
         lib.dflash_last_error_message.argtypes = []
         lib.dflash_abi_version.restype = i32
         lib.dflash_abi_version.argtypes = []
+        lib.dflash_accept_workspace_bytes.restype = ctypes.c_size_t
+        lib.dflash_accept_workspace_bytes.argtypes = [i32, i32]
+        lib.dflash_accept_prefix.restype = ctypes.c_int
+        lib.dflash_accept_prefix.argtypes = [vp, i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         if path is None:
             _lib = lib
         return lib
@@ -274,6 +280,53 @@ def split_combine(partial_out: torch.Tensor, partial_lse: torch.Tensor, out_dtyp
                                   _dtype_code(out), out.data_ptr(), lse.data_ptr(), _stream_handle(stream))
     _check(st)
     return out, lse
+
+
+_accept_ws = {}
+
+
+def accept_workspace_bytes(batch: int, block_len: int) -> int:
+    n = load_library().dflash_accept_workspace_bytes(int(batch), int(block_len))
+    if n == 0:
+        raise DflashError(1, "invalid batch/block_len for the acceptance workspace")
+    return n
+
+
+def accept_prefix(logits: torch.Tensor, draft: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                  accepted: Optional[torch.Tensor] = None, next_token: Optional[torch.Tensor] = None,
+                  target_argmax: Optional[torch.Tensor] = None, want_argmax: bool = True,
+                  stream=None) -> Tuple[torch.Tensor, torch.Tensor, Optional[torch.Tensor]]:
+    """Longest-prefix acceptance (dflash_accept_prefix): logits [B, T, V] bf16/fp32 (last
+    dim contiguous), draft int32 [B, T-1] -> (accepted_len [B], next_token [B], target
+    argmax [B, T] or None), int32 on the device."""
+    lib = load_library()
+    if logits.dim() != 3 or logits.stride(2) != 1 or logits.stride(0) != logits.shape[1] * logits.stride(1):
+        raise ValueError("logits must be [B, T, V] with contiguous rows of a common stride")
+    B, T, V = logits.shape
+    if draft.dtype != torch.int32 or tuple(draft.shape) != (B, T - 1) or not draft.is_contiguous():
+        raise ValueError("draft must be a contiguous int32 [B, T-1] tensor")
+    dev = logits.device
+    if workspace is None:
+        need = accept_workspace_bytes(B, T)
+        key = (dev.type, dev.index)
+        workspace = _accept_ws.get(key)
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=dev)
+            _accept_ws[key] = workspace
+    if accepted is None:
+        accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=dev)
+    if target_argmax is None and want_argmax:
+        target_argmax = torch.empty(B, T, dtype=torch.int32, device=dev)
+    st = lib.dflash_accept_prefix(logits.data_ptr(), _dtype_code(logits), B, T, V, logits.stride(1),
+                                  draft.data_ptr() if draft.numel() else None, accepted.data_ptr(),
+                                  next_token.data_ptr(),
+                                  target_argmax.data_ptr() if target_argmax is not None else None,
+                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream))
+    _check(st)
+    return accepted, next_token, target_argmax
 
 
 def read_error(workspace: Optional[torch.Tensor] = None, clear: bool = True, stream=None) -> int:

@@ -379,6 +379,42 @@ dflash_status dflash_block_attn(const void* q, const void* k_cache, const void* 
     return DFLASH_OK;
 }
 
+size_t dflash_accept_workspace_bytes(int32_t batch, int32_t block_len)
+{
+    if (batch < 1 || block_len < 1 || (int64_t)batch * block_len > 65535) return 0;
+    return round_up(sizeof(unsigned long long) * (size_t)batch * block_len, 256) +
+           round_up(sizeof(int32_t) * (size_t)batch, 256);
+}
+
+dflash_status dflash_accept_prefix(const void* logits, dflash_dtype dtype, int32_t batch, int32_t block_len,
+                                   int32_t vocab, int64_t row_stride, const int32_t* draft, int32_t* accepted_len,
+                                   int32_t* next_token, int32_t* target_argmax, void* workspace,
+                                   size_t workspace_bytes, void* stream)
+{
+    g_last_error.clear();
+    if (dtype != DFLASH_BF16 && dtype != DFLASH_FP32) return fail(DFLASH_ERR_INVALID_ARG, "dtype must be bf16 or fp32");
+    if (batch < 1 || block_len < 1 || (int64_t)batch * block_len > 65535)
+        return fail(DFLASH_ERR_INVALID_ARG, "batch %d x block_len %d outside [1, 65535]", batch, block_len);
+    if (vocab < 1) return fail(DFLASH_ERR_INVALID_ARG, "vocab %d < 1", vocab);
+    const int64_t es = dtype == DFLASH_BF16 ? 2 : 4;
+    if (row_stride < vocab) return fail(DFLASH_ERR_INVALID_ARG, "row_stride %lld < vocab", (long long)row_stride);
+    if (!logits || !accepted_len || !next_token || (block_len > 1 && !draft))
+        return fail(DFLASH_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(logits, (size_t)es) || (draft && !aligned(draft, 4)) || !aligned(accepted_len, 4) ||
+        !aligned(next_token, 4) || (target_argmax && !aligned(target_argmax, 4)))
+        return fail(DFLASH_ERR_INVALID_ARG, "misaligned pointer (logits to their element size, int32 arrays 4 bytes)");
+    const size_t need = dflash_accept_workspace_bytes(batch, block_len);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+        return fail(DFLASH_ERR_WORKSPACE, "acceptance needs a 256-byte aligned workspace of %zu bytes", need);
+    char* wsb = static_cast<char*>(workspace);
+    auto* keys = reinterpret_cast<unsigned long long*>(wsb);
+    auto* counters = reinterpret_cast<int32_t*>(wsb + round_up(sizeof(unsigned long long) * (size_t)batch * block_len, 256));
+    const cudaError_t e = launch_accept(logits, dtype, batch, block_len, vocab, row_stride, draft, accepted_len,
+                                        next_token, target_argmax, keys, counters, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "acceptance kernel launch");
+    return DFLASH_OK;
+}
+
 dflash_status dflash_split_combine(const float* partial_out, const float* partial_lse, int32_t num_splits,
                                    int64_t num_rows, int32_t head_dim, dflash_dtype out_dtype, void* out, float* lse,
                                    void* stream)

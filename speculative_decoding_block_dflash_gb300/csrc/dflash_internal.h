@@ -46,6 +46,12 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout workspace_layout(int32_t B, int32_t T, int32_t Hq, int32_t D, int32_t splits);
 
+// Longest-prefix acceptance (csrc/accept.cu).
+int32_t accept_chunks(int32_t B, int32_t T, int32_t V);
+cudaError_t launch_accept(const void* logits, int32_t dtype, int32_t B, int32_t T, int32_t V, int64_t row_stride,
+                          const int32_t* draft, int32_t* accepted, int32_t* next_token, int32_t* target_argmax,
+                          unsigned long long* keys, int32_t* counters, cudaStream_t stream);
+
 // Slots of the tensor-core kernel's length-balanced split plan for these sizes (auto split
 // count, B > 1, whole grid resident), or 0 when the plan is uniform.
 int32_t balanced_slots(const dflash_dims* d, int32_t T, int32_t window, int kernel);

@@ -209,3 +209,26 @@ def test_read_error_rejects_null(lib):
 def test_binding_refuses_to_run_without_the_library(tmp_path):
     with pytest.raises(RuntimeError):
         B.load_library(str(tmp_path / "missing.so"))
+
+
+def test_accept_workspace_and_argument_checks(lib):
+    # two regions, each 256-byte aligned: B*T 64-bit keys, then B int32 counters
+    assert lib.dflash_accept_workspace_bytes(8, 9) == 768 + 256
+    assert lib.dflash_accept_workspace_bytes(0, 9) == 0
+    assert lib.dflash_accept_workspace_bytes(1000, 100) == 0  # B*T > 65535
+
+    def acc(dtype=B.BF16, batch=2, T=9, V=1000, stride=1008, draft=FAKE, ws=FAKE, ws_bytes=1 << 20, logits=FAKE):
+        return lib.dflash_accept_prefix(logits, dtype, batch, T, V, stride, draft, FAKE, FAKE, None, ws, ws_bytes,
+                                        None)
+
+    assert acc(dtype=7) == B.ERR_INVALID_ARG
+    assert acc(V=0) == B.ERR_INVALID_ARG
+    assert acc(stride=999) == B.ERR_INVALID_ARG          # shorter than a row
+    assert acc(batch=70000) == B.ERR_INVALID_ARG
+    assert acc(draft=None) == B.ERR_INVALID_ARG          # drafts needed when T > 1
+    assert acc(logits=FAKE + 1) == B.ERR_INVALID_ARG     # logits aligned to their element size
+    assert acc(dtype=B.FP32, logits=FAKE + 2) == B.ERR_INVALID_ARG
+    assert acc(ws=None) == B.ERR_WORKSPACE
+    assert acc(ws_bytes=64) == B.ERR_WORKSPACE
+    assert acc(ws=FAKE + 16) == B.ERR_WORKSPACE
+    assert b"workspace" in lib.dflash_last_error_message()
