@@ -31,6 +31,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 WORKLOAD = "global_verify"
@@ -234,6 +235,160 @@ def reference_arm(args, case):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- acceptance
+
+
+def accept_reference_arm(args):
+    """--impl reference --config accept_verify: the oracle on the host, full steps."""
+    from oracle import accept as oracle_accept
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    logits, draft = accept_inputs(dev, 1)
+    host = logits[0].view(torch.int16).cpu().numpy().view(np.uint16)
+    dh = draft.cpu().numpy()
+    for _ in range(args.warmup):
+        oracle_accept.accept_prefix(host, dh, "bf16")
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_accept.accept_prefix(host, dh, "bf16")
+    t_step = (time.perf_counter() - t0) / max(1, args.steps)
+    per = host.size * 2
+    value = per / t_step / 1e9
+    line = {"impl": "reference", "metric": "logits_hbm_gbs", "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": ACCEPT_DESC},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "full steps: numpy argmax over all rows, then the prefix loop"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+ACCEPT_CONFIG = "accept_verify"
+ACCEPT_DESC = ("verify-step acceptance: batch 8, block_len 9 (1 bonus + 8 drafts), bf16 target logits over a "
+               "262144-entry vocabulary (synthetic; the pages do not state the vocabulary size), drafts that "
+               "match the target on a random prefix")
+
+
+def accept_inputs(dev, n_sets, B=8, T=9, V=262144, seed=1234 + 7):
+    """n_sets disjoint logits buffers [B, T, V] bf16 ~ N(0, 1) and, per set, drafts equal to the
+    target tokens up to a random per-request position (workloads-style seeded synthetic data)."""
+    from oracle import accept as oracle_accept
+
+    g = torch.Generator(device=dev).manual_seed(seed)
+    logits = [torch.randn((B, T, V), generator=g, device=dev).to(torch.bfloat16) for _ in range(n_sets)]
+    rng = np.random.default_rng(seed)
+    drafts = []
+    for x in logits[:1]:
+        t = oracle_accept.target_argmax(x.view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
+        d = t[:, :T - 1].copy()
+        for b in range(B):
+            k = int(rng.integers(0, T))
+            if k < T - 1:
+                d[b, k] = (d[b, k] + 1) % V
+        drafts.append(torch.from_numpy(d.astype(np.int32)).to(dev))
+    return logits, drafts[0]
+
+
+def accept_bench(args, dfl, dev, rank, world):
+    per = 8 * 9 * 262144 * 2
+    n_sets = args.layers or max(2, math.ceil(4 * L2_BYTES / per))
+    logits, draft = accept_inputs(dev, n_sets)
+    B, T, V = logits[0].shape
+    ws = torch.zeros(dfl.accept_workspace_bytes(B, T), dtype=torch.uint8, device=dev)
+    acc = torch.empty(B, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    side = torch.cuda.Stream(dev)
+    with torch.cuda.stream(side):
+        for x in logits:
+            dfl.accept_prefix(x, draft, workspace=ws, accepted=acc, next_token=nxt, want_argmax=False, stream=side)
+    torch.cuda.synchronize()
+    graphs = []
+    for x in logits:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=side):
+            dfl.accept_prefix(x, draft, workspace=ws, accepted=acc, next_token=nxt, want_argmax=False, stream=side)
+        graphs.append(gr)
+    for k in range(max(3, args.warmup)):
+        graphs[k % n_sets].replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for k in range(args.steps):
+        graphs[k % n_sets].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if rank == 0:
+        sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    value = world * per / (ms * 1e-3) / 1e9
+    # end to end: drafts in from pinned memory, accepted length and next token back, every step
+    d_h = draft.cpu().pin_memory()
+    a_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    n_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    n_e2e = min(args.steps, args.e2e_steps)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(n_e2e):
+        draft.copy_(d_h, non_blocking=True)
+        dfl.accept_prefix(logits[k % n_sets], draft, workspace=ws, accepted=acc, next_token=nxt, want_argmax=False)
+        a_h.copy_(acc, non_blocking=True)
+        n_h.copy_(nxt, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        from oracle import accept as oracle_accept
+
+        host = logits[0].view(torch.int16).cpu().numpy().view(np.uint16)
+        dh = draft.cpu().numpy()
+        t0 = time.perf_counter()
+        n_rep = 0
+        while time.perf_counter() - t0 < min(args.cpu_budget, 10.0):
+            oracle_accept.accept_prefix(host, dh, "bf16")
+            n_rep += 1
+        t_step = (time.perf_counter() - t0) / n_rep
+        cpu = {"value": per / t_step / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_rep} full steps (numpy argmax over all {B * T} rows, then the prefix loop)"}
+    line = {
+        "metric": "logits_hbm_gbs", "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": ACCEPT_DESC, "global_batch": B * world, "block_len": T, "vocab": V,
+                   "l2": f"inputs larger than L2: {n_sets} rotated logits sets x {per / 1e6:.1f} MB",
+                   "timed_path": "one CUDA-graph replay of one dflash_accept_prefix call per step",
+                   "parallelism": f"replicas x{world}"},
+        "blocks_per_s": world * B / (ms * 1e-3),
+        "e2e": {"value": world * per / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": d_h.numel() * 4, "d2h_bytes_per_step": 2 * B * 4, "ms_per_step": e2e_ms,
+                "note": "public Python API; drafts in, accepted length and next token out, every step; "
+                        "the logits are device-resident"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": value / world, "peak": peak, "unit": "GB/s",
+                     "frac": value / world / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "accept_kernel",
+                     "achieved_basis": "logits bytes per launch / event-timed device time per step"},
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 
@@ -291,6 +446,11 @@ def main():
             if dist:
                 dist.destroy_process_group()
             return
+        if args.config == ACCEPT_CONFIG:
+            accept_reference_arm(args)
+            if dist:
+                dist.destroy_process_group()
+            return
         import workloads
 
         case = workloads.make_case(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
@@ -310,6 +470,12 @@ def main():
     dfl.load_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+
+    if args.config == ACCEPT_CONFIG:
+        accept_bench(args, dfl, dev, rank, world)
+        if dist:
+            dist.destroy_process_group()
+        return
 
     probe = workloads.make_case(args.config, device=dev, layers=1)
     per_layer = kv_bytes_per_step(probe)
