@@ -19,7 +19,7 @@ the first mismatch, or after the whole block when all K are accepted).
 The argmax is numpy's (first maximal index) on the logits widened exactly to float64
 (bf16 is given as its uint16 bit patterns); the prefix rule is a plain loop.
 
-Pinning: ``tests/test_oracle_pins.py`` checks brute force over every draft pattern of tiny
+Pinning: ``tests/test_oracle_accept_pins.py`` checks brute force over every draft pattern of tiny
 blocks, the all-accepted and none-accepted closed forms, tie-breaking and the K = 0 case.
 """
 from __future__ import annotations
