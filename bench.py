@@ -389,6 +389,173 @@ def accept_bench(args, dfl, dev, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- context K/V projection
+
+
+PROJECT_CONFIG = "project_prefill"
+PROJECT_DESC = ("draft-pass context K/V projection of an 8192-token context: hidden 5376 -> 4 KV heads x 512 "
+                "for K and for V (bf16 weights [2048, 5376] each), written into a paged cache of page size 16 "
+                "through a shuffled page table (synthetic hidden states and random-init weights)")
+PROJECT_SHAPE = dict(L=8192, H=5376, Hkv=4, D=512, P=16)
+
+
+def project_inputs(dev, n_sets, seed=4321):
+    """n_sets disjoint (hidden, w_k, w_v) sets, unit-variance outputs; one slot mapping over a
+    shuffled page table; the two caches."""
+    sh = PROJECT_SHAPE
+    L, H, N, P = sh["L"], sh["H"], sh["Hkv"] * sh["D"], sh["P"]
+    g = torch.Generator(device=dev).manual_seed(seed)
+    sets = []
+    for _ in range(n_sets):
+        hidden = torch.randn((L, H), generator=g, device=dev).to(torch.bfloat16)
+        w_k = (torch.randn((N, H), generator=g, device=dev) / H ** 0.5).to(torch.bfloat16)
+        w_v = (torch.randn((N, H), generator=g, device=dev) / H ** 0.5).to(torch.bfloat16)
+        sets.append((hidden, w_k, w_v))
+    num_pages = 2 * L // P
+    rng = np.random.default_rng(seed)
+    table = rng.permutation(num_pages)[: L // P]
+    pos = np.arange(L)
+    slots = torch.from_numpy((table[pos // P] * P + pos % P).astype(np.int32)).to(dev)
+    k_cache = torch.zeros((num_pages, P, sh["Hkv"], sh["D"]), dtype=torch.bfloat16, device=dev)
+    v_cache = torch.zeros_like(k_cache)
+    return sets, slots, k_cache, v_cache
+
+
+def project_flops():
+    sh = PROJECT_SHAPE
+    return 2.0 * sh["L"] * sh["H"] * 2 * sh["Hkv"] * sh["D"]
+
+
+def project_oracle_rate(budget_s, rows=256, seed=99):
+    """The oracle (float64 numpy matmul) on a bounded sample of token rows: (TFLOP/s, sample text)."""
+    from oracle import project as oracle_project
+
+    sh = PROJECT_SHAPE
+    H, N = sh["H"], sh["Hkv"] * sh["D"]
+    rng = np.random.default_rng(seed)
+    h = rng.standard_normal((rows, H))
+    wk = rng.standard_normal((N, H)) / H ** 0.5
+    wv = rng.standard_normal((N, H)) / H ** 0.5
+    t0 = time.perf_counter()
+    n = 0
+    while n == 0 or time.perf_counter() - t0 < budget_s:
+        oracle_project.project_kv(h, wk, wv, sh["Hkv"], sh["D"])
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    rate = 2.0 * rows * H * 2 * N / dt / 1e12
+    return rate, f"{n} oracle calls on {rows} of the {sh['L']} token rows (float64 numpy matmul, BLAS threads)"
+
+
+def project_reference_arm(args):
+    """--impl reference --config project_prefill: the oracle on the host cores."""
+    budget = max(1.0, min(args.ref_budget, 120.0)) / max(1, args.steps + args.warmup)
+    rate, sample = project_oracle_rate(budget)
+    ms = project_flops() / (rate * 1e12) * 1e3
+    line = {"impl": "reference", "metric": "projection_tflops", "value": rate, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": PROJECT_DESC},
+            "cpu_baseline": {"value": rate, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": rate, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def project_bench(args, dfl, dev, rank, world):
+    sh = PROJECT_SHAPE
+    per_set = (sh["L"] * sh["H"] + 2 * sh["Hkv"] * sh["D"] * sh["H"]) * 2
+    n_sets = args.layers or max(2, math.ceil(4 * L2_BYTES / per_set))
+    sets, slots, k_cache, v_cache = project_inputs(dev, n_sets)
+    side = torch.cuda.Stream(dev)
+    with torch.cuda.stream(side):
+        for hidden, w_k, w_v in sets:
+            dfl.project_kv(hidden, w_k, w_v, slots, k_cache, v_cache, stream=side)
+    torch.cuda.synchronize()
+    graphs = []
+    for hidden, w_k, w_v in sets:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=side):
+            dfl.project_kv(hidden, w_k, w_v, slots, k_cache, v_cache, stream=side)
+        graphs.append(gr)
+    for k in range(max(3, args.warmup)):
+        graphs[k % n_sets].replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for k in range(args.steps):
+        graphs[k % n_sets].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if rank == 0:
+        sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    flops = project_flops()
+    value = world * flops / (ms * 1e-3) / 1e12
+    # end to end: the hidden states and slot mapping in from pinned memory, the error word back
+    h_h = sets[0][0].cpu().pin_memory()
+    s_h = slots.cpu().pin_memory()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    err_h = torch.empty(1, dtype=torch.int32).pin_memory()
+    hidden_d = torch.empty_like(sets[0][0])
+    n_e2e = max(1, min(args.steps, 20))
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(n_e2e):
+        hidden_d.copy_(h_h, non_blocking=True)
+        slots.copy_(s_h, non_blocking=True)
+        _, w_k, w_v = sets[k % n_sets]
+        dfl.project_kv(hidden_d, w_k, w_v, slots, k_cache, v_cache, device_error=err)
+        err_h.copy_(err, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if int(err_h.item()) != 0:
+        raise RuntimeError(f"device error word {int(err_h.item())} after the projection")
+    if rank != 0:
+        return
+    peak, peak_kind = measured_tflops()
+    traffic, tnote = traffic_from_profiles("project_kv_kernel")
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, sample = project_oracle_rate(min(args.cpu_budget, 10.0))
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle", "sample": sample}
+    line = {
+        "metric": "projection_tflops", "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": PROJECT_DESC, "tokens": sh["L"], "hidden": sh["H"], "num_kv_heads": sh["Hkv"],
+                   "head_dim": sh["D"], "page_size": sh["P"],
+                   "l2": f"inputs larger than L2: {n_sets} rotated (hidden, w_k, w_v) sets x {per_set / 1e6:.1f} MB",
+                   "timed_path": "one CUDA-graph replay of one dflash_project_kv call per step",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h_h.numel() * 2 + s_h.numel() * 4, "d2h_bytes_per_step": 4,
+                "ms_per_step": e2e_ms,
+                "note": "public Python API; hidden states and slot mapping in from pinned host memory and the "
+                        "error word back, every step; the weights and the paged cache stay resident"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / world / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "project_kv_kernel",
+                     "achieved_basis": "2*L*H*(2*Hkv*D) flops per launch / event-timed device time per step",
+                     "traffic_note": tnote},
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 
@@ -429,6 +596,17 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_tflops():
+    """Dense bf16 tensor peak: the measured burst figure (a kernel timed in short loops), else fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            return float(json.load(open(path))["bf16_tflops"]), "measured (burst)"
+        except (ValueError, KeyError, OSError):
+            pass
+    return 1900.0, "fallback"
+
+
 def main():
     args = parse_args()
     rank = env_int("RANK", 0)
@@ -448,6 +626,11 @@ def main():
             return
         if args.config == ACCEPT_CONFIG:
             accept_reference_arm(args)
+            if dist:
+                dist.destroy_process_group()
+            return
+        if args.config == PROJECT_CONFIG:
+            project_reference_arm(args)
             if dist:
                 dist.destroy_process_group()
             return
@@ -473,6 +656,11 @@ def main():
 
     if args.config == ACCEPT_CONFIG:
         accept_bench(args, dfl, dev, rank, world)
+        if dist:
+            dist.destroy_process_group()
+        return
+    if args.config == PROJECT_CONFIG:
+        project_bench(args, dfl, dev, rank, world)
         if dist:
             dist.destroy_process_group()
         return

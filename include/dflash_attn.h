@@ -281,6 +281,42 @@ DFLASH_API dflash_status dflash_accept_prefix(const void* logits, dflash_dtype d
                                               int32_t* target_argmax, void* workspace, size_t workspace_bytes,
                                               void* stream);
 
+/*
+ * Context K/V projection for the draft pass, fused with the paged-cache write. The
+ * drafter's cross-attention takes its context K/V from the target's hidden states
+ * (kenforever1 "dflash-gemma4-31b-notes", the code lines under "why non-causal
+ * attention"); the vLLM DFlash review's risk list names this precompute as a bare linear
+ * layer, so no bias, normalisation or rotary embedding is applied. For every token t
+ * whose slot_mapping[t] = s >= 0:
+ *   k_cache[s / page_size, s % page_size, h, d] = bf16( sum_k hidden[t, k] * w_k[h*D + d, k] )
+ *   v_cache[s / page_size, s % page_size, h, d] = bf16( sum_k hidden[t, k] * w_v[h*D + d, k] )
+ * with fp32 accumulation on the tensor cores (a bf16 rounding of the fp32 sum). Tokens
+ * with s < 0 are skipped (padding); s >= num_pages * page_size sets
+ * DFLASH_DEVERR_PAGE_ID in *device_error and is skipped.
+ *
+ *   hidden        device bf16 [num_tokens, hidden_size], row t at t * hidden_stride
+ *                 elements; 16-byte aligned, hidden_stride >= hidden_size, both
+ *                 multiples of 8.
+ *   w_k, w_v      device bf16 [num_kv_heads * head_dim, hidden_size], contiguous
+ *                 (the out x in layout of a linear layer's weight); 16-byte aligned.
+ *   slot_mapping  device int32 [num_tokens]: page * page_size + position in page.
+ *   k_cache, v_cache  device bf16, the layout of dflash_block_attn (dims->kv_stride_*,
+ *                 multiples of 8 elements, head_dim contiguous); written.
+ *   dims          num_kv_heads, head_dim (a multiple of 16, <= 512), page_size,
+ *                 num_pages, dtype (DFLASH_BF16) and the three strides are read; the
+ *                 other fields are ignored.
+ *   device_error  device uint32 word (bits OR-ed in; DFLASH_DEVERR_TIMEOUT if a bounded
+ *                 pipeline wait gave up) or NULL.
+ * Limits: 0 <= num_tokens <= DFLASH_PROJECT_MAX_TOKENS (0 is a no-op),
+ * num_kv_heads * head_dim <= 65536. Invalid arguments are reported before any launch.
+ * Asynchronous on `stream`; needs no workspace and allocates nothing.
+ */
+#define DFLASH_PROJECT_MAX_TOKENS (1 << 24)
+DFLASH_API dflash_status dflash_project_kv(const void* hidden, int32_t num_tokens, int32_t hidden_size,
+                                           int64_t hidden_stride, const void* w_k, const void* w_v,
+                                           const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                                           const dflash_dims* dims, uint32_t* device_error, void* stream);
+
 /* DFLASH_ABI_VERSION of the loaded library. */
 DFLASH_API int32_t dflash_abi_version(void);
 

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     abi_version,
     accept_prefix,
     accept_workspace_bytes,
+    project_kv,
     block_attn,
     block_attn_noalloc,
     load_library,

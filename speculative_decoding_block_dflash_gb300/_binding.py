@@ -40,6 +40,7 @@ EXPORTED = (
     "dflash_abi_version",
     "dflash_accept_prefix",
     "dflash_accept_workspace_bytes",
+    "dflash_project_kv",
 )
 
 
@@ -114,6 +115,8 @@ def load_library(path: Optional[str] = None):
         lib.dflash_accept_workspace_bytes.argtypes = [i32, i32]
         lib.dflash_accept_prefix.restype = ctypes.c_int
         lib.dflash_accept_prefix.argtypes = [vp, i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        lib.dflash_project_kv.restype = ctypes.c_int
+        lib.dflash_project_kv.argtypes = [vp, i32, i32, i64, vp, vp, vp, vp, vp, dims_p, vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -327,6 +330,50 @@ def accept_prefix(logits: torch.Tensor, draft: torch.Tensor, workspace: Optional
                                   _stream_handle(stream))
     _check(st)
     return accepted, next_token, target_argmax
+
+
+def project_kv(hidden: torch.Tensor, w_k: torch.Tensor, w_v: torch.Tensor, slot_mapping: torch.Tensor,
+               k_cache: torch.Tensor, v_cache: torch.Tensor, device_error: Optional[torch.Tensor] = None,
+               stream=None) -> None:
+    """Context K/V projection into the paged cache (dflash_project_kv): hidden [L, H] bf16
+    (rows of any stride, last dim contiguous), w_k / w_v [Hkv*D, H] bf16 contiguous,
+    slot_mapping int32 [L] (page * page_size + position; < 0 skips the token), caches
+    [num_pages, page_size, Hkv, D] bf16 (d contiguous, same strides). device_error: an
+    optional int32/uint32 device word that receives DEVERR_* bits."""
+    lib = load_library()
+    if hidden.dim() != 2 or hidden.stride(1) != 1:
+        raise ValueError("hidden must be [L, H] with a contiguous last dimension")
+    if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.stride() != v_cache.stride():
+        raise ValueError("k_cache and v_cache must be [num_pages, page_size, Hkv, D] of the same shape and strides")
+    if k_cache.stride(3) != 1:
+        raise ValueError("the caches' head_dim must be contiguous")
+    L, H = hidden.shape
+    N = k_cache.shape[2] * k_cache.shape[3]
+    for name, w in (("w_k", w_k), ("w_v", w_v)):
+        if tuple(w.shape) != (N, H) or not w.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [{N}, {H}] tensor")
+    if slot_mapping.dtype != torch.int32 or tuple(slot_mapping.shape) != (L,) or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous int32 [L] tensor")
+    for t in (hidden, w_k, w_v, k_cache, v_cache):
+        if t.dtype != torch.bfloat16:
+            raise TypeError("hidden, weights and caches must be bf16")
+    d = Dims()
+    d.batch = 1
+    d.num_q_heads = k_cache.shape[2]
+    d.num_kv_heads = k_cache.shape[2]
+    d.head_dim = k_cache.shape[3]
+    d.page_size = k_cache.shape[1]
+    d.num_pages = k_cache.shape[0]
+    d.max_pages = 1
+    d.max_seq_len = 0
+    d.dtype = BF16
+    d.kv_stride_page, d.kv_stride_slot, d.kv_stride_head = (int(s) for s in k_cache.stride()[:3])
+    st = lib.dflash_project_kv(hidden.data_ptr() if L else None, L, H, hidden.stride(0) if L else H,
+                               w_k.data_ptr(), w_v.data_ptr(), slot_mapping.data_ptr() if L else None,
+                               k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(d),
+                               device_error.data_ptr() if device_error is not None else None,
+                               _stream_handle(stream))
+    _check(st)
 
 
 def read_error(workspace: Optional[torch.Tensor] = None, clear: bool = True, stream=None) -> int:

@@ -415,6 +415,44 @@ dflash_status dflash_accept_prefix(const void* logits, dflash_dtype dtype, int32
     return DFLASH_OK;
 }
 
+dflash_status dflash_project_kv(const void* hidden, int32_t num_tokens, int32_t hidden_size, int64_t hidden_stride,
+                                const void* w_k, const void* w_v, const int32_t* slot_mapping, void* k_cache,
+                                void* v_cache, const dflash_dims* dims, uint32_t* device_error, void* stream)
+{
+    g_last_error.clear();
+    if (!dims) return fail(DFLASH_ERR_INVALID_ARG, "NULL dims");
+    if (dims->dtype != DFLASH_BF16) return fail(DFLASH_ERR_UNSUPPORTED, "the projection is bf16 only");
+    if (num_tokens < 0 || num_tokens > DFLASH_PROJECT_MAX_TOKENS)
+        return fail(DFLASH_ERR_INVALID_ARG, "num_tokens %d outside [0, %d]", num_tokens, DFLASH_PROJECT_MAX_TOKENS);
+    if (hidden_size < 8 || hidden_size % 8 != 0)
+        return fail(DFLASH_ERR_INVALID_ARG, "hidden_size %d must be a positive multiple of 8", hidden_size);
+    if (hidden_stride < hidden_size || hidden_stride % 8 != 0)
+        return fail(DFLASH_ERR_INVALID_ARG, "hidden_stride %lld must be >= hidden_size and a multiple of 8",
+                    (long long)hidden_stride);
+    const int32_t Hkv = dims->num_kv_heads, D = dims->head_dim;
+    if (Hkv < 1 || D < 16 || D > DFLASH_MAX_HEAD_DIM || D % 16 != 0)
+        return fail(DFLASH_ERR_INVALID_ARG, "num_kv_heads %d / head_dim %d (a multiple of 16 in [16, %d])", Hkv, D,
+                    DFLASH_MAX_HEAD_DIM);
+    if ((int64_t)Hkv * D > 65536) return fail(DFLASH_ERR_INVALID_ARG, "num_kv_heads * head_dim above 65536");
+    if (dims->page_size < 1 || dims->num_pages < 1)
+        return fail(DFLASH_ERR_INVALID_ARG, "page_size %d / num_pages %d must be >= 1", dims->page_size,
+                    dims->num_pages);
+    const int64_t sp = dims->kv_stride_page, ss = dims->kv_stride_slot, sh = dims->kv_stride_head;
+    if (sp < 0 || ss < 0 || sh < 0 || sp % 8 || ss % 8 || sh % 8)
+        return fail(DFLASH_ERR_INVALID_ARG, "cache strides must be non-negative multiples of 8 elements");
+    if (num_tokens == 0) return DFLASH_OK;
+    if (!hidden || !w_k || !w_v || !slot_mapping || !k_cache || !v_cache)
+        return fail(DFLASH_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(hidden, 16) || !aligned(w_k, 16) || !aligned(w_v, 16) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || !aligned(slot_mapping, 4) || (device_error && !aligned(device_error, 4)))
+        return fail(DFLASH_ERR_INVALID_ARG, "misaligned pointer (16 bytes; slot_mapping and device_error 4)");
+    const cudaError_t e = launch_project_kv(hidden, num_tokens, hidden_size, hidden_stride, w_k, w_v, slot_mapping,
+                                            k_cache, v_cache, Hkv, D, dims->page_size, dims->num_pages, sp, ss, sh,
+                                            device_error, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "projection kernel launch");
+    return DFLASH_OK;
+}
+
 dflash_status dflash_split_combine(const float* partial_out, const float* partial_lse, int32_t num_splits,
                                    int64_t num_rows, int32_t head_dim, dflash_dtype out_dtype, void* out, float* lse,
                                    void* stream)

@@ -52,6 +52,13 @@ cudaError_t launch_accept(const void* logits, int32_t dtype, int32_t B, int32_t 
                           const int32_t* draft, int32_t* accepted, int32_t* next_token, int32_t* target_argmax,
                           unsigned long long* keys, int32_t* counters, cudaStream_t stream);
 
+// Context K/V projection (csrc/project_kv.cu): persistent CTAs (at most one per SM).
+int32_t project_kv_grid(int32_t L, int32_t N);
+cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t hidden_stride, const void* w_k,
+                              const void* w_v, const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                              int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages, int64_t sp, int64_t ss,
+                              int64_t sh, uint32_t* err, cudaStream_t stream);
+
 // Slots of the tensor-core kernel's length-balanced split plan for these sizes (auto split
 // count, B > 1, whole grid resident), or 0 when the plan is uniform.
 int32_t balanced_slots(const dflash_dims* d, int32_t T, int32_t window, int kernel);

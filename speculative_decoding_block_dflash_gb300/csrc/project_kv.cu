@@ -1,0 +1,357 @@
+// Context K/V projection for the draft pass, fused with the paged-cache write.
+//
+// The drafter's cross-attention reads context K/V computed from the target's hidden states
+// (kenforever1 "dflash-gemma4-31b-notes", the code lines under "why non-causal attention";
+// the vLLM DFlash review's risk list names this precompute as a bare linear layer). For
+// every token t with cache slot s_t >= 0:
+//   K[s_t, h, d] = bf16( sum_k hidden[t, k] * W_k[h*D + d, k] )   (fp32 accumulation)
+//   V[s_t, h, d] = bf16( sum_k hidden[t, k] * W_v[h*D + d, k] )
+// where slot s maps to page s / page_size, position s % page_size.
+//
+// One persistent CTA per SM walks output tiles of 128 tokens x 256 features (of K or of V),
+// the tile index t = m * (2 * n_half) + nt (feature tiles fastest, so that the CTAs running at
+// once share their hidden rows and the whole weight set stays in L2). Warp roles:
+//   warp 0     TMA producer: per 64-wide slice of the hidden dimension, a 128 x 64 box of
+//              hidden and a 256 x 64 box of the weight (both 128-byte swizzled) into a
+//              4-stage ring;
+//   warp 1     MMA issuer: tcgen05.mma M=128 N=256 K=16, fp32 accumulator in TMEM, two
+//              accumulators (2 x 256 columns) so the epilogue of one tile overlaps the
+//              main loop of the next;
+//   warps 2-5  epilogue: thread = token row (TMEM lane), 16 columns at a time, bf16 pack and
+//              two 16-byte stores into the token's cache slot.
+// Rows past the token count and hidden columns past H are zero-filled by the tensor copies.
+// Every wait is bounded (DFLASH_DEVERR_TIMEOUT, the kernel returns).
+#include <mutex>
+
+#include "tc_ptx.cuh"
+
+namespace dflash {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;  // tokens per tile
+constexpr int kBN = 256;  // features per tile
+constexpr int kBK = 64;   // hidden elements per stage (128 bytes: one swizzle row)
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmaWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kTmemCols = 2 * kBN;
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 5;  // full, empty, acc_full[2], acc_empty[2], drain
+constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kSmemUsed = kMiscOff + 16;
+constexpr int kAlloc = kSmemUsed + 1024;  // the ring is aligned up to 1024 bytes (swizzle atoms)
+static_assert(kAlloc <= 227 * 1024, "shared memory");
+
+struct ProjParams {
+    const int32_t* slot_mapping;
+    __nv_bfloat16* k_cache;
+    __nv_bfloat16* v_cache;
+    uint32_t* err;
+    int32_t L, H, N, D, page_size;
+    int32_t n_half;  // feature tiles of one projection: ceil(N / kBN)
+    int32_t tiles;   // ceil(L / kBM) * 2 * n_half
+    int64_t total_slots;
+    int64_t sp, ss, sh;
+};
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 16 fp32 accumulator columns -> 16 bf16 at dst (16-byte aligned).
+__device__ __forceinline__ void store16(__nv_bfloat16* dst, const uint32_t (&r)[16])
+{
+    uint4 a, b;
+    a.x = pack_bf16x2(r[0], r[1]);
+    a.y = pack_bf16x2(r[2], r[3]);
+    a.z = pack_bf16x2(r[4], r[5]);
+    a.w = pack_bf16x2(r[6], r[7]);
+    b.x = pack_bf16x2(r[8], r[9]);
+    b.y = pack_bf16x2(r[10], r[11]);
+    b.z = pack_bf16x2(r[12], r[13]);
+    b.w = pack_bf16x2(r[14], r[15]);
+    reinterpret_cast<uint4*>(dst)[0] = a;
+    reinterpret_cast<uint4*>(dst)[1] = b;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    project_kv_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_wk,
+                      const __grid_constant__ CUtensorMap tm_wv, const ProjParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = smem;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
+    uint64_t* full = bars;                  // [kStages] TMA -> MMA: stage landed
+    uint64_t* empty = bars + kStages;       // [kStages] MMA -> TMA: stage consumed
+    uint64_t* acc_full = bars + 2 * kStages;  // [2] MMA -> epilogue: accumulator a holds a finished tile
+    uint64_t* acc_empty = acc_full + 2;     // [2] epilogue -> MMA: accumulator a read out
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int KB = (p.H + kBK - 1) / kBK;
+    const int row_tiles = 2 * p.n_half;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full + a, 1);
+            mbar_init(acc_empty + a, kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ TMA producer
+        bool ok = true;
+        uint32_t issued_par[kStages];
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) issued_par[s] = 2;  // 2 = nothing issued
+        int seq = 0;
+        for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+            const int m = t / row_tiles;
+            const int nt = t - m * row_tiles;
+            const bool is_v = nt >= p.n_half;
+            const int col0 = (is_v ? nt - p.n_half : nt) * kBN;
+            const CUtensorMap* tw = is_v ? &tm_wv : &tm_wk;
+            for (int kb = 0; kb < KB; ++kb, ++seq) {
+                const int s = seq % kStages;
+                const uint32_t ph = (uint32_t)(seq / kStages) & 1u;
+                if (lane == 0) ok = wait_bounded(empty + s, ph ^ 1u, abort_flag, p.err);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                if (lane == 0) {
+                    uint8_t* st = ring + s * kStageBytes;
+                    mbar_expect_tx(full + s, kStageBytes);
+                    tma_load_2d(st, &tm_h, full + s, kb * kBK, m * kBM);
+                    tma_load_2d(st + kABytes, tw, full + s, kb * kBK, col0);
+                    issued_par[s] = ph;
+                }
+                __syncwarp();
+            }
+        }
+        // On an abort, no copy of ours may still be landing when the CTA exits.
+        if (lane == 0 && !ok) {
+            for (int s = 0; s < kStages; ++s) {
+                if (issued_par[s] > 1) continue;
+                const unsigned long long t_start = globaltimer();
+                while (!mbar_try_wait(full + s, issued_par[s]) && globaltimer() - t_start < kTimeoutNs) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t idesc = make_idesc(kBM, kBN, 0, 0);  // A (hidden) and B (weight) K-major
+        const uint32_t ring_addr = smem_u32(ring);
+        bool ok = true;
+        int seq = 0;
+        int i = 0;
+        for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++i) {
+            const int a = i & 1;
+            const uint32_t acc = tmem + (uint32_t)(a * kBN);
+            // the epilogue has read out this accumulator's previous tile
+            if (lane == 0) ok = wait_bounded(acc_empty + a, ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, p.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            for (int kb = 0; kb < KB; ++kb, ++seq) {
+                const int s = seq % kStages;
+                const uint32_t ph = (uint32_t)(seq / kStages) & 1u;
+                if (lane == 0) ok = wait_bounded(full + s, ph, abort_flag, p.err);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sa = ring_addr + (uint32_t)(s * kStageBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        tc_mma(acc, sw128_desc(sa + kk * 32, 16, 1024), sw128_desc(sa + kABytes + kk * 32, 16, 1024),
+                               idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(empty + s);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(acc_full + a);
+            __syncwarp();
+        }
+        // Our MMAs are complete before TMEM is released.
+        if (lane == 0) {
+            tc_commit(drain);
+            const unsigned long long t_start = globaltimer();
+            while (!mbar_try_wait(drain, 0) && globaltimer() - t_start < kTimeoutNs) {
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (thread = token row)
+        const int quarter = warp & 3;  // the TMEM lane quarter this warp may read
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        int i = 0;
+        for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++i) {
+            const int a = i & 1;
+            const int m = t / row_tiles;
+            const int nt = t - m * row_tiles;
+            const bool is_v = nt >= p.n_half;
+            const int col0 = (is_v ? nt - p.n_half : nt) * kBN;
+            const int ncols = min(kBN, p.N - col0);  // a multiple of 16
+            const int row = m * kBM + quarter * 32 + lane;
+            __nv_bfloat16* dst = nullptr;  // this token's slot, or none
+            if (row < p.L) {
+                const int32_t slot = __ldg(p.slot_mapping + row);
+                if (slot >= 0) {
+                    if ((int64_t)slot < p.total_slots)
+                        dst = (is_v ? p.v_cache : p.k_cache) + (int64_t)(slot / p.page_size) * p.sp +
+                              (int64_t)(slot % p.page_size) * p.ss;
+                    else
+                        raise_error(p.err, DFLASH_DEVERR_PAGE_ID);
+                }
+            }
+            bool ok = true;
+            if (lane == 0) ok = wait_bounded(acc_full + a, (uint32_t)(i >> 1) & 1u, abort_flag, p.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t acc = tmem + lane_base + (uint32_t)(a * kBN);
+            for (int c = 0; c < ncols; c += 32) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(acc + c, r0);
+                tmem_ld16(acc + c + 16, r1);  // inside the accumulator even when past ncols
+                tmem_ld_wait();
+                reg_fence16(r0);
+                reg_fence16(r1);
+                if (dst) {
+                    const int f0 = col0 + c;  // feature of column c: head f / D, dim f % D
+                    store16(dst + (int64_t)(f0 / p.D) * p.sh + f0 % p.D, r0);
+                    if (c + 16 < ncols) {
+                        const int f1 = f0 + 16;
+                        store16(dst + (int64_t)(f1 / p.D) * p.sh + f1 % p.D, r1);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + a);
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2D bf16 map of `rows` rows of `cols` elements (row stride `stride` elements), box 64 x box_rows,
+// 128-byte swizzle; out-of-range elements read as zero.
+bool encode_2d(EncodeTiledFn enc, CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int64_t stride,
+               int box_rows)
+{
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int32_t project_kv_grid(int32_t L, int32_t N)
+{
+    const int64_t tiles = (int64_t)((L + kBM - 1) / kBM) * 2 * ((N + kBN - 1) / kBN);
+    return (int32_t)std::min<int64_t>(tiles, device_sm_count());
+}
+
+cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t hidden_stride, const void* w_k,
+                              const void* w_v, const int32_t* slot_mapping, void* k_cache, void* v_cache,
+                              int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages, int64_t sp, int64_t ss,
+                              int64_t sh, uint32_t* err, cudaStream_t stream)
+{
+    if (L == 0) return cudaSuccess;
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int32_t N = Hkv * D;
+    CUtensorMap th, twk, twv;
+    if (!encode_2d(enc, &th, hidden, H, L, hidden_stride, kBM) || !encode_2d(enc, &twk, w_k, H, N, H, kBN) ||
+        !encode_2d(enc, &twv, w_v, H, N, H, kBN))
+        return cudaErrorInvalidValue;
+    ProjParams p;
+    p.slot_mapping = slot_mapping;
+    p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+    p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+    p.err = err;
+    p.L = L;
+    p.H = H;
+    p.N = N;
+    p.D = D;
+    p.page_size = page_size;
+    p.n_half = (N + kBN - 1) / kBN;
+    p.tiles = ((L + kBM - 1) / kBM) * 2 * p.n_half;
+    p.total_slots = (int64_t)num_pages * page_size;
+    p.sp = sp;
+    p.ss = ss;
+    p.sh = sh;
+    cudaError_t e = cudaFuncSetAttribute(project_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+    if (e != cudaSuccess) return e;
+    project_kv_kernel<<<project_kv_grid(L, N), kThreads, kAlloc, stream>>>(th, twk, twv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace dflash

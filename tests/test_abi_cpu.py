@@ -232,3 +232,35 @@ def test_accept_workspace_and_argument_checks(lib):
     assert acc(ws_bytes=64) == B.ERR_WORKSPACE
     assert acc(ws=FAKE + 16) == B.ERR_WORKSPACE
     assert b"workspace" in lib.dflash_last_error_message()
+
+
+@cpu_only
+def test_project_kv_argument_checks(lib):
+    P = ctypes.c_void_p
+
+    def proj(L=64, H=5376, stride=5376, hidden=FAKE, wk=FAKE, wv=FAKE, slots=FAKE, kc=FAKE, vc=FAKE, err=None,
+             **dkw):
+        d = good_dims(**dkw)
+        return lib.dflash_project_kv(P(hidden), L, H, stride, P(wk), P(wv), P(slots), P(kc), P(vc),
+                                     ctypes.byref(d), P(err) if err else None, None)
+
+    assert proj(L=0, hidden=None, slots=None) == B.OK  # no tokens: nothing is read or launched
+    assert proj(dtype=B.FP32) == B.ERR_UNSUPPORTED
+    assert proj(L=-1) == B.ERR_INVALID_ARG
+    assert proj(L=(1 << 24) + 1) == B.ERR_INVALID_ARG
+    assert proj(H=5370, stride=5370) == B.ERR_INVALID_ARG   # hidden size not a multiple of 8
+    assert proj(stride=5368) == B.ERR_INVALID_ARG           # row stride shorter than a row
+    assert proj(stride=5380) == B.ERR_INVALID_ARG           # row stride not a multiple of 8
+    assert proj(head_dim=24) == B.ERR_INVALID_ARG           # head_dim not a multiple of 16
+    assert proj(head_dim=1024) == B.ERR_INVALID_ARG
+    assert proj(num_kv_heads=0) == B.ERR_INVALID_ARG
+    assert proj(page_size=0) == B.ERR_INVALID_ARG
+    assert proj(num_pages=0) == B.ERR_INVALID_ARG
+    assert proj(kv_stride_head=516) == B.ERR_INVALID_ARG
+    assert proj(hidden=None) == B.ERR_INVALID_ARG
+    assert proj(slots=None) == B.ERR_INVALID_ARG
+    assert proj(kc=FAKE + 8) == B.ERR_INVALID_ARG           # caches 16-byte aligned
+    assert proj(wk=FAKE + 2) == B.ERR_INVALID_ARG
+    assert proj(slots=FAKE + 2) == B.ERR_INVALID_ARG
+    assert proj(err=FAKE + 1) == B.ERR_INVALID_ARG
+    assert b"misaligned" in lib.dflash_last_error_message()
