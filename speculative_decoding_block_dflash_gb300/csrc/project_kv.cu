@@ -8,19 +8,23 @@
 //   V[s_t, h, d] = bf16( sum_k hidden[t, k] * W_v[h*D + d, k] )
 // where slot s maps to page s / page_size, position s % page_size.
 //
-// One persistent CTA per SM walks output tiles of 128 tokens x 256 features (of K or of V),
+// One persistent CTA per SM walks output tiles of 256 tokens x 256 features (of K or of V),
 // the tile index t = m * (2 * n_half) + nt (feature tiles fastest, so that the CTAs running at
 // once share their hidden rows and the whole weight set stays in L2). Warp roles:
-//   warp 0     TMA producer: per 64-wide slice of the hidden dimension, a 128 x 64 box of
+//   warp 0     TMA producer: per 64-wide slice of the hidden dimension, a 256 x 64 box of
 //              hidden and a 256 x 64 box of the weight (both 128-byte swizzled) into a
-//              4-stage ring;
-//   warp 1     MMA issuer: tcgen05.mma M=128 N=256 K=16, fp32 accumulator in TMEM, two
-//              accumulators (2 x 256 columns) so the epilogue of one tile overlaps the
-//              main loop of the next;
-//   warps 2-5  epilogue: thread = token row (TMEM lane), 16 columns at a time, bf16 pack and
-//              two 16-byte stores into the token's cache slot.
-// Rows past the token count and hidden columns past H are zero-filled by the tensor copies.
-// Every wait is bounded (DFLASH_DEVERR_TIMEOUT, the kernel returns).
+//              3-stage ring;
+//   warp 1     MMA issuer: two tcgen05.mma M=128 N=256 K=16 per 16-wide step (token rows
+//              0-127 and 128-255 against the same weight rows), fp32 accumulators in all
+//              512 TMEM columns;
+//   warps 2-9  epilogue: two warps per TMEM lane quarter (one per accumulator), thread =
+//              token row, 16 columns at a time, bf16 pack and two 16-byte stores into the
+//              token's cache slot.
+// A 256-row tile halves the bytes each SM must land per flop against a 128-row one: the
+// tensor copies into one SM, not the MMAs, bound this kernel. A tile whose second half lies
+// wholly past the last token skips that half's MMAs. Rows past the token count and hidden
+// columns past H are zero-filled by the tensor copies. Every wait is bounded
+// (DFLASH_DEVERR_TIMEOUT, the kernel returns).
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -30,20 +34,20 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBM = 128;  // tokens per tile
+constexpr int kBM = 256;  // tokens per tile (two 128-row MMA halves)
 constexpr int kBN = 256;  // features per tile
 constexpr int kBK = 64;   // hidden elements per stage (128 bytes: one swizzle row)
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTmaWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kTmemCols = 2 * kBN;
+constexpr int kTmemCols = 2 * kBN;  // accumulator of rows 0-127 in columns [0, 256), rows 128-255 in [256, 512)
 constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 5;  // full, empty, acc_full[2], acc_empty[2], drain
+constexpr int kNumBars = 2 * kStages + 3;  // full, empty, acc_full, acc_empty, drain
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemUsed = kMiscOff + 16;
 constexpr int kAlloc = kSmemUsed + 1024;  // the ring is aligned up to 1024 bytes (swizzle atoms)
@@ -102,9 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
     uint64_t* full = bars;                  // [kStages] TMA -> MMA: stage landed
     uint64_t* empty = bars + kStages;       // [kStages] MMA -> TMA: stage consumed
-    uint64_t* acc_full = bars + 2 * kStages;  // [2] MMA -> epilogue: accumulator a holds a finished tile
-    uint64_t* acc_empty = acc_full + 2;     // [2] epilogue -> MMA: accumulator a read out
-    uint64_t* drain = acc_empty + 2;
+    uint64_t* acc_full = bars + 2 * kStages;  // MMA -> epilogue: the accumulators hold a finished tile
+    uint64_t* acc_empty = acc_full + 1;     // epilogue -> MMA: the accumulators have been read out
+    uint64_t* drain = acc_empty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
     const int warp = threadIdx.x >> 5;
@@ -117,10 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(acc_full + a, 1);
-            mbar_init(acc_empty + a, kEpiWarps);
-        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, kEpiWarps);
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -175,16 +177,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = make_idesc(kBM, kBN, 0, 0);  // A (hidden) and B (weight) K-major
+        constexpr uint32_t idesc = make_idesc(kBM / 2, kBN, 0, 0);  // A (hidden) and B (weight) K-major
         const uint32_t ring_addr = smem_u32(ring);
         bool ok = true;
         int seq = 0;
         int i = 0;
         for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++i) {
-            const int a = i & 1;
-            const uint32_t acc = tmem + (uint32_t)(a * kBN);
-            // the epilogue has read out this accumulator's previous tile
-            if (lane == 0) ok = wait_bounded(acc_empty + a, ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, p.err);
+            const int m = t / row_tiles;
+            const bool two = m * kBM + kBM / 2 < p.L;  // the second 128-row half holds tokens
+            // the epilogue has read out the previous tile
+            if (lane == 0) ok = wait_bounded(acc_empty, ((uint32_t)i & 1u) ^ 1u, abort_flag, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
@@ -197,16 +199,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if (lane == 0) {
                     const uint32_t sa = ring_addr + (uint32_t)(s * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc_mma(acc, sw128_desc(sa + kk * 32, 16, 1024), sw128_desc(sa + kABytes + kk * 32, 16, 1024),
-                               idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        const uint64_t bdesc = sw128_desc(sb + kk * 32, 16, 1024);
+                        const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
+                        tc_mma(tmem, sw128_desc(sa + kk * 32, 16, 1024), bdesc, idesc, acc_flag);
+                        if (two)
+                            tc_mma(tmem + kBN, sw128_desc(sa + kABytes / 2 + kk * 32, 16, 1024), bdesc, idesc,
+                                   acc_flag);
+                    }
                     tc_commit(empty + s);
                 }
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(acc_full + a);
+            if (lane == 0) tc_commit(acc_full);
             __syncwarp();
         }
         // Our MMAs are complete before TMEM is released.
@@ -219,17 +227,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue (thread = token row)
-        const int quarter = warp & 3;  // the TMEM lane quarter this warp may read
-        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const int quarter = warp & 3;           // the TMEM lane quarter this warp may read
+        const int half = (warp - 2) >> 2;       // 0: rows 0-127 of the tile, 1: rows 128-255
+        const uint32_t acc = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * kBN);
         int i = 0;
         for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++i) {
-            const int a = i & 1;
             const int m = t / row_tiles;
             const int nt = t - m * row_tiles;
             const bool is_v = nt >= p.n_half;
             const int col0 = (is_v ? nt - p.n_half : nt) * kBN;
             const int ncols = min(kBN, p.N - col0);  // a multiple of 16
-            const int row = m * kBM + quarter * 32 + lane;
+            const bool active = m * kBM + half * (kBM / 2) < p.L;  // this half was computed
+            const int row = m * kBM + half * (kBM / 2) + quarter * 32 + lane;
             __nv_bfloat16* dst = nullptr;  // this token's slot, or none
             if (row < p.L) {
                 const int32_t slot = __ldg(p.slot_mapping + row);
@@ -242,30 +251,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             bool ok = true;
-            if (lane == 0) ok = wait_bounded(acc_full + a, (uint32_t)(i >> 1) & 1u, abort_flag, p.err);
+            if (lane == 0) ok = wait_bounded(acc_full, (uint32_t)i & 1u, abort_flag, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t acc = tmem + lane_base + (uint32_t)(a * kBN);
-            for (int c = 0; c < ncols; c += 32) {
-                uint32_t r0[16], r1[16];
-                tmem_ld16(acc + c, r0);
-                tmem_ld16(acc + c + 16, r1);  // inside the accumulator even when past ncols
-                tmem_ld_wait();
-                reg_fence16(r0);
-                reg_fence16(r1);
-                if (dst) {
-                    const int f0 = col0 + c;  // feature of column c: head f / D, dim f % D
-                    store16(dst + (int64_t)(f0 / p.D) * p.sh + f0 % p.D, r0);
-                    if (c + 16 < ncols) {
-                        const int f1 = f0 + 16;
-                        store16(dst + (int64_t)(f1 / p.D) * p.sh + f1 % p.D, r1);
+            if (active) {
+                for (int c = 0; c < ncols; c += 32) {
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(acc + c, r0);
+                    tmem_ld16(acc + c + 16, r1);  // inside the accumulator even when past ncols
+                    tmem_ld_wait();
+                    reg_fence16(r0);
+                    reg_fence16(r1);
+                    if (dst) {
+                        const int f0 = col0 + c;  // feature of column c: head f / D, dim f % D
+                        store16(dst + (int64_t)(f0 / p.D) * p.sh + f0 % p.D, r0);
+                        if (c + 16 < ncols) {
+                            const int f1 = f0 + 16;
+                            store16(dst + (int64_t)(f1 / p.D) * p.sh + f1 % p.D, r1);
+                        }
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty + a);
+            if (lane == 0) mbar_arrive(acc_empty);
         }
     }
 
