@@ -499,22 +499,36 @@ def project_bench(args, dfl, dev, rank, world):
     ms = ev0.elapsed_time(ev1) / args.steps
     flops = project_flops()
     value = world * flops / (ms * 1e-3) / 1e12
-    # end to end: the hidden states and slot mapping in from pinned memory, the error word back
+    # end to end: the hidden states and slot mapping in from pinned memory, the error word back,
+    # every step. The inputs are double-buffered: a copy stream loads step k+1's hidden states
+    # while the kernel of step k runs.
     h_h = sets[0][0].cpu().pin_memory()
     s_h = slots.cpu().pin_memory()
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     err_h = torch.empty(1, dtype=torch.int32).pin_memory()
-    hidden_d = torch.empty_like(sets[0][0])
-    n_e2e = max(1, min(args.steps, 20))
+    hbuf = [torch.empty_like(sets[0][0]) for _ in range(2)]
+    sbuf = [torch.empty_like(slots) for _ in range(2)]
+    copied = [torch.cuda.Event() for _ in range(2)]
+    used = [torch.cuda.Event() for _ in range(2)]
+    copier = torch.cuda.Stream(dev)
+    n_e2e = max(2, min(args.steps, 20))
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    copier.wait_event(e0)
     for k in range(n_e2e):
-        hidden_d.copy_(h_h, non_blocking=True)
-        slots.copy_(s_h, non_blocking=True)
+        j = k % 2
+        with torch.cuda.stream(copier):
+            if k >= 2:
+                copier.wait_event(used[j])
+            hbuf[j].copy_(h_h, non_blocking=True)
+            sbuf[j].copy_(s_h, non_blocking=True)
+            copied[j].record(copier)
+        stream.wait_event(copied[j])
         _, w_k, w_v = sets[k % n_sets]
-        dfl.project_kv(hidden_d, w_k, w_v, slots, k_cache, v_cache, device_error=err)
+        dfl.project_kv(hbuf[j], w_k, w_v, sbuf[j], k_cache, v_cache, device_error=err)
+        used[j].record(stream)
         err_h.copy_(err, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -541,14 +555,161 @@ def project_bench(args, dfl, dev, rank, world):
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h_h.numel() * 2 + s_h.numel() * 4, "d2h_bytes_per_step": 4,
                 "ms_per_step": e2e_ms,
-                "note": "public Python API; hidden states and slot mapping in from pinned host memory and the "
-                        "error word back, every step; the weights and the paged cache stay resident"},
+                "note": "public Python API; hidden states and slot mapping in from pinned host memory (double-"
+                        "buffered on a copy stream) and the error word back, every step; the weights and the "
+                        "paged cache stay resident"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "tensor", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
                      "frac": value / world / peak, "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "project_kv_kernel",
                      "achieved_basis": "2*L*H*(2*Hkv*D) flops per launch / event-timed device time per step",
                      "traffic_note": tnote},
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- DFlash2 grouped convolution
+
+
+CONV_CONFIG = "conv_block"
+CONV_DESC = ("DFlash2 grouped dynamic depthwise convolution over drafted blocks: 32 requests x 16 positions "
+             "(1 + 15 speculative tokens, the DFlash2 default), 5120 channels in 8 contiguous groups, 4 taps, bf16 "
+             "activations with fp32 static and dynamic taps (synthetic; the pages state neither the width, the "
+             "group count nor the tap count)")
+CONV_SHAPE = dict(B=32, T=16, C=5120, taps=4, G=8)
+
+
+def conv_inputs(dev, n_sets, seed=2468):
+    sh = CONV_SHAPE
+    g = torch.Generator(device=dev).manual_seed(seed)
+    sets = []
+    for _ in range(n_sets):
+        x = torch.randn((sh["B"], sh["T"], sh["C"]), generator=g, device=dev).to(torch.bfloat16)
+        delta = torch.randn((sh["B"], sh["T"], sh["taps"], sh["G"]), generator=g, device=dev) * 0.25
+        sets.append((x, delta, torch.empty_like(x)))
+    base = torch.randn((sh["taps"], sh["C"]), generator=g, device=dev) * 0.5
+    return sets, base
+
+
+def conv_bytes():
+    sh = CONV_SHAPE
+    return (2 * sh["B"] * sh["T"] * sh["C"] * 2 + sh["B"] * sh["T"] * sh["taps"] * sh["G"] * 4
+            + sh["taps"] * sh["C"] * 4)
+
+
+def conv_oracle_rate(budget_s):
+    from oracle import grouped_conv as oc
+
+    sh = CONV_SHAPE
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((sh["B"], sh["T"], sh["C"]))
+    base = rng.standard_normal((sh["taps"], sh["C"]))
+    delta = rng.standard_normal((sh["B"], sh["T"], sh["taps"], sh["G"]))
+    t0 = time.perf_counter()
+    n = 0
+    while n == 0 or time.perf_counter() - t0 < budget_s:
+        oc.grouped_conv(x, base, delta)
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return conv_bytes() / dt / 1e9, f"{n} full oracle calls (float64 numpy loop over positions and taps)"
+
+
+def conv_reference_arm(args):
+    budget = max(1.0, min(args.ref_budget, 120.0)) / max(1, args.steps + args.warmup)
+    rate, sample = conv_oracle_rate(budget)
+    ms = conv_bytes() / (rate * 1e9) * 1e3
+    line = {"impl": "reference", "metric": "conv_hbm_gbs", "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": CONV_DESC},
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def conv_bench(args, dfl, dev, rank, world):
+    per = conv_bytes()
+    n_sets = args.layers or max(2, math.ceil(4 * L2_BYTES / per))
+    sets, base = conv_inputs(dev, n_sets)
+    side = torch.cuda.Stream(dev)
+    with torch.cuda.stream(side):
+        for x, delta, out in sets:
+            dfl.grouped_conv(x, base, delta, out=out, stream=side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for x, delta, out in sets:
+            dfl.grouped_conv(x, base, delta, out=out, stream=side)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, math.ceil(args.steps / n_sets))
+    steps = reps * n_sets
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if rank == 0:
+        sampler.stop()
+    ms = ev0.elapsed_time(ev1) / steps
+    value = world * per / (ms * 1e-3) / 1e9
+    # end to end: x and delta in from pinned memory, out back, every step
+    x0, d0, o0 = sets[0]
+    x_h = x0.cpu().pin_memory()
+    d_h = d0.cpu().pin_memory()
+    o_h = torch.empty_like(o0, device="cpu").pin_memory()
+    n_e2e = max(1, min(steps, 200))
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        x0.copy_(x_h, non_blocking=True)
+        d0.copy_(d_h, non_blocking=True)
+        dfl.grouped_conv(x0, base, d0, out=o0)
+        o_h.copy_(o0, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, sample = conv_oracle_rate(min(args.cpu_budget, 10.0))
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+    sh = CONV_SHAPE
+    line = {
+        "metric": "conv_hbm_gbs", "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": CONV_DESC, "global_batch": sh["B"] * world, "block_len": sh["T"],
+                   "channels": sh["C"], "taps": sh["taps"], "groups": sh["G"],
+                   "l2": f"inputs larger than L2: {n_sets} rotated (x, delta, out) sets x {per / 1e6:.2f} MB",
+                   "timed_path": f"CUDA-graph replays of {n_sets} dflash_grouped_conv calls, one per step",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": world * per / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": x_h.numel() * 2 + d_h.numel() * 4, "d2h_bytes_per_step": o_h.numel() * 2,
+                "ms_per_step": e2e_ms,
+                "note": "public Python API; x and delta in from pinned host memory, out back, every step"},
+        "gpu_launches": steps,
+        "roofline": {"bound": "hbm", "achieved": value / world, "peak": peak, "unit": "GB/s",
+                     "frac": value / world / peak, "traffic": traffic_from_profiles("grouped_conv_kernel")[0],
+                     "peak_kind": peak_kind, "kernel": "grouped_conv_kernel",
+                     "achieved_basis": "x read + out written + delta + base bytes per launch / event-timed time"},
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
     if cpu:
@@ -634,6 +795,11 @@ def main():
             if dist:
                 dist.destroy_process_group()
             return
+        if args.config == CONV_CONFIG:
+            conv_reference_arm(args)
+            if dist:
+                dist.destroy_process_group()
+            return
         import workloads
 
         case = workloads.make_case(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
@@ -661,6 +827,11 @@ def main():
         return
     if args.config == PROJECT_CONFIG:
         project_bench(args, dfl, dev, rank, world)
+        if dist:
+            dist.destroy_process_group()
+        return
+    if args.config == CONV_CONFIG:
+        conv_bench(args, dfl, dev, rank, world)
         if dist:
             dist.destroy_process_group()
         return

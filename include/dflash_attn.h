@@ -317,6 +317,30 @@ DFLASH_API dflash_status dflash_project_kv(const void* hidden, int32_t num_token
                                            const int32_t* slot_mapping, void* k_cache, void* v_cache,
                                            const dflash_dims* dims, uint32_t* device_error, void* stream);
 
+/*
+ * DFlash2 grouped dynamic depthwise convolution inside a drafted block (prhub report on vLLM
+ * PR #52816 "DFlash2", the motivation paragraph and change 1: proposal positions see earlier
+ * positions of the same block without another backbone pass). For request b, block
+ * position i and channel c:
+ *   out[b, i, c] = sum over t < num_taps with t <= i of
+ *                  (base[t, c] + delta[b, i, t, g(c)]) * x[b, i - t, c]
+ * with g(c) = c / (channels / num_groups): contiguous channel groups. Taps that reach past the
+ * start of the request's block contribute zero. fp32 accumulation; out is rounded to dtype.
+ *
+ *   x, out     device, [batch, block_len, channels] contiguous, dtype (bf16 or fp32), aligned to
+ *              the element size; out must not overlap x.
+ *   base       device float32 [num_taps, channels]: the static per-channel taps.
+ *   delta      device float32 [batch, block_len, num_taps, num_groups]: the dynamic taps of each
+ *              position and group (what the module's "prepare" step projects from its input).
+ * Limits: 1 <= batch <= 65535, 1 <= block_len, num_taps <= DFLASH_MAX_BLOCK_LEN, channels a
+ * positive multiple of num_groups. Invalid arguments are reported before any launch.
+ * Asynchronous on `stream`; needs no workspace.
+ */
+DFLASH_API dflash_status dflash_grouped_conv(const void* x, void* out, dflash_dtype dtype, int32_t batch,
+                                             int32_t block_len, int32_t channels, int32_t num_taps,
+                                             int32_t num_groups, const float* base, const float* delta,
+                                             void* stream);
+
 /* DFLASH_ABI_VERSION of the loaded library. */
 DFLASH_API int32_t dflash_abi_version(void);
 

@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     accept_prefix,
     accept_workspace_bytes,
     project_kv,
+    grouped_conv,
     block_attn,
     block_attn_noalloc,
     load_library,

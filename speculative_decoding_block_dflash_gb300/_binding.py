@@ -41,6 +41,7 @@ EXPORTED = (
     "dflash_accept_prefix",
     "dflash_accept_workspace_bytes",
     "dflash_project_kv",
+    "dflash_grouped_conv",
 )
 
 
@@ -117,6 +118,8 @@ def load_library(path: Optional[str] = None):
         lib.dflash_accept_prefix.argtypes = [vp, i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.dflash_project_kv.restype = ctypes.c_int
         lib.dflash_project_kv.argtypes = [vp, i32, i32, i64, vp, vp, vp, vp, vp, dims_p, vp, vp]
+        lib.dflash_grouped_conv.restype = ctypes.c_int
+        lib.dflash_grouped_conv.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -374,6 +377,30 @@ def project_kv(hidden: torch.Tensor, w_k: torch.Tensor, w_v: torch.Tensor, slot_
                                device_error.data_ptr() if device_error is not None else None,
                                _stream_handle(stream))
     _check(st)
+
+
+def grouped_conv(x: torch.Tensor, base: torch.Tensor, delta: torch.Tensor, out: Optional[torch.Tensor] = None,
+                 stream=None) -> torch.Tensor:
+    """DFlash2 grouped dynamic depthwise convolution (dflash_grouped_conv): x [B, T, C] bf16/fp32,
+    base float32 [taps, C], delta float32 [B, T, taps, G] -> out [B, T, C] of x's dtype."""
+    lib = load_library()
+    if x.dim() != 3 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [B, T, C] tensor")
+    B, T, C = x.shape
+    if base.dim() != 2 or base.shape[1] != C or base.dtype != torch.float32 or not base.is_contiguous():
+        raise ValueError("base must be a contiguous float32 [taps, C] tensor")
+    taps = base.shape[0]
+    if (delta.dim() != 4 or tuple(delta.shape[:3]) != (B, T, taps) or delta.dtype != torch.float32
+            or not delta.is_contiguous()):
+        raise ValueError("delta must be a contiguous float32 [B, T, taps, G] tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of x's shape and dtype")
+    st = lib.dflash_grouped_conv(x.data_ptr(), out.data_ptr(), _dtype_code(x), B, T, C, taps, delta.shape[3],
+                                 base.data_ptr(), delta.data_ptr(), _stream_handle(stream))
+    _check(st)
+    return out
 
 
 def read_error(workspace: Optional[torch.Tensor] = None, clear: bool = True, stream=None) -> int:

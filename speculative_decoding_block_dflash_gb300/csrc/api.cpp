@@ -453,6 +453,31 @@ dflash_status dflash_project_kv(const void* hidden, int32_t num_tokens, int32_t 
     return DFLASH_OK;
 }
 
+dflash_status dflash_grouped_conv(const void* x, void* out, dflash_dtype dtype, int32_t batch, int32_t block_len,
+                                  int32_t channels, int32_t num_taps, int32_t num_groups, const float* base,
+                                  const float* delta, void* stream)
+{
+    g_last_error.clear();
+    if (dtype != DFLASH_BF16 && dtype != DFLASH_FP32) return fail(DFLASH_ERR_INVALID_ARG, "dtype must be bf16 or fp32");
+    if (batch < 1 || batch > 65535) return fail(DFLASH_ERR_INVALID_ARG, "batch %d outside [1, 65535]", batch);
+    if (block_len < 1 || block_len > DFLASH_MAX_BLOCK_LEN)
+        return fail(DFLASH_ERR_INVALID_ARG, "block_len %d outside [1, %d]", block_len, DFLASH_MAX_BLOCK_LEN);
+    if (num_taps < 1 || num_taps > DFLASH_MAX_BLOCK_LEN)
+        return fail(DFLASH_ERR_INVALID_ARG, "num_taps %d outside [1, %d]", num_taps, DFLASH_MAX_BLOCK_LEN);
+    if (channels < 1 || num_groups < 1 || channels % num_groups != 0)
+        return fail(DFLASH_ERR_INVALID_ARG, "channels %d must be a positive multiple of num_groups %d", channels,
+                    num_groups);
+    if (!x || !out || !base || !delta) return fail(DFLASH_ERR_INVALID_ARG, "NULL pointer");
+    if (x == out) return fail(DFLASH_ERR_INVALID_ARG, "out must not alias x");
+    const size_t es = dtype == DFLASH_BF16 ? 2 : 4;
+    if (!aligned(x, es) || !aligned(out, es) || !aligned(base, 4) || !aligned(delta, 4))
+        return fail(DFLASH_ERR_INVALID_ARG, "misaligned pointer (x and out to their element size, base and delta 4)");
+    const cudaError_t e = launch_grouped_conv(x, out, dtype, batch, block_len, channels, num_taps, num_groups, base,
+                                              delta, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "grouped convolution kernel launch");
+    return DFLASH_OK;
+}
+
 dflash_status dflash_split_combine(const float* partial_out, const float* partial_lse, int32_t num_splits,
                                    int64_t num_rows, int32_t head_dim, dflash_dtype out_dtype, void* out, float* lse,
                                    void* stream)

@@ -52,6 +52,10 @@ cudaError_t launch_accept(const void* logits, int32_t dtype, int32_t B, int32_t 
                           const int32_t* draft, int32_t* accepted, int32_t* next_token, int32_t* target_argmax,
                           unsigned long long* keys, int32_t* counters, cudaStream_t stream);
 
+// DFlash2 grouped dynamic depthwise convolution (csrc/grouped_conv.cu).
+cudaError_t launch_grouped_conv(const void* x, void* out, int32_t dtype, int32_t B, int32_t T, int32_t C,
+                                int32_t taps, int32_t G, const float* base, const float* delta, cudaStream_t stream);
+
 // Context K/V projection (csrc/project_kv.cu): persistent CTAs (at most one per SM).
 int32_t project_kv_grid(int32_t L, int32_t N);
 cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t hidden_stride, const void* w_k,

@@ -264,3 +264,29 @@ def test_project_kv_argument_checks(lib):
     assert proj(slots=FAKE + 2) == B.ERR_INVALID_ARG
     assert proj(err=FAKE + 1) == B.ERR_INVALID_ARG
     assert b"misaligned" in lib.dflash_last_error_message()
+
+
+@cpu_only
+def test_grouped_conv_argument_checks(lib):
+    P = ctypes.c_void_p
+
+    def conv(x=FAKE, out=FAKE + 4096, dtype=B.BF16, B_=2, T=16, C=512, taps=4, G=8, base=FAKE, delta=FAKE):
+        return lib.dflash_grouped_conv(P(x) if x else None, P(out) if out else None, dtype, B_, T, C, taps, G,
+                                       P(base) if base else None, P(delta) if delta else None, None)
+
+    assert conv(dtype=5) == B.ERR_INVALID_ARG
+    assert conv(B_=0) == B.ERR_INVALID_ARG
+    assert conv(B_=70000) == B.ERR_INVALID_ARG
+    assert conv(T=0) == B.ERR_INVALID_ARG
+    assert conv(T=65) == B.ERR_INVALID_ARG
+    assert conv(taps=0) == B.ERR_INVALID_ARG
+    assert conv(taps=65) == B.ERR_INVALID_ARG
+    assert conv(G=7) == B.ERR_INVALID_ARG          # 512 channels do not split into 7 groups
+    assert conv(G=0) == B.ERR_INVALID_ARG
+    assert conv(x=None) == B.ERR_INVALID_ARG
+    assert conv(delta=None) == B.ERR_INVALID_ARG
+    assert conv(out=FAKE) == B.ERR_INVALID_ARG     # in place is rejected
+    assert conv(x=FAKE + 1) == B.ERR_INVALID_ARG
+    assert conv(dtype=B.FP32, out=FAKE + 4098) == B.ERR_INVALID_ARG
+    assert conv(base=FAKE + 2) == B.ERR_INVALID_ARG
+    assert b"misaligned" in lib.dflash_last_error_message()
