@@ -717,6 +717,180 @@ def conv_bench(args, dfl, dev, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- DFlash2 candidate selector
+
+
+SEL_CONFIG = "selector_walk"
+SEL_DESC = ("DFlash2 candidate-selector walk: 32 requests x 15 draft slots x 8 candidates per slot, predecessor "
+            "and successor codebooks of 151936 x 256 bf16, temperature 1 (inverse-CDF sampling, q returned) "
+            "(synthetic; the pages state neither the codebook width, the vocabulary nor K)")
+SEL_SHAPE = dict(R=32, S=15, K=8, V=151936, E=256, T=1.0)
+
+
+def sel_bytes():
+    sh = SEL_SHAPE
+    R, S, K, E = sh["R"], sh["S"], sh["K"], sh["E"]
+    rows = R * ((1 + K) + (S - 1) * (2 * K))  # predecessor + candidate codebook rows gathered per call
+    return rows * E * 2 + R * S * (E * 4 + K * 8 + 4) + R * S * (K * 8 + 8)
+
+
+def sel_inputs(dev, n_sets, seed=1357):
+    sh = SEL_SHAPE
+    R, S, K, V, E = sh["R"], sh["S"], sh["K"], sh["V"], sh["E"]
+    g = torch.Generator(device=dev).manual_seed(seed)
+    A = torch.randn((V, E), generator=g, device=dev).to(torch.bfloat16)
+    B = torch.randn((V, E), generator=g, device=dev).to(torch.bfloat16)
+    sets = []
+    for _ in range(n_sets):
+        proj = torch.randn((R, S, E), generator=g, device=dev) / E ** 0.5
+        cand = torch.randint(0, V, (R, S, K), generator=g, device=dev, dtype=torch.int32)
+        unary = torch.randn((R, S, K), generator=g, device=dev)
+        anchor = torch.randint(0, V, (R,), generator=g, device=dev, dtype=torch.int32)
+        u = torch.rand((R, S), generator=g, device=dev)
+        sets.append((proj, cand, unary, anchor, u))
+    return A, B, sets
+
+
+def sel_oracle_rate(budget_s):
+    from oracle import selector as osel
+
+    sh = SEL_SHAPE
+    R, S, K, E = sh["R"], sh["S"], sh["K"], sh["E"]
+    V = 4096  # the host sample gathers from a smaller codebook; the walk's arithmetic is the same
+    rng = np.random.default_rng(11)
+    A = rng.standard_normal((V, E))
+    B = rng.standard_normal((V, E))
+    proj = rng.standard_normal((R, S, E))
+    cand = rng.integers(0, V, (R, S, K))
+    unary = rng.standard_normal((R, S, K))
+    anchor = rng.integers(0, V, R)
+    u = rng.random((R, S))
+    t0 = time.perf_counter()
+    n = 0
+    while n == 0 or time.perf_counter() - t0 < budget_s:
+        osel.walk(A, B, proj, cand, unary, anchor, temperature=sh["T"], u=u)
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    return sel_bytes() / dt / 1e9, f"{n} full oracle walks (float64, a {V}-row codebook)"
+
+
+def sel_reference_arm(args):
+    budget = max(1.0, min(args.ref_budget, 120.0)) / max(1, args.steps + args.warmup)
+    rate, sample = sel_oracle_rate(budget)
+    ms = sel_bytes() / (rate * 1e9) * 1e3
+    line = {"impl": "reference", "metric": "selector_gather_gbs", "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": SEL_DESC},
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def sel_bench(args, dfl, dev, rank, world):
+    sh = SEL_SHAPE
+    R, S, K, E = sh["R"], sh["S"], sh["K"], sh["E"]
+    per = sel_bytes()
+    n_sets = args.layers or max(2, math.ceil(4 * L2_BYTES / per))
+    A, B, sets = sel_inputs(dev, n_sets)
+    ws = torch.zeros(dfl.selector_workspace_bytes(R, S, K), dtype=torch.uint8, device=dev)
+    tokens = torch.empty((R, S), dtype=torch.int32, device=dev)
+    chosen = torch.empty_like(tokens)
+    scores = torch.empty((R, S, K), device=dev)
+    q = torch.empty((R, S, K), device=dev)
+    side = torch.cuda.Stream(dev)
+
+    def call(st, stream):
+        proj, cand, unary, anchor, u = st
+        dfl.selector_walk(A, B, proj, cand, unary, anchor, temperature=sh["T"], uniforms=u, workspace=ws,
+                          tokens=tokens, chosen=chosen, path_scores=scores, q=q, stream=stream)
+
+    with torch.cuda.stream(side):
+        for st in sets:
+            call(st, side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for st in sets:
+            call(st, side)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    reps = max(1, math.ceil(args.steps / n_sets))
+    steps = reps * n_sets
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if rank == 0:
+        sampler.stop()
+    ms = ev0.elapsed_time(ev1) / steps
+    value = world * per / (ms * 1e-3) / 1e9
+    # end to end: the step's inputs in from pinned memory, tokens and q back, every step
+    proj, cand, unary, anchor, u = sets[0]
+    host_in = [t.cpu().pin_memory() for t in (proj, cand, unary, anchor, u)]
+    tok_h = torch.empty_like(tokens, device="cpu").pin_memory()
+    q_h = torch.empty_like(q, device="cpu").pin_memory()
+    n_e2e = max(1, min(steps, 200))
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        for d, h in zip((proj, cand, unary, anchor, u), host_in):
+            d.copy_(h, non_blocking=True)
+        dfl.selector_walk(A, B, proj, cand, unary, anchor, temperature=sh["T"], uniforms=u, workspace=ws,
+                          tokens=tokens, chosen=chosen, path_scores=scores, q=q)
+        tok_h.copy_(tokens, non_blocking=True)
+        q_h.copy_(q, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        rate, sample = sel_oracle_rate(min(args.cpu_budget, 10.0))
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+    line = {
+        "metric": "selector_gather_gbs", "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": SEL_DESC, "global_batch": R * world, "slots": S, "candidates": K,
+                   "vocab": sh["V"], "dim": E,
+                   "l2": f"inputs larger than L2: 2 x {sh['V'] * E * 2 / 1e6:.0f} MB codebooks, {n_sets} rotated "
+                         f"candidate sets of random rows",
+                   "timed_path": f"CUDA-graph replays of {n_sets} dflash_selector_walk calls, one per step",
+                   "parallelism": f"replicas x{world}"},
+        "e2e": {"value": world * per / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host_in),
+                "d2h_bytes_per_step": tok_h.numel() * 4 + q_h.numel() * 4, "ms_per_step": e2e_ms,
+                "note": "public Python API; projections, candidates, unary, anchors and uniforms in from pinned "
+                        "host memory, tokens and q back, every step; the codebooks stay resident"},
+        "gpu_launches": steps,
+        "roofline": {"bound": "hbm", "achieved": value / world, "peak": peak, "unit": "GB/s",
+                     "frac": value / world / peak, "traffic": traffic_from_profiles("selector_kernel")[0],
+                     "peak_kind": peak_kind, "kernel": "selector_kernel",
+                     "achieved_basis": "gathered codebook rows + proj + candidates + outputs per launch / "
+                                       "event-timed time"},
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 
@@ -800,6 +974,11 @@ def main():
             if dist:
                 dist.destroy_process_group()
             return
+        if args.config == SEL_CONFIG:
+            sel_reference_arm(args)
+            if dist:
+                dist.destroy_process_group()
+            return
         import workloads
 
         case = workloads.make_case(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
@@ -832,6 +1011,11 @@ def main():
         return
     if args.config == CONV_CONFIG:
         conv_bench(args, dfl, dev, rank, world)
+        if dist:
+            dist.destroy_process_group()
+        return
+    if args.config == SEL_CONFIG:
+        sel_bench(args, dfl, dev, rank, world)
         if dist:
             dist.destroy_process_group()
         return

@@ -110,6 +110,7 @@ typedef enum dflash_kernel {
 #define DFLASH_DEVERR_PAGE_ID 1u     /* page_table entry outside [0, num_pages) */
 #define DFLASH_DEVERR_SEQ_LEN 2u     /* seq_lens[b] < T or above the stated bounds */
 #define DFLASH_DEVERR_TIMEOUT 4u     /* a bounded pipeline wait gave up (kernel returned early) */
+#define DFLASH_DEVERR_TOKEN_ID 8u    /* a token id outside [0, vocab) (read as token 0) */
 
 /* Sizes and layout of one call. All counts are elements, not bytes. */
 typedef struct dflash_dims {
@@ -340,6 +341,44 @@ DFLASH_API dflash_status dflash_grouped_conv(const void* x, void* out, dflash_dt
                                              int32_t block_len, int32_t channels, int32_t num_taps,
                                              int32_t num_groups, const float* base, const float* delta,
                                              void* stream);
+
+/*
+ * DFlash2 candidate-selector walk (prhub report on vLLM PR #52816 "DFlash2", the motivation
+ * paragraph and changes 1-2). The head keeps num_candidates = K tokens per draft slot. The
+ * transition from token p to candidate k of slot s of request r scores
+ *   edge(p -> k) = sum_e A[p, e] * proj[r, s, e] * B[cand[r, s, k], e] + unary[r, s, k]
+ * (A: predecessor codebook, B: successor codebook, proj: the projected hidden state of the
+ * slot). From p = anchor[r], slot by slot: with temperature 0 the walk takes the first k of
+ * maximal edge; with temperature T > 0 it forms q = softmax(edge / T) over the K candidates and
+ * takes the smallest k whose running sum of q exceeds uniforms[r, s] (K - 1 if rounding leaves
+ * none). The chosen token becomes the next slot's p.
+ *
+ *   pred_codebook, succ_codebook  device bf16 [vocab, dim], 16-byte aligned; dim a multiple of 8.
+ *   proj          device float32 [R, S, dim], 16-byte aligned.
+ *   candidates    device int32 [R, S, K]; unary device float32 [R, S, K] (finite).
+ *   anchor        device int32 [R]: the verified token each walk starts from.
+ *   uniforms      device float32 [R, S] in [0, 1); needed when temperature > 0, else ignored.
+ *   tokens        device int32 [R, S], written: the walk's token per slot.
+ *   chosen        device int32 [R, S] or NULL: the chosen candidate index per slot.
+ *   path_scores   device float32 [R, S, K] or NULL: the K edges from the walk's predecessor.
+ *   q             device float32 [R, S, K] or NULL: the sampling distribution (T > 0 only).
+ *   device_error  device uint32 word or NULL: DFLASH_DEVERR_TOKEN_ID for ids outside [0, vocab).
+ *   workspace     device, 256-byte aligned, dflash_selector_workspace_bytes() long, zeroed once
+ *                 before its first use. Layout: a fixed 256 KB block of per-request arrival
+ *                 counters (left at zero by every call, so one zeroed workspace serves calls of
+ *                 any size), then the R x S x K x K edge tables.
+ * fp32 arithmetic (bf16 codebooks widened exactly). Limits: 1 <= R, S <= 65535, 1 <= K <= 64,
+ * K * dim * 6 bytes <= 200 KB. Asynchronous on `stream`; calls sharing a workspace must not
+ * overlap.
+ */
+DFLASH_API size_t dflash_selector_workspace_bytes(int32_t num_requests, int32_t num_slots, int32_t num_candidates);
+DFLASH_API dflash_status dflash_selector_walk(const void* pred_codebook, const void* succ_codebook, int32_t vocab,
+                                              int32_t dim, const float* proj, const int32_t* candidates,
+                                              const float* unary, const int32_t* anchor, int32_t num_requests,
+                                              int32_t num_slots, int32_t num_candidates, float temperature,
+                                              const float* uniforms, int32_t* tokens, int32_t* chosen,
+                                              float* path_scores, float* q, uint32_t* device_error,
+                                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* DFLASH_ABI_VERSION of the loaded library. */
 DFLASH_API int32_t dflash_abi_version(void);

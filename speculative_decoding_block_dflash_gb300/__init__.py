@@ -8,6 +8,7 @@ from ._binding import (  # noqa: F401
     DEVERR_PAGE_ID,
     DEVERR_SEQ_LEN,
     DEVERR_TIMEOUT,
+    DEVERR_TOKEN_ID,
     EXPORTED,
     FP32,
     KERNELS,
@@ -20,6 +21,8 @@ from ._binding import (  # noqa: F401
     accept_workspace_bytes,
     project_kv,
     grouped_conv,
+    selector_walk,
+    selector_workspace_bytes,
     block_attn,
     block_attn_noalloc,
     load_library,

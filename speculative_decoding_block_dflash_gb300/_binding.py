@@ -26,7 +26,7 @@ BF16, FP32 = 0, 1
 # dflash_kernel
 KERNELS = {"auto": 0, "simt": 1, "tc": 2, "tc_pair": 3}
 # device error bits
-DEVERR_PAGE_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4
+DEVERR_PAGE_ID, DEVERR_SEQ_LEN, DEVERR_TIMEOUT, DEVERR_TOKEN_ID = 1, 2, 4, 8
 
 EXPORTED = (
     "dflash_block_attn",
@@ -42,6 +42,8 @@ EXPORTED = (
     "dflash_accept_workspace_bytes",
     "dflash_project_kv",
     "dflash_grouped_conv",
+    "dflash_selector_workspace_bytes",
+    "dflash_selector_walk",
 )
 
 
@@ -120,6 +122,11 @@ def load_library(path: Optional[str] = None):
         lib.dflash_project_kv.argtypes = [vp, i32, i32, i64, vp, vp, vp, vp, vp, dims_p, vp, vp]
         lib.dflash_grouped_conv.restype = ctypes.c_int
         lib.dflash_grouped_conv.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+        lib.dflash_selector_workspace_bytes.restype = ctypes.c_size_t
+        lib.dflash_selector_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.dflash_selector_walk.restype = ctypes.c_int
+        lib.dflash_selector_walk.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp, vp,
+                                             vp, vp, ctypes.c_size_t, vp]
         if path is None:
             _lib = lib
         return lib
@@ -401,6 +408,70 @@ def grouped_conv(x: torch.Tensor, base: torch.Tensor, delta: torch.Tensor, out: 
                                  base.data_ptr(), delta.data_ptr(), _stream_handle(stream))
     _check(st)
     return out
+
+
+def selector_workspace_bytes(num_requests: int, num_slots: int, num_candidates: int) -> int:
+    n = load_library().dflash_selector_workspace_bytes(int(num_requests), int(num_slots), int(num_candidates))
+    if n == 0:
+        raise DflashError(ERR_INVALID_ARG, "invalid sizes for the selector workspace")
+    return n
+
+
+_sel_ws = {}
+
+
+def selector_walk(pred_codebook: torch.Tensor, succ_codebook: torch.Tensor, proj: torch.Tensor,
+                  candidates: torch.Tensor, unary: torch.Tensor, anchor: torch.Tensor, temperature: float = 0.0,
+                  uniforms: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                  tokens: Optional[torch.Tensor] = None, chosen: Optional[torch.Tensor] = None,
+                  path_scores: Optional[torch.Tensor] = None, q: Optional[torch.Tensor] = None,
+                  want_scores: bool = True, device_error: Optional[torch.Tensor] = None, stream=None):
+    """DFlash2 candidate-selector walk (dflash_selector_walk). Codebooks bf16 [V, E]; proj float32
+    [R, S, E]; candidates int32 [R, S, K]; unary float32 [R, S, K]; anchor int32 [R]; uniforms
+    float32 [R, S] when temperature > 0. Returns (tokens [R, S], chosen [R, S], path_scores
+    [R, S, K] or None, q [R, S, K] or None)."""
+    lib = load_library()
+    V, E = pred_codebook.shape
+    R, S, K = candidates.shape
+    for name, t, dt in (("pred_codebook", pred_codebook, torch.bfloat16), ("succ_codebook", succ_codebook, torch.bfloat16),
+                        ("proj", proj, torch.float32), ("candidates", candidates, torch.int32),
+                        ("unary", unary, torch.float32), ("anchor", anchor, torch.int32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} tensor")
+    if tuple(succ_codebook.shape) != (V, E) or tuple(proj.shape) != (R, S, E) or tuple(unary.shape) != (R, S, K) \
+            or tuple(anchor.shape) != (R,):
+        raise ValueError("inconsistent selector shapes")
+    dev = candidates.device
+    if temperature > 0:
+        if uniforms is None or uniforms.dtype != torch.float32 or tuple(uniforms.shape) != (R, S) \
+                or not uniforms.is_contiguous():
+            raise ValueError("temperature > 0 needs contiguous float32 uniforms [R, S]")
+    if workspace is None:
+        need = selector_workspace_bytes(R, S, K)
+        key = (dev.type, dev.index)
+        workspace = _sel_ws.get(key)
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=dev)
+            _sel_ws[key] = workspace
+    if tokens is None:
+        tokens = torch.empty((R, S), dtype=torch.int32, device=dev)
+    if chosen is None:
+        chosen = torch.empty((R, S), dtype=torch.int32, device=dev)
+    if path_scores is None and want_scores:
+        path_scores = torch.empty((R, S, K), dtype=torch.float32, device=dev)
+    if q is None and temperature > 0:
+        q = torch.empty((R, S, K), dtype=torch.float32, device=dev)
+    st = lib.dflash_selector_walk(pred_codebook.data_ptr(), succ_codebook.data_ptr(), V, E, proj.data_ptr(),
+                                  candidates.data_ptr(), unary.data_ptr(), anchor.data_ptr(), R, S, K,
+                                  float(temperature), uniforms.data_ptr() if uniforms is not None else None,
+                                  tokens.data_ptr(), chosen.data_ptr(),
+                                  path_scores.data_ptr() if path_scores is not None else None,
+                                  q.data_ptr() if q is not None else None,
+                                  device_error.data_ptr() if device_error is not None else None,
+                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream))
+    _check(st)
+    return tokens, chosen, path_scores, q
 
 
 def read_error(workspace: Optional[torch.Tensor] = None, clear: bool = True, stream=None) -> int:

@@ -478,6 +478,59 @@ dflash_status dflash_grouped_conv(const void* x, void* out, dflash_dtype dtype, 
     return DFLASH_OK;
 }
 
+constexpr size_t kSelectorCounterBytes = 65536 * sizeof(int32_t);  // one counter per possible request
+
+size_t dflash_selector_workspace_bytes(int32_t num_requests, int32_t num_slots, int32_t num_candidates)
+{
+    if (num_requests < 1 || num_requests > 65535 || num_slots < 1 || num_slots > 65535 || num_candidates < 1 ||
+        num_candidates > 64)
+        return 0;
+    // a fixed counter block first, so that a workspace zeroed once stays valid for calls of any
+    // size (a counter never lands where an earlier call left its edge table), then the tables
+    const size_t tab = sizeof(float) * (size_t)num_requests * num_slots * num_candidates * num_candidates;
+    return kSelectorCounterBytes + round_up(tab, 256);
+}
+
+dflash_status dflash_selector_walk(const void* pred_codebook, const void* succ_codebook, int32_t vocab, int32_t dim,
+                                   const float* proj, const int32_t* candidates, const float* unary,
+                                   const int32_t* anchor, int32_t num_requests, int32_t num_slots,
+                                   int32_t num_candidates, float temperature, const float* uniforms, int32_t* tokens,
+                                   int32_t* chosen, float* path_scores, float* q, uint32_t* device_error,
+                                   void* workspace, size_t workspace_bytes, void* stream)
+{
+    g_last_error.clear();
+    const int32_t R = num_requests, S = num_slots, K = num_candidates, E = dim;
+    if (R < 1 || R > 65535 || S < 1 || S > 65535)
+        return fail(DFLASH_ERR_INVALID_ARG, "num_requests %d / num_slots %d outside [1, 65535]", R, S);
+    if (K < 1 || K > 64) return fail(DFLASH_ERR_INVALID_ARG, "num_candidates %d outside [1, 64]", K);
+    if (vocab < 1) return fail(DFLASH_ERR_INVALID_ARG, "vocab %d < 1", vocab);
+    if (E < 8 || E % 8 != 0) return fail(DFLASH_ERR_INVALID_ARG, "dim %d must be a positive multiple of 8", E);
+    if (selector_smem_bytes(K, E) > 200 * 1024)
+        return fail(DFLASH_ERR_UNSUPPORTED, "num_candidates * dim = %lld above %d", (long long)K * E,
+                    200 * 1024 / 6);
+    if (!(temperature >= 0.f) || !std::isfinite(temperature))
+        return fail(DFLASH_ERR_INVALID_ARG, "temperature must be finite and >= 0");
+    if (!pred_codebook || !succ_codebook || !proj || !candidates || !unary || !anchor || !tokens)
+        return fail(DFLASH_ERR_INVALID_ARG, "NULL pointer");
+    if (temperature > 0.f && !uniforms) return fail(DFLASH_ERR_INVALID_ARG, "temperature > 0 needs uniforms");
+    if (!aligned(pred_codebook, 16) || !aligned(succ_codebook, 16) || !aligned(proj, 16) || !aligned(candidates, 4) ||
+        !aligned(unary, 4) || !aligned(anchor, 4) || !aligned(tokens, 4) || (uniforms && !aligned(uniforms, 4)) ||
+        (chosen && !aligned(chosen, 4)) || (path_scores && !aligned(path_scores, 4)) || (q && !aligned(q, 4)) ||
+        (device_error && !aligned(device_error, 4)))
+        return fail(DFLASH_ERR_INVALID_ARG, "misaligned pointer (codebooks and proj 16 bytes, the rest 4)");
+    const size_t need = dflash_selector_workspace_bytes(R, S, K);
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < need)
+        return fail(DFLASH_ERR_WORKSPACE, "the selector needs a 256-byte aligned workspace of %zu bytes", need);
+    char* wsb = static_cast<char*>(workspace);
+    int32_t* counters = reinterpret_cast<int32_t*>(wsb);
+    float* tab = reinterpret_cast<float*>(wsb + kSelectorCounterBytes);
+    const cudaError_t e = launch_selector(pred_codebook, succ_codebook, vocab, E, proj, candidates, unary, anchor, R,
+                                          S, K, temperature, uniforms, tokens, chosen, path_scores, q, device_error,
+                                          tab, counters, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "selector kernel launch");
+    return DFLASH_OK;
+}
+
 dflash_status dflash_split_combine(const float* partial_out, const float* partial_lse, int32_t num_splits,
                                    int64_t num_rows, int32_t head_dim, dflash_dtype out_dtype, void* out, float* lse,
                                    void* stream)

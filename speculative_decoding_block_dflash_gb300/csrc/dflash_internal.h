@@ -52,6 +52,14 @@ cudaError_t launch_accept(const void* logits, int32_t dtype, int32_t B, int32_t 
                           const int32_t* draft, int32_t* accepted, int32_t* next_token, int32_t* target_argmax,
                           unsigned long long* keys, int32_t* counters, cudaStream_t stream);
 
+// DFlash2 candidate-selector walk (csrc/selector.cu).
+size_t selector_smem_bytes(int32_t K, int32_t E);
+cudaError_t launch_selector(const void* A, const void* B, int32_t V, int32_t E, const float* proj, const int32_t* cand,
+                            const float* unary, const int32_t* anchor, int32_t R, int32_t S, int32_t K,
+                            float temperature, const float* uniforms, int32_t* tokens, int32_t* chosen,
+                            float* path_scores, float* q, uint32_t* err, float* tab, int32_t* counters,
+                            cudaStream_t stream);
+
 // DFlash2 grouped dynamic depthwise convolution (csrc/grouped_conv.cu).
 cudaError_t launch_grouped_conv(const void* x, void* out, int32_t dtype, int32_t B, int32_t T, int32_t C,
                                 int32_t taps, int32_t G, const float* base, const float* delta, cudaStream_t stream);

@@ -290,3 +290,36 @@ def test_grouped_conv_argument_checks(lib):
     assert conv(dtype=B.FP32, out=FAKE + 4098) == B.ERR_INVALID_ARG
     assert conv(base=FAKE + 2) == B.ERR_INVALID_ARG
     assert b"misaligned" in lib.dflash_last_error_message()
+
+
+@cpu_only
+def test_selector_workspace_and_argument_checks(lib):
+    P = ctypes.c_void_p
+    # a fixed 256 KB counter block, then the R*S*K*K edge tables
+    assert lib.dflash_selector_workspace_bytes(32, 15, 8) == 262144 + 32 * 15 * 64 * 4
+    assert lib.dflash_selector_workspace_bytes(1, 1, 1) == 262144 + 256
+    assert lib.dflash_selector_workspace_bytes(0, 15, 8) == 0
+    assert lib.dflash_selector_workspace_bytes(2, 15, 65) == 0
+
+    def walk(A=FAKE, V=1000, E=256, proj=FAKE, R=2, S=15, K=8, T=0.0, u=None, tokens=FAKE, ws=FAKE, ws_bytes=1 << 20,
+             err=None):
+        return lib.dflash_selector_walk(P(A) if A else None, P(FAKE), V, E, P(proj), P(FAKE), P(FAKE), P(FAKE), R, S, K,
+                                        T, P(u) if u else None, P(tokens) if tokens else None, None, None, None,
+                                        P(err) if err else None, P(ws) if ws else None, ws_bytes, None)
+
+    assert walk(K=0) == B.ERR_INVALID_ARG
+    assert walk(K=65) == B.ERR_INVALID_ARG
+    assert walk(R=0) == B.ERR_INVALID_ARG
+    assert walk(V=0) == B.ERR_INVALID_ARG
+    assert walk(E=12) == B.ERR_INVALID_ARG            # dim not a multiple of 8
+    assert walk(K=64, E=4096) == B.ERR_UNSUPPORTED    # the staged rows exceed shared memory
+    assert walk(T=-1.0) == B.ERR_INVALID_ARG
+    assert walk(T=float("nan")) == B.ERR_INVALID_ARG
+    assert walk(T=0.7) == B.ERR_INVALID_ARG           # sampling needs uniforms
+    assert walk(A=None) == B.ERR_INVALID_ARG
+    assert walk(tokens=None) == B.ERR_INVALID_ARG
+    assert walk(proj=FAKE + 4) == B.ERR_INVALID_ARG   # proj rows are read 16 bytes at a time
+    assert walk(err=FAKE + 2) == B.ERR_INVALID_ARG
+    assert walk(ws=None) == B.ERR_WORKSPACE
+    assert walk(ws_bytes=1024) == B.ERR_WORKSPACE
+    assert b"workspace" in lib.dflash_last_error_message()
