@@ -42,6 +42,31 @@ UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
 
 
+def max_over_ranks(x: float) -> float:
+    """The largest value of a per-rank float over the job (the slowest rank sets the job's
+    time); the value itself when no process group is running."""
+    import torch.distributed as tdist
+
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) if tdist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as tdist
+
+    if tdist.is_available() and tdist.is_initialized() and tdist.get_world_size() > 1:
+        tdist.barrier()
+
+
+def process_group_backend() -> str:
+    """nccl with GPUs, gloo on a host without them (the CPU tests of the multi-rank path)."""
+    return "nccl" if torch.cuda.is_available() else "gloo"
+
+
 def env_int(name, default):
     try:
         return int(os.environ.get(name, default))
@@ -318,6 +343,7 @@ def accept_bench(args, dfl, dev, rank, world):
         sampler.start()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     ev0.record(stream)
@@ -328,7 +354,7 @@ def accept_bench(args, dfl, dev, rank, world):
     t_wall1 = time.time()
     if rank == 0:
         sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
     value = world * per / (ms * 1e-3) / 1e9
     # end to end: drafts in from pinned memory, accepted length and next token back, every step
     d_h = draft.cpu().pin_memory()
@@ -346,7 +372,7 @@ def accept_bench(args, dfl, dev, rank, world):
         n_h.copy_(nxt, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e)
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
@@ -486,6 +512,7 @@ def project_bench(args, dfl, dev, rank, world):
         sampler.start()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     ev0.record(stream)
@@ -496,7 +523,7 @@ def project_bench(args, dfl, dev, rank, world):
     t_wall1 = time.time()
     if rank == 0:
         sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps)
     flops = project_flops()
     value = world * flops / (ms * 1e-3) / 1e12
     # end to end: the hidden states and slot mapping in from pinned memory, the error word back,
@@ -532,7 +559,7 @@ def project_bench(args, dfl, dev, rank, world):
         err_h.copy_(err, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e)
     if int(err_h.item()) != 0:
         raise RuntimeError(f"device error word {int(err_h.item())} after the projection")
     if rank != 0:
@@ -654,6 +681,7 @@ def conv_bench(args, dfl, dev, rank, world):
         sampler.start()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     ev0.record(stream)
@@ -664,7 +692,7 @@ def conv_bench(args, dfl, dev, rank, world):
     t_wall1 = time.time()
     if rank == 0:
         sampler.stop()
-    ms = ev0.elapsed_time(ev1) / steps
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / steps)
     value = world * per / (ms * 1e-3) / 1e9
     # end to end: x and delta in from pinned memory, out back, every step
     x0, d0, o0 = sets[0]
@@ -683,7 +711,7 @@ def conv_bench(args, dfl, dev, rank, world):
         o_h.copy_(o0, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e)
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
@@ -824,6 +852,7 @@ def sel_bench(args, dfl, dev, rank, world):
         sampler.start()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
     ev0.record(stream)
@@ -834,7 +863,7 @@ def sel_bench(args, dfl, dev, rank, world):
     t_wall1 = time.time()
     if rank == 0:
         sampler.stop()
-    ms = ev0.elapsed_time(ev1) / steps
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / steps)
     value = world * per / (ms * 1e-3) / 1e9
     # end to end: the step's inputs in from pinned memory, tokens and q back, every step
     proj, cand, unary, anchor, u = sets[0]
@@ -855,7 +884,7 @@ def sel_bench(args, dfl, dev, rank, world):
         q_h.copy_(q, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e)
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
@@ -952,8 +981,11 @@ def main():
         import torch.distributed as dist_mod
 
         dist = dist_mod
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if process_group_backend() == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     if args.impl == "reference":
         if rank != 0:
             if dist:
