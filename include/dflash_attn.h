@@ -308,15 +308,24 @@ DFLASH_API dflash_status dflash_accept_prefix(const void* logits, dflash_dtype d
  *                 other fields are ignored.
  *   device_error  device uint32 word (bits OR-ed in; DFLASH_DEVERR_TIMEOUT if a bounded
  *                 pipeline wait gave up) or NULL.
+ *   workspace     device, 256-byte aligned, zeroed once before its first use, or NULL. With
+ *                 at least dflash_project_kv_workspace_bytes() bytes, the tiles of a partial
+ *                 last round of the persistent grid are split in two along the hidden
+ *                 dimension, and the halves meet in the workspace: an 8 KB block of counters
+ *                 (left at zero by every call, unless a device timeout was reported), then
+ *                 fp32 partial tiles. NULL (or too small) computes every tile whole. Results
+ *                 differ only in the fp32 summation order.
  * Limits: 0 <= num_tokens <= DFLASH_PROJECT_MAX_TOKENS (0 is a no-op),
  * num_kv_heads * head_dim <= 65536. Invalid arguments are reported before any launch.
- * Asynchronous on `stream`; needs no workspace and allocates nothing.
+ * Asynchronous on `stream`; allocates nothing. Calls that share a workspace must not overlap.
  */
 #define DFLASH_PROJECT_MAX_TOKENS (1 << 24)
+DFLASH_API size_t dflash_project_kv_workspace_bytes(void); /* for the current device */
 DFLASH_API dflash_status dflash_project_kv(const void* hidden, int32_t num_tokens, int32_t hidden_size,
                                            int64_t hidden_stride, const void* w_k, const void* w_v,
                                            const int32_t* slot_mapping, void* k_cache, void* v_cache,
-                                           const dflash_dims* dims, uint32_t* device_error, void* stream);
+                                           const dflash_dims* dims, uint32_t* device_error, void* workspace,
+                                           size_t workspace_bytes, void* stream);
 
 /*
  * DFlash2 grouped dynamic depthwise convolution inside a drafted block (prhub report on vLLM

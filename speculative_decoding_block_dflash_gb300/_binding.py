@@ -41,6 +41,7 @@ EXPORTED = (
     "dflash_accept_prefix",
     "dflash_accept_workspace_bytes",
     "dflash_project_kv",
+    "dflash_project_kv_workspace_bytes",
     "dflash_grouped_conv",
     "dflash_selector_workspace_bytes",
     "dflash_selector_walk",
@@ -119,7 +120,9 @@ def load_library(path: Optional[str] = None):
         lib.dflash_accept_prefix.restype = ctypes.c_int
         lib.dflash_accept_prefix.argtypes = [vp, i32, i32, i32, i32, i64, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
         lib.dflash_project_kv.restype = ctypes.c_int
-        lib.dflash_project_kv.argtypes = [vp, i32, i32, i64, vp, vp, vp, vp, vp, dims_p, vp, vp]
+        lib.dflash_project_kv.argtypes = [vp, i32, i32, i64, vp, vp, vp, vp, vp, dims_p, vp, vp, ctypes.c_size_t, vp]
+        lib.dflash_project_kv_workspace_bytes.restype = ctypes.c_size_t
+        lib.dflash_project_kv_workspace_bytes.argtypes = []
         lib.dflash_grouped_conv.restype = ctypes.c_int
         lib.dflash_grouped_conv.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
         lib.dflash_selector_workspace_bytes.restype = ctypes.c_size_t
@@ -342,15 +345,29 @@ def accept_prefix(logits: torch.Tensor, draft: torch.Tensor, workspace: Optional
     return accepted, next_token, target_argmax
 
 
+_proj_ws = {}
+
+
 def project_kv(hidden: torch.Tensor, w_k: torch.Tensor, w_v: torch.Tensor, slot_mapping: torch.Tensor,
                k_cache: torch.Tensor, v_cache: torch.Tensor, device_error: Optional[torch.Tensor] = None,
-               stream=None) -> None:
+               workspace: Optional[torch.Tensor] = None, split: bool = True, stream=None) -> None:
     """Context K/V projection into the paged cache (dflash_project_kv): hidden [L, H] bf16
     (rows of any stride, last dim contiguous), w_k / w_v [Hkv*D, H] bf16 contiguous,
     slot_mapping int32 [L] (page * page_size + position; < 0 skips the token), caches
     [num_pages, page_size, Hkv, D] bf16 (d contiguous, same strides). device_error: an
-    optional int32/uint32 device word that receives DEVERR_* bits."""
+    optional int32/uint32 device word that receives DEVERR_* bits. With split (the default)
+    the last round's tiles are split in two through a workspace (a zeroed cached one when
+    none is given); split=False computes every tile whole."""
     lib = load_library()
+    if split and workspace is None and hidden.numel():
+        dev = hidden.device
+        key = (dev.type, dev.index)
+        workspace = _proj_ws.get(key)
+        if workspace is None:
+            workspace = torch.zeros(lib.dflash_project_kv_workspace_bytes(), dtype=torch.uint8, device=dev)
+            _proj_ws[key] = workspace
+    if not split:
+        workspace = None
     if hidden.dim() != 2 or hidden.stride(1) != 1:
         raise ValueError("hidden must be [L, H] with a contiguous last dimension")
     if k_cache.dim() != 4 or k_cache.shape != v_cache.shape or k_cache.stride() != v_cache.stride():
@@ -382,6 +399,8 @@ def project_kv(hidden: torch.Tensor, w_k: torch.Tensor, w_v: torch.Tensor, slot_
                                w_k.data_ptr(), w_v.data_ptr(), slot_mapping.data_ptr() if L else None,
                                k_cache.data_ptr(), v_cache.data_ptr(), ctypes.byref(d),
                                device_error.data_ptr() if device_error is not None else None,
+                               workspace.data_ptr() if workspace is not None else None,
+                               workspace.numel() * workspace.element_size() if workspace is not None else 0,
                                _stream_handle(stream))
     _check(st)
 

@@ -415,9 +415,12 @@ dflash_status dflash_accept_prefix(const void* logits, dflash_dtype dtype, int32
     return DFLASH_OK;
 }
 
+size_t dflash_project_kv_workspace_bytes(void) { return project_kv_workspace_bytes(); }
+
 dflash_status dflash_project_kv(const void* hidden, int32_t num_tokens, int32_t hidden_size, int64_t hidden_stride,
                                 const void* w_k, const void* w_v, const int32_t* slot_mapping, void* k_cache,
-                                void* v_cache, const dflash_dims* dims, uint32_t* device_error, void* stream)
+                                void* v_cache, const dflash_dims* dims, uint32_t* device_error, void* workspace,
+                                size_t workspace_bytes, void* stream)
 {
     g_last_error.clear();
     if (!dims) return fail(DFLASH_ERR_INVALID_ARG, "NULL dims");
@@ -446,9 +449,12 @@ dflash_status dflash_project_kv(const void* hidden, int32_t num_tokens, int32_t 
     if (!aligned(hidden, 16) || !aligned(w_k, 16) || !aligned(w_v, 16) || !aligned(k_cache, 16) ||
         !aligned(v_cache, 16) || !aligned(slot_mapping, 4) || (device_error && !aligned(device_error, 4)))
         return fail(DFLASH_ERR_INVALID_ARG, "misaligned pointer (16 bytes; slot_mapping and device_error 4)");
+    if (workspace && !aligned(workspace, 256))
+        return fail(DFLASH_ERR_WORKSPACE, "the projection workspace must be 256-byte aligned");
     const cudaError_t e = launch_project_kv(hidden, num_tokens, hidden_size, hidden_stride, w_k, w_v, slot_mapping,
                                             k_cache, v_cache, Hkv, D, dims->page_size, dims->num_pages, sp, ss, sh,
-                                            device_error, static_cast<cudaStream_t>(stream));
+                                            device_error, workspace, workspace ? workspace_bytes : 0,
+                                            static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "projection kernel launch");
     return DFLASH_OK;
 }

@@ -66,10 +66,12 @@ cudaError_t launch_grouped_conv(const void* x, void* out, int32_t dtype, int32_t
 
 // Context K/V projection (csrc/project_kv.cu): persistent CTAs (at most one per SM).
 int32_t project_kv_grid(int32_t L, int32_t N);
+size_t project_kv_workspace_bytes();
 cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t hidden_stride, const void* w_k,
                               const void* w_v, const int32_t* slot_mapping, void* k_cache, void* v_cache,
                               int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages, int64_t sp, int64_t ss,
-                              int64_t sh, uint32_t* err, cudaStream_t stream);
+                              int64_t sh, uint32_t* err, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
 
 // Slots of the tensor-core kernel's length-balanced split plan for these sizes (auto split
 // count, B > 1, whole grid resident), or 0 when the plan is uniform.

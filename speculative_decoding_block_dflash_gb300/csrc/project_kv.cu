@@ -21,7 +21,15 @@
 //              token row, 16 columns at a time, bf16 pack and two 16-byte stores into the
 //              token's cache slot.
 // A 256-row tile halves the bytes each SM must land per flop against a 128-row one: the
-// tensor copies into one SM, not the MMAs, bound this kernel. A tile whose second half lies
+// tensor copies into one SM, not the MMAs, bound this kernel.
+//
+// When the tiles leave a partial last round (tiles mod CTAs = rem, 2 * rem <= CTAs) and the
+// caller gives a workspace, the last rem tiles are split along the hidden dimension into two
+// halves that run on 2 * rem CTAs of the last round. The first half to reach its epilogue
+// (an arrival counter) writes its fp32 accumulator to the workspace and raises a flag; the
+// other waits for the flag (bounded), adds the partial to its own accumulator and writes the
+// bf16 rows. Both halves of a tile are in the same round, so the waiter only waits for a
+// CTA that is already writing. A tile whose second half lies
 // wholly past the last token skips that half's MMAs. Rows past the token count and hidden
 // columns past H are zero-filled by the tensor copies. Every wait is bounded
 // (DFLASH_DEVERR_TIMEOUT, the kernel returns).
@@ -52,6 +60,7 @@ constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemUsed = kMiscOff + 16;
 constexpr int kAlloc = kSmemUsed + 1024;  // the ring is aligned up to 1024 bytes (swizzle atoms)
 static_assert(kAlloc <= 227 * 1024, "shared memory");
+constexpr size_t kProjectSyncBytes = 8192;  // two int32 per split tile, a fixed block
 
 struct ProjParams {
     const int32_t* slot_mapping;
@@ -61,9 +70,46 @@ struct ProjParams {
     int32_t L, H, N, D, page_size;
     int32_t n_half;  // feature tiles of one projection: ceil(N / kBN)
     int32_t tiles;   // ceil(L / kBM) * 2 * n_half
+    int32_t full_tiles;  // tiles computed whole; tiles [full_tiles, tiles) are split in two
+    int32_t units;       // full_tiles + 2 * (tiles - full_tiles): the persistent loop's work units
+    float* partial;      // [tiles - full_tiles][kBM][kBN] fp32: the first half's accumulator
+    int32_t* sync;       // [tiles - full_tiles][2]: arrivals, partial-ready flag (zero between calls)
     int64_t total_slots;
     int64_t sp, ss, sh;
 };
+
+// Work unit u of the persistent loop: a whole tile, or one half (along the hidden dimension) of
+// a split tile.
+struct Unit {
+    int tile, kb0, kb1, slot, half;  // slot < 0: a whole tile
+};
+
+__device__ __forceinline__ Unit unit_of(const ProjParams& p, int u, int KB)
+{
+    Unit w;
+    if (u < p.full_tiles) {
+        w.tile = u;
+        w.kb0 = 0;
+        w.kb1 = KB;
+        w.slot = -1;
+        w.half = 0;
+    } else {
+        const int v = u - p.full_tiles;
+        w.slot = v >> 1;
+        w.half = v & 1;
+        w.tile = p.full_tiles + w.slot;
+        w.kb0 = w.half ? KB / 2 : 0;
+        w.kb1 = w.half ? KB : KB / 2;
+    }
+    return w;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* ptr)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1)
 {
@@ -111,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* drain = acc_empty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+    __shared__ int ticket_s;  // arrival order of this CTA's half of a split tile
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int KB = (p.H + kBK - 1) / kBK;
@@ -143,13 +190,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < kStages; ++s) issued_par[s] = 2;  // 2 = nothing issued
         int seq = 0;
-        for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
-            const int m = t / row_tiles;
-            const int nt = t - m * row_tiles;
+        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            const Unit w = unit_of(p, u, KB);
+            const int m = w.tile / row_tiles;
+            const int nt = w.tile - m * row_tiles;
             const bool is_v = nt >= p.n_half;
             const int col0 = (is_v ? nt - p.n_half : nt) * kBN;
             const CUtensorMap* tw = is_v ? &tm_wv : &tm_wk;
-            for (int kb = 0; kb < KB; ++kb, ++seq) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++seq) {
                 const int s = seq % kStages;
                 const uint32_t ph = (uint32_t)(seq / kStages) & 1u;
                 if (lane == 0) ok = wait_bounded(empty + s, ph ^ 1u, abort_flag, p.err);
@@ -182,15 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int seq = 0;
         int i = 0;
-        for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x, ++i) {
-            const int m = t / row_tiles;
+        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++i) {
+            const Unit w = unit_of(p, u, KB);
+            const int m = w.tile / row_tiles;
             const bool two = m * kBM + kBM / 2 < p.L;  // the second 128-row half holds tokens
             // the epilogue has read out the previous tile
             if (lane == 0) ok = wait_bounded(acc_empty, ((uint32_t)i & 1u) ^ 1u, abort_flag, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            for (int kb = 0; kb < KB; ++kb, ++seq) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb, ++seq) {
                 const int s = seq % kStages;
                 const uint32_t ph = (uint32_t)(seq / kStages) & 1u;
                 if (lane == 0) ok = wait_bounded(full + s, ph, abort_flag, p.err);
@@ -203,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; ++kk) {
                         const uint64_t bdesc = sw128_desc(sb + kk * 32, 16, 1024);
-                        const uint32_t acc_flag = (kb > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t acc_flag = (kb > w.kb0 || kk > 0) ? 1u : 0u;
                         tc_mma(tmem, sw128_desc(sa + kk * 32, 16, 1024), bdesc, idesc, acc_flag);
                         if (two)
                             tc_mma(tmem + kBN, sw128_desc(sa + kABytes / 2 + kk * 32, 16, 1024), bdesc, idesc,
@@ -231,14 +280,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = (warp - 2) >> 2;       // 0: rows 0-127 of the tile, 1: rows 128-255
         const uint32_t acc = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * kBN);
         int i = 0;
-        for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++i) {
-            const int m = t / row_tiles;
-            const int nt = t - m * row_tiles;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+            const Unit w = unit_of(p, u, KB);
+            const int m = w.tile / row_tiles;
+            const int nt = w.tile - m * row_tiles;
             const bool is_v = nt >= p.n_half;
             const int col0 = (is_v ? nt - p.n_half : nt) * kBN;
             const int ncols = min(kBN, p.N - col0);  // a multiple of 16
             const bool active = m * kBM + half * (kBM / 2) < p.L;  // this half was computed
-            const int row = m * kBM + half * (kBM / 2) + quarter * 32 + lane;
+            const int trow = half * (kBM / 2) + quarter * 32 + lane;  // row within the tile
+            const int row = m * kBM + trow;
             __nv_bfloat16* dst = nullptr;  // this token's slot, or none
             if (row < p.L) {
                 const int32_t slot = __ldg(p.slot_mapping + row);
@@ -253,8 +304,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             if (lane == 0) ok = wait_bounded(acc_full, (uint32_t)i & 1u, abort_flag, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
+            // A split tile's epilogue meets at named barriers: its 8 warps first agree on the
+            // wait's outcome (every warp reaches this barrier), so that they leave together.
+            if (w.slot >= 0) ok = !named_bar_or_256(!ok);
             if (!ok) break;
             tc_fence_after();
+            // a split tile: the first half to arrive publishes its partial, the second adds it
+            int role = 0;  // 0: whole tile, 1: publish the partial, 2: add the partial and store
+            float* part = nullptr;
+            if (w.slot >= 0) {
+                int32_t* sync = p.sync + 2 * w.slot;
+                if (threadIdx.x == 64) ticket_s = atomicAdd(sync, 1);
+                named_bar_sync_256();  // the 8 epilogue warps
+                role = ticket_s == 0 ? 1 : 2;
+                part = p.partial + (int64_t)w.slot * kBM * kBN + (int64_t)trow * kBN;
+                if (role == 2) {
+                    // wait (bounded) until the first half's partial is visible
+                    if (threadIdx.x == 64) {
+                        const unsigned long long t_start = globaltimer();
+                        int ready = ld_acquire_gpu(sync + 1);
+                        while (!ready && globaltimer() - t_start < kTimeoutNs) ready = ld_acquire_gpu(sync + 1);
+                        if (!ready) raise_error(p.err, DFLASH_DEVERR_TIMEOUT);
+                    }
+                    named_bar_sync_256();  // the 8 epilogue warps
+                }
+            }
             if (active) {
                 for (int c = 0; c < ncols; c += 32) {
                     uint32_t r0[16], r1[16];
@@ -263,6 +337,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
                     reg_fence16(r0);
                     reg_fence16(r1);
+                    if (role == 1) {
+                        float4* pp = reinterpret_cast<float4*>(part + c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            pp[v] = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
+                                                __uint_as_float(r0[4 * v + 2]), __uint_as_float(r0[4 * v + 3]));
+                            pp[4 + v] = make_float4(__uint_as_float(r1[4 * v]), __uint_as_float(r1[4 * v + 1]),
+                                                    __uint_as_float(r1[4 * v + 2]), __uint_as_float(r1[4 * v + 3]));
+                        }
+                        continue;
+                    }
+                    if (role == 2) {
+                        const float4* pp = reinterpret_cast<const float4*>(part + c);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float4 a = __ldcg(pp + v), b = __ldcg(pp + 4 + v);
+                            r0[4 * v] = __float_as_uint(__uint_as_float(r0[4 * v]) + a.x);
+                            r0[4 * v + 1] = __float_as_uint(__uint_as_float(r0[4 * v + 1]) + a.y);
+                            r0[4 * v + 2] = __float_as_uint(__uint_as_float(r0[4 * v + 2]) + a.z);
+                            r0[4 * v + 3] = __float_as_uint(__uint_as_float(r0[4 * v + 3]) + a.w);
+                            r1[4 * v] = __float_as_uint(__uint_as_float(r1[4 * v]) + b.x);
+                            r1[4 * v + 1] = __float_as_uint(__uint_as_float(r1[4 * v + 1]) + b.y);
+                            r1[4 * v + 2] = __float_as_uint(__uint_as_float(r1[4 * v + 2]) + b.z);
+                            r1[4 * v + 3] = __float_as_uint(__uint_as_float(r1[4 * v + 3]) + b.w);
+                        }
+                    }
                     if (dst) {
                         const int f0 = col0 + c;  // feature of column c: head f / D, dim f % D
                         store16(dst + (int64_t)(f0 / p.D) * p.sh + f0 % p.D, r0);
@@ -271,6 +371,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             store16(dst + (int64_t)(f1 / p.D) * p.sh + f1 % p.D, r1);
                         }
                     }
+                }
+            }
+            if (role == 1) {
+                // publish: every thread's partial rows are written before the flag is raised
+                __threadfence();
+                named_bar_sync_256();  // the 8 epilogue warps
+                if (threadIdx.x == 64) atomicExch(p.sync + 2 * w.slot + 1, 1);
+            } else if (role == 2) {
+                named_bar_sync_256();  // the 8 epilogue warps
+                if (threadIdx.x == 64) {  // both halves are done with this slot: reset it
+                    p.sync[2 * w.slot] = 0;
+                    p.sync[2 * w.slot + 1] = 0;
                 }
             }
             tc_fence_before();
@@ -329,10 +441,16 @@ int32_t project_kv_grid(int32_t L, int32_t N)
     return (int32_t)std::min<int64_t>(tiles, device_sm_count());
 }
 
+size_t project_kv_workspace_bytes()
+{
+    // the sync block, then one fp32 tile per split tile (at most half the CTAs' count)
+    return kProjectSyncBytes + (size_t)(device_sm_count() / 2) * kBM * kBN * sizeof(float);
+}
+
 cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t hidden_stride, const void* w_k,
                               const void* w_v, const int32_t* slot_mapping, void* k_cache, void* v_cache,
                               int32_t Hkv, int32_t D, int32_t page_size, int32_t num_pages, int64_t sp, int64_t ss,
-                              int64_t sh, uint32_t* err, cudaStream_t stream)
+                              int64_t sh, uint32_t* err, void* workspace, size_t workspace_bytes, cudaStream_t stream)
 {
     if (L == 0) return cudaSuccess;
     EncodeTiledFn enc = encode_fn();
@@ -358,9 +476,20 @@ cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t 
     p.sp = sp;
     p.ss = ss;
     p.sh = sh;
+    const int grid = project_kv_grid(L, N);
+    // split the tiles of a partial last round in two along the hidden dimension when the
+    // halves fit in that round and the workspace holds their partials
+    const int rem = p.tiles % grid;
+    const int KB = (H + kBK - 1) / kBK;
+    const bool split = workspace && rem > 0 && 2 * rem <= grid && KB >= 2 &&
+                       workspace_bytes >= kProjectSyncBytes + (size_t)rem * kBM * kBN * sizeof(float);
+    p.full_tiles = split ? p.tiles - rem : p.tiles;
+    p.units = split ? p.tiles + rem : p.tiles;
+    p.sync = static_cast<int32_t*>(workspace);
+    p.partial = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + kProjectSyncBytes) : nullptr;
     cudaError_t e = cudaFuncSetAttribute(project_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
     if (e != cudaSuccess) return e;
-    project_kv_kernel<<<project_kv_grid(L, N), kThreads, kAlloc, stream>>>(th, twk, twv, p);
+    project_kv_kernel<<<grid, kThreads, kAlloc, stream>>>(th, twk, twv, p);
     return cudaGetLastError();
 }
 

@@ -239,10 +239,10 @@ def test_project_kv_argument_checks(lib):
     P = ctypes.c_void_p
 
     def proj(L=64, H=5376, stride=5376, hidden=FAKE, wk=FAKE, wv=FAKE, slots=FAKE, kc=FAKE, vc=FAKE, err=None,
-             **dkw):
+             ws=None, **dkw):
         d = good_dims(**dkw)
         return lib.dflash_project_kv(P(hidden), L, H, stride, P(wk), P(wv), P(slots), P(kc), P(vc),
-                                     ctypes.byref(d), P(err) if err else None, None)
+                                     ctypes.byref(d), P(err) if err else None, P(ws) if ws else None, 1 << 24, None)
 
     assert proj(L=0, hidden=None, slots=None) == B.OK  # no tokens: nothing is read or launched
     assert proj(dtype=B.FP32) == B.ERR_UNSUPPORTED
@@ -264,6 +264,7 @@ def test_project_kv_argument_checks(lib):
     assert proj(slots=FAKE + 2) == B.ERR_INVALID_ARG
     assert proj(err=FAKE + 1) == B.ERR_INVALID_ARG
     assert b"misaligned" in lib.dflash_last_error_message()
+    assert proj(ws=FAKE + 16) == B.ERR_WORKSPACE       # the workspace is 256-byte aligned
 
 
 @cpu_only

@@ -164,3 +164,25 @@ def test_full_size_prefill_sampled_rows():
     _check(hidden, w_k, w_v, k_cache, v_cache, pages, pos, rows=rows)
     _untouched(k_cache, pages, pos)
     _untouched(v_cache, pages, pos)
+
+
+@pytest.mark.parametrize("split", [True, False])
+def test_split_last_round_matches_oracle(split):
+    # 5000 tokens into 4 x 512 features: 20 x 16 = 320 tiles of 256 x 256 on 152 SMs leave 16
+    # for a third round, which the split runs as 32 halves along the hidden dimension
+    L, H, Hkv, D, P = 5000, 512, 4, 512, 16
+    num_pages = L // P + 8
+    hidden, w_k, w_v, k_cache, v_cache = _inputs(L, H, Hkv, D, P, num_pages, seed=31)
+    pages, pos, slots = _slots(L, P, num_pages, seed=32)
+    ws = torch.zeros(dfl.load_library().dflash_project_kv_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace: its counters were reset
+        k_cache.fill_(SENTINEL)
+        v_cache.fill_(SENTINEL)
+        dfl.project_kv(hidden, w_k, w_v, slots, k_cache, v_cache, device_error=err, workspace=ws if split else None,
+                       split=split)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        _check(hidden, w_k, w_v, k_cache, v_cache, pages, pos)
+        _untouched(k_cache, pages, pos)
+    assert int(ws[:8192].view(torch.int32).abs().sum().item()) == 0  # the counter block is back at zero
