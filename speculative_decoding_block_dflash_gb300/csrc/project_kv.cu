@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++seq) {
                 const int s = seq % kStages;
                 const uint32_t ph = (uint32_t)(seq / kStages) & 1u;
-                if (lane == 0) ok = wait_bounded(empty + s, ph ^ 1u, abort_flag, p.err);
+                if (lane == 0) ok = ring_wait(empty + s, ph ^ 1u, abort_flag, p.err);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 if (lane == 0) {
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++seq) {
                 const int s = seq % kStages;
                 const uint32_t ph = (uint32_t)(seq / kStages) & 1u;
-                if (lane == 0) ok = wait_bounded(full + s, ph, abort_flag, p.err);
+                if (lane == 0) ok = ring_wait(full + s, ph, abort_flag, p.err);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 tc_fence_after();

@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const RingSlot sl = ring_slot(seq, S, E);
                         uint64_t* fb = sl.extra ? xfull + sl.idx : full + sl.idx;
                         if (!sl.extra) {
-                            if (lane == 0) ok = wait_bounded(empty + sl.idx, sl.phase ^ 1u, abort_flag, p.err);
+                            if (lane == 0) ok = ring_wait(empty + sl.idx, sl.phase ^ 1u, abort_flag, p.err);
                             ok = __shfl_sync(0xffffffffu, ok, 0);
                             if (!ok) break;
                         }
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         auto wait_lane0 = [&](uint64_t* bar, uint32_t par) -> bool {
             bool got = true;
-            if (lane == 0) got = wait_bounded(bar, par, abort_flag, p.err);
+            if (lane == 0) got = ring_wait(bar, par, abort_flag, p.err);
             return __shfl_sync(0xffffffffu, got, 0);
         };
         // wait for the next stage; its shared address (and whether it is an extra slot)
@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // uniform across the 128 softmax threads (so none is left at a barrier).
         auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool got = true;
-            if (tid == 0) got = wait_bounded(bar, parity, abort_flag, p.err);
+            if (tid == 0) got = ring_wait(bar, parity, abort_flag, p.err);
             return !named_bar_or_128(!got);
         };
 

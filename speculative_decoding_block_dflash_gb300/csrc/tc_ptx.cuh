@@ -74,6 +74,40 @@ static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity,
     }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the short hand-offs of a pipeline (a ring stage landed or freed, a tile's
+// scores or probabilities ready): a spin on the non-suspending test_wait. A try_wait that
+// suspends resumes some time after the phase completes; on these hand-offs, taken several
+// hundred times per tile, that latency added 10-30 % to the kernels' times. Same outcome and
+// error reporting as wait_bounded.
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        for (int k = 0; k < 64; ++k)
+            if (mbar_test_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            raise_error(err, DFLASH_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
