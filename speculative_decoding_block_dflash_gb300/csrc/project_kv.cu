@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int m = w.tile / row_tiles;
             const bool two = m * kBM + kBM / 2 < p.L;  // the second 128-row half holds tokens
             // the epilogue has read out the previous tile
-            if (lane == 0) ok = wait_bounded(acc_empty, ((uint32_t)i & 1u) ^ 1u, abort_flag, p.err);
+            if (lane == 0) ok = ring_wait(acc_empty, ((uint32_t)i & 1u) ^ 1u, abort_flag, p.err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
@@ -301,12 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         raise_error(p.err, DFLASH_DEVERR_PAGE_ID);
                 }
             }
-            bool ok = true;
-            if (lane == 0) ok = wait_bounded(acc_full, (uint32_t)i & 1u, abort_flag, p.err);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            // A split tile's epilogue meets at named barriers: its 8 warps first agree on the
-            // wait's outcome (every warp reaches this barrier), so that they leave together.
-            if (w.slot >= 0) ok = !named_bar_or_256(!ok);
+            // One thread spins on the accumulators (the other epilogue warps sleep at the named
+            // barrier, leaving the issue slots to the producer and MMA warps); the barrier's OR
+            // gives all 8 warps the wait's outcome, so that they leave together.
+            bool got = true;
+            if (threadIdx.x == 64) got = ring_wait(acc_full, (uint32_t)i & 1u, abort_flag, p.err);
+            const bool ok = !named_bar_or_256(!got);
             if (!ok) break;
             tc_fence_after();
             // a split tile: the first half to arrive publishes its partial, the second adds it
