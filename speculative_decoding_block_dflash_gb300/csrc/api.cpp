@@ -197,6 +197,13 @@ int64_t work_units(const dflash_dims* d, int32_t T, int kernel)
     return (int64_t)d->batch * d->num_q_heads * ((T + 15) / 16);
 }
 
+// Chunks longer than kLongChunkKeys run better as many uniform waves of about
+// kTargetChunkKeys keys than as one wave of long streams (measured on 8 requests of 131072
+// keys: 19 chunks of 6.9k keys, 8 waves, 3659 us; one balanced wave, 4245 us; 12 or 24
+// chunks, 4280 and 3978 us).
+constexpr int64_t kLongChunkKeys = 16384;
+constexpr int64_t kTargetChunkKeys = 7168;
+
 int32_t plan_splits_impl(const dflash_dims* d, int32_t T, int32_t window, int32_t requested, int kernel)
 {
     if (requested > 0) return requested > DFLASH_MAX_SPLITS ? -DFLASH_ERR_INVALID_ARG : requested;
@@ -215,6 +222,8 @@ int32_t plan_splits_impl(const dflash_dims* d, int32_t T, int32_t window, int32_
     const int64_t units = work_units(d, T, kernel);
     const int64_t sms = device_sm_count();
     int64_t s = sms / units;
+    // one wave would leave very long chunks: take more, shorter chunks over several waves
+    if (span / std::max<int64_t>(1, s) > kLongChunkKeys) s = (span + kTargetChunkKeys - 1) / kTargetChunkKeys;
     s = std::min<int64_t>(s, max_by_len);
     s = std::min<int64_t>(s, DFLASH_MAX_SPLITS);
     return (int32_t)std::max<int64_t>(1, s);
@@ -224,7 +233,7 @@ int32_t plan_splits_impl(const dflash_dims* d, int32_t T, int32_t window, int32_
 
 namespace dflash {
 
-int32_t balanced_slots(const dflash_dims* d, int32_t T, int32_t window, int kernel)
+int32_t balanced_slots(const dflash_dims* d, int32_t T, int32_t window, int kernel, bool allow_long)
 {
     if (kernel != DFLASH_KERNEL_TC || d->batch < 2) return 0;
     AttnParams p{};
@@ -241,6 +250,10 @@ int32_t balanced_slots(const dflash_dims* d, int32_t T, int32_t window, int kern
     c = std::min<int64_t>(c, (int64_t)d->batch * std::max<int64_t>(1, span / 128));  // >= a tile each
     c = std::min<int64_t>(c, DFLASH_MAX_SPLITS);
     if (c < d->batch || c < 2) return 0;
+    // one wave of slots over long requests gives long streams: the uniform plan's several
+    // waves of shorter chunks do better (the in-kernel combine needs the grid resident, so the
+    // balanced plan cannot spread wider)
+    if (!allow_long && (int64_t)d->batch * span / c > kLongChunkKeys) return 0;
     return (int32_t)c;
 }
 
@@ -291,6 +304,18 @@ dflash_status dflash_block_attn(const void* q, const void* k_cache, const void* 
                                 int32_t block_len, int32_t causal, int32_t window, float scale, void* out,
                                 float* lse, const dflash_opts* opts)
 {
+    return dflash::block_attn_planned(q, k_cache, v_cache, page_table, seq_lens, dims, block_len, causal, window,
+                                      scale, out, lse, opts, 0, false);
+}
+
+}  // extern "C"
+
+dflash_status dflash::block_attn_planned(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* page_table, const int32_t* seq_lens, const dflash_dims* dims,
+                                         int32_t block_len, int32_t causal, int32_t window, float scale, void* out,
+                                         float* lse, const dflash_opts* opts, int32_t forced_splits,
+                                         bool forced_balanced)
+{
     g_last_error.clear();
     dflash_status s = check_dims(dims, block_len);
     if (s != DFLASH_OK) return s;
@@ -316,11 +341,16 @@ dflash_status dflash_block_attn(const void* q, const void* k_cache, const void* 
                                                   ? "the tensor-core kernel does not cover these sizes/dtype"
                                                   : "unknown kernel selector %d",
                     kreq);
-    const int32_t splits = plan_splits_impl(dims, block_len, window, requested, kernel);
-    if (splits < 1) return fail(DFLASH_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", requested, DFLASH_MAX_SPLITS);
-
-    // Length-balanced plan: partials are [slot][T][Hq][D], so the layout is sized for one request.
-    const bool balanced = requested == 0 && splits > 1 && balanced_slots(dims, block_len, window, kernel) == splits;
+    int32_t splits = forced_splits;
+    bool balanced = forced_balanced;
+    if (splits < 1) {
+        splits = plan_splits_impl(dims, block_len, window, requested, kernel);
+        if (splits < 1)
+            return fail(DFLASH_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", requested, DFLASH_MAX_SPLITS);
+        // Length-balanced plan: partials are [slot][T][Hq][D], so the layout is sized for one request.
+        balanced = requested == 0 && splits > 1 && balanced_slots(dims, block_len, window, kernel) == splits;
+    }
+    if (balanced && kernel != DFLASH_KERNEL_TC) return fail(DFLASH_ERR_INVALID_ARG, "balanced plan needs the TC kernel");
     const WorkspaceLayout wl =
         workspace_layout(balanced ? 1 : dims->batch, block_len, dims->num_q_heads, dims->head_dim, splits);
     void* ws = opts ? opts->workspace : nullptr;
@@ -378,6 +408,8 @@ dflash_status dflash_block_attn(const void* q, const void* k_cache, const void* 
     }
     return DFLASH_OK;
 }
+
+extern "C" {
 
 size_t dflash_accept_workspace_bytes(int32_t batch, int32_t block_len)
 {

@@ -74,8 +74,14 @@ cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t 
                               cudaStream_t stream);
 
 // Slots of the tensor-core kernel's length-balanced split plan for these sizes (auto split
-// count, B > 1, whole grid resident), or 0 when the plan is uniform.
-int32_t balanced_slots(const dflash_dims* d, int32_t T, int32_t window, int kernel);
+// count, B > 1, whole grid resident), or 0 when the plan is uniform. The auto plan leaves it
+// for very long key spans (allow_long = false); the no-alloc entry point may still take it.
+int32_t balanced_slots(const dflash_dims* d, int32_t T, int32_t window, int kernel, bool allow_long = false);
+// dflash_block_attn with the split plan given (forced_splits >= 1) or planned (forced_splits < 1).
+dflash_status block_attn_planned(const void* q, const void* k_cache, const void* v_cache, const int32_t* page_table,
+                                 const int32_t* seq_lens, const dflash_dims* dims, int32_t block_len, int32_t causal,
+                                 int32_t window, float scale, void* out, float* lse, const dflash_opts* opts,
+                                 int32_t forced_splits, bool forced_balanced);
 // Kernel a selector resolves to for these sizes (a dflash_kernel value), or -status.
 int resolve_kernel(const dflash_dims* d, int32_t T, int32_t window, int32_t requested);
 

@@ -49,7 +49,7 @@ extern "C" DFLASH_API dflash_status dflash_block_attn_noalloc(
     const dflash_dims* dims, int32_t block_len, int32_t causal, int32_t window, float scale, void* out, float* lse,
     int32_t num_splits, int32_t kernel, void* stream)
 {
-    const int32_t splits = dflash_plan_splits(dims, block_len, window, num_splits, kernel);
+    int32_t splits = dflash_plan_splits(dims, block_len, window, num_splits, kernel);
     if (splits < 1) {
         // invalid sizes: let the main entry point report the precise reason
         dflash_opts o{};
@@ -60,9 +60,25 @@ extern "C" DFLASH_API dflash_status dflash_block_attn_noalloc(
                                  out, lse, &o);
     }
     const int kres = resolve_kernel(dims, block_len, window, kernel);
-    const bool balanced = num_splits == 0 && splits > 1 && balanced_slots(dims, block_len, window, kres) == splits;
-    const size_t need =
-        workspace_layout(balanced ? 1 : dims->batch, block_len, dims->num_q_heads, dims->head_dim, splits).total;
+    bool balanced = num_splits == 0 && splits > 1 && balanced_slots(dims, block_len, window, kres) == splits;
+    auto need_of = [&](int32_t s, bool bal) {
+        return workspace_layout(bal ? 1 : dims->batch, block_len, dims->num_q_heads, dims->head_dim, s).total;
+    };
+    size_t need = need_of(splits, balanced);
+    if (num_splits == 0 && need > (size_t)DFLASH_NOALLOC_SCRATCH_BYTES) {
+        // The auto plan's partials do not fit the scratch (many uniform waves over very long
+        // requests): take the one-wave length-balanced plan, whose partials are sized for one
+        // request, if it fits; else the most uniform chunks that fit.
+        const int32_t bal = balanced_slots(dims, block_len, window, kres, /*allow_long=*/true);
+        if (bal > 1 && need_of(bal, true) <= (size_t)DFLASH_NOALLOC_SCRATCH_BYTES) {
+            splits = bal;
+            balanced = true;
+        } else {
+            while (splits > 1 && need_of(splits, false) > (size_t)DFLASH_NOALLOC_SCRATCH_BYTES) --splits;
+            balanced = false;
+        }
+        need = need_of(splits, balanced);
+    }
     if (need > (size_t)DFLASH_NOALLOC_SCRATCH_BYTES)
         return report_error(DFLASH_ERR_WORKSPACE,
                             "dflash_block_attn_noalloc: %d splits need %zu bytes of scratch, more than the %u bytes "
@@ -77,11 +93,12 @@ extern "C" DFLASH_API dflash_status dflash_block_attn_noalloc(
     e = cudaMemsetAsync(ws, 0, wl.part_lse_off, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return report_error(DFLASH_ERR_CUDA, "clearing the scratch header: %s", cudaGetErrorString(e));
     dflash_opts o{};
-    o.num_splits = num_splits;  // the same request re-plans to the same split count and layout
+    o.num_splits = num_splits;
     o.kernel = kernel;
     o.workspace = ws;
     o.workspace_bytes = DFLASH_NOALLOC_SCRATCH_BYTES;
     o.stream = stream;
-    return dflash_block_attn(q, k_cache, v_cache, page_table, seq_lens, dims, block_len, causal, window, scale, out,
-                             lse, &o);
+    // the plan chosen above (it may differ from the auto plan when that would not fit)
+    return block_attn_planned(q, k_cache, v_cache, page_table, seq_lens, dims, block_len, causal, window, scale, out,
+                              lse, &o, splits, balanced);
 }

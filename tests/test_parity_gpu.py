@@ -365,3 +365,26 @@ def test_cuda_graph_capture_and_replay():
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert torch.equal(lse, lref)
+
+
+def _plan_dims(B, T, Hq, Hkv, D, P, max_pages):
+    d = dfl.Dims()
+    d.batch, d.num_q_heads, d.num_kv_heads, d.head_dim = B, Hq, Hkv, D
+    d.page_size, d.num_pages, d.max_pages, d.max_seq_len = P, B * max_pages, max_pages, 0
+    d.dtype = dfl.BF16
+    d.kv_stride_head, d.kv_stride_slot, d.kv_stride_page = D, Hkv * D, P * Hkv * D
+    return d
+
+
+def test_auto_plan_spreads_long_spans_over_waves():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # 8 requests of up to 131072 keys, blocks of 16 (two row groups per KV head): one wave of
+    # balanced slots would stream ~55k keys each, so the plan is uniform chunks of ~7k keys
+    long = _plan_dims(8, 16, 32, 4, 512, 16, 131072 // 16)
+    assert dfl.plan_splits(long, 16, 0, 0, "tc") == -(-131072 // 7168)
+    # up to 32768 keys over 8 requests keeps the one-wave length-balanced plan
+    sweep = _plan_dims(8, 9, 32, 4, 512, 16, 32768 // 16)
+    assert dfl.plan_splits(sweep, 9, 0, 0, "tc") == sms // 4
+    # one request of 8192 keys: one wave of 38 chunks on 152 SMs
+    one = _plan_dims(1, 9, 32, 4, 512, 16, 8192 // 16)
+    assert dfl.plan_splits(one, 9, 0, 0, "tc") == sms // 4
