@@ -98,3 +98,18 @@ def test_noalloc_rejects_plans_beyond_its_scratch():
                                        case.block_len, 0, 0, case.scale, out.data_ptr(), None, 32, 0, None)
     assert st == B.ERR_WORKSPACE
     assert "scratch" in lib.dflash_last_error_message().decode()
+
+
+def test_noalloc_falls_back_when_the_auto_plan_does_not_fit():
+    # 8 requests of 40000 keys in blocks of 16: the auto plan is 6 uniform chunks of ~7k keys,
+    # whose fp32 partials (~50 MB) exceed the 32 MiB scratch; the no-alloc call takes the
+    # one-wave length-balanced plan (partials sized for one request) and agrees with it
+    case = workloads.make_custom("noalloc_long", 8, 16, 32, 4, 512, [40000] * 8, seed=75, device="cuda")
+    dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
+    splits = dfl.plan_splits(dims, case.block_len, 0, 0, "auto")
+    assert splits == -(-dims.max_pages * dims.page_size // 7168)
+    assert dfl.workspace_bytes(dims, case.block_len, splits) > 32 * 1024 * 1024
+    ref_o, ref_l = _reference(case, 0, "auto")
+    out, lse = _noalloc(case, 0, "auto")
+    _close(out, ref_o, 1e-2)
+    _close(lse, ref_l, 1e-2)
