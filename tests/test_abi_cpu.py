@@ -324,3 +324,16 @@ def test_selector_workspace_and_argument_checks(lib):
     assert walk(ws=None) == B.ERR_WORKSPACE
     assert walk(ws_bytes=1024) == B.ERR_WORKSPACE
     assert b"workspace" in lib.dflash_last_error_message()
+
+
+def test_auto_plan_takes_uniform_waves_for_long_spans(lib):
+    # the planner's host logic (no kernel runs): 8 requests of up to 131072 keys in blocks of 16
+    # would give one balanced wave of ~55k-key chunks, so the auto plan takes uniform chunks of
+    # about 7168 keys over several waves; up to 32768 keys keeps the one-wave balanced plan
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    long = good_dims(batch=8, max_pages=131072 // 16, num_pages=8 * (131072 // 16))
+    assert lib.dflash_plan_splits(ctypes.byref(long), 16, 0, 0, 0) == -(-131072 // 7168)
+    sweep = good_dims(batch=8, max_pages=32768 // 16, num_pages=8 * (32768 // 16))
+    assert lib.dflash_plan_splits(ctypes.byref(sweep), 9, 0, 0, 0) == sms // 4
+    # an explicit count is taken as given
+    assert lib.dflash_plan_splits(ctypes.byref(long), 16, 0, 5, 0) == 5
