@@ -405,8 +405,8 @@ def accept_bench(args, dfl, dev, rank, world):
                         "the logits are device-resident"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": value / world, "peak": peak, "unit": "GB/s",
-                     "frac": value / world / peak, "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "accept_kernel",
+                     "frac": value / world / peak, "traffic": traffic_from_profiles("accept_kernel")[0],
+                     "peak_kind": peak_kind, "kernel": "accept_kernel",
                      "achieved_basis": "logits bytes per launch / event-timed device time per step"},
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
