@@ -314,7 +314,8 @@ def accept_prefix(logits: torch.Tensor, draft: torch.Tensor, workspace: Optional
                   stream=None) -> Tuple[torch.Tensor, torch.Tensor, Optional[torch.Tensor]]:
     """Longest-prefix acceptance (dflash_accept_prefix): logits [B, T, V] bf16/fp32 (last
     dim contiguous), draft int32 [B, T-1] -> (accepted_len [B], next_token [B], target
-    argmax [B, T] or None), int32 on the device."""
+    argmax [B, T] or None), int32 on the device. Without a workspace the call uses one cached
+    per device: calls that may overlap (different streams) must each pass their own."""
     lib = load_library()
     if logits.dim() != 3 or logits.stride(2) != 1 or logits.stride(0) != logits.shape[1] * logits.stride(1):
         raise ValueError("logits must be [B, T, V] with contiguous rows of a common stride")
@@ -356,8 +357,9 @@ def project_kv(hidden: torch.Tensor, w_k: torch.Tensor, w_v: torch.Tensor, slot_
     slot_mapping int32 [L] (page * page_size + position; < 0 skips the token), caches
     [num_pages, page_size, Hkv, D] bf16 (d contiguous, same strides). device_error: an
     optional int32/uint32 device word that receives DEVERR_* bits. With split (the default)
-    the last round's tiles are split in two through a workspace (a zeroed cached one when
-    none is given); split=False computes every tile whole."""
+    the last round's tiles are split in two through a workspace (a zeroed one cached per
+    device when none is given: calls that may overlap must each pass their own);
+    split=False computes every tile whole."""
     lib = load_library()
     if split and workspace is None and hidden.numel():
         dev = hidden.device
@@ -448,7 +450,8 @@ def selector_walk(pred_codebook: torch.Tensor, succ_codebook: torch.Tensor, proj
     """DFlash2 candidate-selector walk (dflash_selector_walk). Codebooks bf16 [V, E]; proj float32
     [R, S, E]; candidates int32 [R, S, K]; unary float32 [R, S, K]; anchor int32 [R]; uniforms
     float32 [R, S] when temperature > 0. Returns (tokens [R, S], chosen [R, S], path_scores
-    [R, S, K] or None, q [R, S, K] or None)."""
+    [R, S, K] or None, q [R, S, K] or None). Without a workspace the call uses one cached per
+    device: calls that may overlap (different streams) must each pass their own."""
     lib = load_library()
     V, E = pred_codebook.shape
     R, S, K = candidates.shape
