@@ -34,9 +34,14 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-WORKLOAD = "global_verify"
-WORKLOAD_DESC = ("global-layer verify: batch 1, block_len 9, 32 q heads / 4 KV heads (GQA 8), head_dim 512, "
-                 "context 8192, paged KV page size 16, shuffled page table over a 2x pool, bf16, causal=False")
+WORKLOAD = "long_draft"
+WORKLOAD_DESC = ("long-context split-KV draft cross-attention: batch 8, block_len 16 (num_spec 15), 32 q heads / "
+                 "4 KV heads (GQA 8), head_dim 512, context 131072 tokens paged (page 16, shuffled page table), "
+                 "16 split-KV chunks with LSE combine; K/V projected from N(0,1) hidden states of width 5376 "
+                 "through N(0, 0.02^2) weights, bf16, causal=False")
+# The other attention workloads, measured in the same run and reported under "workloads".
+OTHER_WORKLOADS = ["global_verify", "batch_sweep_b1", "batch_sweep_b2", "batch_sweep_b4", "batch_sweep_b8",
+                   "sliding", "sliding_causal"]
 METRIC = "kv_hbm_gbs"
 UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
@@ -81,11 +86,13 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=WORKLOAD)
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc", "tc_pair"])
     ap.add_argument("--splits", type=int, default=-1, help="-1: the workload's own (auto unless fixed)")
     ap.add_argument("--layers", type=int, default=0, help="page-set rotation count (0 = enough to exceed 4x L2)")
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="headline run only: skip the other attention workloads' extra key")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle time for --impl reference")
     return ap.parse_args()
@@ -200,12 +207,12 @@ def host_copy_of_layer(case, layer=0):
     return dict(q=case.q.cpu(), k=k, v=v, pt=pt2, sl=case.seq_lens.cpu())
 
 
-def time_oracle_full(case, budget_s):
+def time_oracle_full(case, budget_s, threads=None):
     """Oracle over whole steps (every row, every key) until the budget is used; seconds per step."""
     import oracle
 
     h = host_copy_of_layer(case)
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     times = []
     t_start = time.perf_counter()
     while True:
@@ -216,6 +223,57 @@ def time_oracle_full(case, budget_s):
         if time.perf_counter() - t_start > budget_s or len(times) >= 50:
             break
     return statistics.median(times), len(times), threads
+
+
+def group_host_problem(case, b, g, kb):
+    """Host copy of one (request b, KV head g) group of a case restricted to keys [kb, L_b): the
+    G query heads' block rows and the pages that hold those keys, compacted (index work only).
+    Returns the oracle's inputs and the key range in the compacted positions."""
+    T, P = case.block_len, case.page_size
+    G = case.num_q_heads // case.num_kv_heads
+    L = case.seq_lens_host()[b]
+    p0, p1 = kb // P, (L + P - 1) // P
+    pages = case.page_table[b, p0:p1].long()
+    k = case.k_cache[pages][:, :, g:g + 1, :].cpu()
+    v = case.v_cache[pages][:, :, g:g + 1, :].cpu()
+    q = case.q[b * T:(b + 1) * T, g * G:(g + 1) * G, :].cpu()
+    pt = torch.arange(p1 - p0, dtype=torch.int32).view(1, -1)
+    sl = torch.tensor([L - p0 * P], dtype=torch.int32)
+    return dict(q=q, k=k, v=v, pt=pt, sl=sl, key_range=(kb - p0 * P, L - p0 * P))
+
+
+def time_oracle_group_sample(case, budget_s, threads=None):
+    """Oracle time per full step, estimated from whole (request, KV head) groups.
+
+    Only for non-causal global workloads, whose oracle work is (rows x keys seen): groups are
+    timed one after another (request-major) until about budget_s of oracle time is spent or
+    every group is done, and a full step is the sampled time x (keys of all groups / keys of
+    the sampled groups)."""
+    import oracle
+
+    assert not case.causal and case.window == 0
+    threads = threads or oracle.default_threads()
+    lens = case.seq_lens_host()
+    t_sum, keys_done, groups = 0.0, 0, []
+    for b in range(case.batch):
+        for g in range(case.num_kv_heads):
+            h = group_host_problem(case, b, g, 0)
+            t0 = time.perf_counter()
+            oracle.block_attn(h["q"], h["k"], h["v"], h["pt"], h["sl"], case.block_len, scale=case.scale,
+                              key_range=h["key_range"], num_threads=threads)
+            t_sum += time.perf_counter() - t0
+            keys_done += lens[b]
+            groups.append((b, g))
+            if t_sum >= budget_s:
+                break
+        if t_sum >= budget_s:
+            break
+    total_keys = sum(lens) * case.num_kv_heads
+    t_step = t_sum * total_keys / keys_done
+    rows = case.block_len * (case.num_q_heads // case.num_kv_heads)
+    sample = (f"{len(groups)} of {case.batch * case.num_kv_heads} (request, KV head) groups, each in full "
+              f"({rows} rows x every key), {t_sum:.1f} s; scaled by keys to a full step")
+    return t_step, sample, threads
 
 
 def reference_arm(args, case):
@@ -256,6 +314,59 @@ def reference_arm(args, case):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "block_queries_per_s": case.batch / t_step,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def group_reference_arm(args):
+    """--impl reference for long_draft: each step is the oracle over one (request, KV head) group
+    of the workload restricted to its last keys (a group of the same shapes and distributions,
+    generated on its own), scaled by the keys of every group to a full step."""
+    import oracle
+    import workloads
+
+    sh = workloads.LONG_DRAFT
+    threads = oracle.default_threads()
+    n_steps = args.steps + args.warmup
+
+    def make(keys):
+        case = workloads.make_group_sample(WORKLOAD, keys, device="cpu", seed=1234 + 4)
+        h = host_copy_of_layer(case)
+        return case, h
+
+    def run(case, h):
+        t0 = time.perf_counter()
+        oracle.block_attn(h["q"], h["k"], h["v"], h["pt"], h["sl"], case.block_len, scale=case.scale,
+                          num_threads=threads)
+        return time.perf_counter() - t0
+
+    cal_keys = 512
+    case, h = make(cal_keys)
+    t_cal = run(case, h)
+    keys = int(min(sh["L"], max(cal_keys, cal_keys * args.ref_budget / max(1e-6, n_steps * t_cal))))
+    keys = max(case.page_size, keys // case.page_size * case.page_size)
+    case, h = make(keys)
+    for _ in range(args.warmup):
+        run(case, h)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run(case, h)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    total_keys = sh["B"] * sh["L"] * sh["Hkv"]
+    t_step = dt * total_keys / keys
+    kv = total_keys * sh["D"] * 2 * 2
+    value = kv / t_step / 1e9
+    sample = (f"each step: oracle over one (request, KV head) group (all {sh['T'] * sh['Hq'] // sh['Hkv']} rows) "
+              f"and the last {keys} of its {sh['L']} keys, generated with the workload's shapes and "
+              f"distributions; time scaled by {total_keys / keys:.0f} to a full step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "block_queries_per_s": sh["B"] / t_step,
     }
     print(json.dumps(line), flush=True)
 
@@ -923,13 +1034,18 @@ def sel_bench(args, dfl, dev, rank, world):
 # ----------------------------------------------------------------------------- GPU arm
 
 
-def traffic_from_profiles(kernel_name):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+def traffic_from_profiles(kernel_name, workload=None):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on this workload (records
+    keyed "kernel@workload", or by the kernel alone for single-workload kernels), if the kernel
+    source is unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None, None
     try:
-        rec = json.load(open(path)).get(kernel_name)
+        recs = json.load(open(path))
+        rec = recs.get(f"{kernel_name}@{workload}") if workload else None
+        if rec is None:
+            rec = recs.get(kernel_name)
     except (ValueError, OSError):
         return None, None
     if not rec:
@@ -1011,6 +1127,11 @@ def main():
             if dist:
                 dist.destroy_process_group()
             return
+        if args.config == WORKLOAD:
+            group_reference_arm(args)
+            if dist:
+                dist.destroy_process_group()
+            return
         import workloads
 
         case = workloads.make_case(args.config, device="cuda" if torch.cuda.is_available() else "cpu")
@@ -1052,12 +1173,174 @@ def main():
             dist.destroy_process_group()
         return
 
-    probe = workloads.make_case(args.config, device=dev, layers=1)
+    headline = args.config == WORKLOAD
+    st = attn_setup(args.config, args, dfl, dev, workloads)
+    case, splits, layers = st["case"], st["splits"], st["layers"]
+    kv = kv_bytes_per_step(case)
+
+    for k in range(max(3, args.warmup)):
+        st["graphs"][k % layers].replay()
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0, period_ms=20)
+    if rank == 0:
+        sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for k in range(args.steps):
+        st["graphs"][k % layers].replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total_t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+    if dist:
+        dist.all_reduce(ms_total_t, op=dist.ReduceOp.MAX)
+    ms_per_step = float(ms_total_t.item()) / args.steps
+    value = world * kv / (ms_per_step * 1e-3) / 1e9
+    bq = world * case.batch / (ms_per_step * 1e-3)
+
+    # A clock record that covers what it times: at least one second of the same replays, with
+    # the SM clock and throttle reasons sampled inside it (the timed region above can be
+    # shorter than the sampling period).
+    n_win = max(args.steps, int(math.ceil(1000.0 / max(1e-3, ms_per_step))))
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    tw0 = time.time()
+    w0.record(stream)
+    for k in range(n_win):
+        st["graphs"][k % layers].replay()
+    w1.record(stream)
+    torch.cuda.synchronize()
+    tw1 = time.time()
+    win_ms = w0.elapsed_time(w1) / n_win
+    if rank == 0:
+        sampler.stop()
+
+    # eager ctypes path, one call per step, for reference (not the headline)
+    n_eager = min(args.steps, 2000)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for k in range(n_eager):
+        st["call"](k % layers)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / n_eager
+
+    e2e = e2e_measure(st, args, dfl, dev, stream, dist)
+    assert dfl.read_error(st["ws"]) == 0, "device-side check failed"
+
+    info = st["plan"]
+    kernel_name = info["kernel_name"]
+    peak, peak_kind = measured_peaks()
+    traffic, traffic_note = traffic_from_profiles(kernel_name, args.config)
+    achieved = kv / (ms_per_step * 1e-3) / 1e9
+    gpu_launches = args.steps * info["launches"]
+    del st
+    torch.cuda.empty_cache()
+
+    # the other attention workloads, each on its own graphs (parity cases elsewhere; reported here)
+    others = {}
+    if headline and not args.no_other_workloads:
+        for name in OTHER_WORKLOADS:
+            others[name] = other_workload(name, args, dfl, dev, workloads, peak)
+            torch.cuda.empty_cache()
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    clocks = sampler.summary(t_wall0, t_wall1)
+    win_clocks = sampler.summary(tw0, tw1)
+    clocks["window"] = {"replays": n_win, "seconds": tw1 - tw0, "ms_per_step": win_ms,
+                        "sm_mhz": win_clocks["sm_mhz"], "sm_max_mhz": win_clocks["sm_max_mhz"],
+                        "reasons": win_clocks["reasons"], "samples": win_clocks["samples"]}
+    if not clocks["samples"]:
+        # the timed region fell between two samples: the window's clocks stand for it
+        clocks["sm_mhz"], clocks["sm_max_mhz"] = win_clocks["sm_mhz"], win_clocks["sm_max_mhz"]
+        clocks["reasons"] = win_clocks["reasons"]
+        clocks["samples_note"] = "no sample fell inside the timed region; the clocks are the 1 s window's"
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        case_cpu = workloads.make_case(args.config, device=dev, layers=1)
+        if headline:
+            t_step, sample, threads = time_oracle_group_sample(case_cpu, args.cpu_budget)
+            cpu = {"value": kv / t_step / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+        else:
+            t_step, n_rep, threads = time_oracle_full(case_cpu, args.cpu_budget)
+            cpu = {"value": kv / t_step / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+                   "sample": f"{n_rep} full steps of layer 0 (all {case_cpu.q.shape[0] * case_cpu.q.shape[1]} "
+                             f"rows, every visible key), median {t_step * 1e3:.1f} ms per step"}
+        del case_cpu
+        if headline:
+            # the global-layer verify workload on one host core, in full
+            gv = workloads.make_case("global_verify", device=dev, layers=1)
+            t1, n1, _ = time_oracle_full(gv, 0.0, threads=1)
+            cpu["global_verify_1core"] = {"value": kv_bytes_per_step(gv) / t1 / 1e9, "unit": UNIT, "cores": 1,
+                                          "ms_per_step": t1 * 1e3,
+                                          "sample": "one full step (all 288 rows, every key) on one thread"}
+            del gv
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if case.q.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC if headline else args.config,
+                   "global_batch": case.batch * world, "block_len": case.block_len,
+                   "seq_len": max(case.seq_lens_host()), "splits": splits, "kernel": kernel_name,
+                   "l2": f"inputs larger than L2: {layers} rotated page sets x {kv / 1e6:.1f} MB K/V",
+                   "timed_path": "one CUDA-graph replay of one dflash_block_attn call per step",
+                   "parallelism": f"replicas x{world}"},
+        "block_queries_per_s": bq,
+        "query_rows_per_s": bq * case.block_len * case.num_q_heads,
+        "eager_ms_per_step": eager_ms,
+        "e2e": e2e,
+        "gpu_launches": gpu_launches,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": kernel_name,
+                     "achieved_basis": "algorithmic K/V bytes per launch / event-timed device time per step",
+                     "traffic_note": traffic_note},
+        "clocks": clocks,
+    }
+    if others:
+        line["workloads"] = others
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def attn_setup(name, args, dfl, dev, workloads, steps_hint=None):
+    """Inputs of a named attention workload with enough rotated page sets ("layers") to exceed
+    4x L2 between two visits, its workspace, and one captured CUDA graph per layer."""
+    probe = workloads.make_case(name, device=dev, layers=1)
     per_layer = kv_bytes_per_step(probe)
     layers = args.layers or max(2, math.ceil(4 * L2_BYTES / max(1, per_layer)))
     del probe
     torch.cuda.empty_cache()
-    case = workloads.make_case(args.config, device=dev, layers=layers)
+    case = workloads.make_case(name, device=dev, layers=layers)
     splits_req = case.num_splits if args.splits < 0 else args.splits
     dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
     splits = dfl.plan_splits(dims, case.block_len, case.window, splits_req, args.kernel)
@@ -1084,54 +1367,15 @@ def main():
         graphs.append(g)
     torch.cuda.synchronize()
     assert dfl.read_error(ws) == 0, "device-side check failed during warm-up"
+    plan = dfl.plan_info(dims, case.block_len, case.window, splits_req, args.kernel)
+    return dict(case=case, graphs=graphs, call=call, layers=layers, splits=splits, splits_req=splits_req,
+                ws=ws, out=out, lse=lse, plan=plan)
 
-    stream = torch.cuda.current_stream(dev)
-    for k in range(max(3, args.warmup)):
-        graphs[k % layers].replay()
-    torch.cuda.synchronize()
 
-    sampler = ClockSampler(dev.index if dev.index is not None else 0)
-    if rank == 0:
-        sampler.start()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    ev0.record(stream)
-    for k in range(args.steps):
-        graphs[k % layers].replay()
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    if dist:
-        dist.barrier()
-    ms_total = ev0.elapsed_time(ev1)
-    if rank == 0:
-        sampler.stop()
-    ms_total_t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-    if dist:
-        dist.all_reduce(ms_total_t, op=dist.ReduceOp.MAX)
-    ms_per_step = float(ms_total_t.item()) / args.steps
-    kv = kv_bytes_per_step(case)
-    value = world * kv / (ms_per_step * 1e-3) / 1e9
-    bq = world * case.batch / (ms_per_step * 1e-3)
-
-    # eager ctypes path, one call per step, for reference (not the headline)
-    torch.cuda.synchronize()
-    n_eager = min(args.steps, 2000)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for k in range(n_eager):
-        call(k % layers)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    eager_ms = e0.elapsed_time(e1) / n_eager
-
-    # end to end through the public API with host buffers: H2D q/page_table/seq_lens
-    # from pinned memory, the call, D2H of out and lse -- every step
+def e2e_measure(st, args, dfl, dev, stream, dist):
+    """End to end through the public API with host buffers: H2D of q / page_table / seq_lens from
+    pinned memory, the call, D2H of out and lse -- every step."""
+    case, layers, out, lse, ws = st["case"], st["layers"], st["out"], st["lse"], st["ws"]
     q_h = case.q.cpu().pin_memory()
     pts_h = [pt.cpu().pin_memory() for pt in case.page_tables]
     sl_h = case.seq_lens.cpu().pin_memory()
@@ -1147,7 +1391,7 @@ def main():
         pt_d.copy_(pts_h[k % layers], non_blocking=True)
         sl_d.copy_(sl_h, non_blocking=True)
         dfl.block_attn(q_d, case.k_cache, case.v_cache, pt_d, sl_d, case.block_len, causal=case.causal,
-                       window=case.window, scale=case.scale, out=out, lse=lse, num_splits=splits_req,
+                       window=case.window, scale=case.scale, out=out, lse=lse, num_splits=st["splits_req"],
                        kernel=args.kernel, workspace=ws)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
@@ -1155,6 +1399,8 @@ def main():
     for k in range(3):
         e2e_step(k)
     torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for k in range(n_e2e):
         e2e_step(k)
@@ -1165,94 +1411,43 @@ def main():
     if dist:
         dist.all_reduce(e2e_ms_t, op=dist.ReduceOp.MAX)
     e2e_ms = float(e2e_ms_t.item())
+    world = dist.get_world_size() if dist else 1
     h2d = q_h.numel() * q_h.element_size() + pts_h[0].numel() * 4 + sl_h.numel() * 4
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
-    assert dfl.read_error(ws) == 0, "device-side check failed"
-
-    tc = (args.kernel == "tc") or (args.kernel == "auto" and case.q.dtype == torch.bfloat16 and
-                                   _tc_used(dfl, dims, case, splits_req))
-    kernel_name = "tc_attn_kernel" if tc else "simt_attn_kernel"
-    # attention, plus the split combine unless the tensor-core kernel combines in-kernel
-    # (it does whenever its whole grid is resident: one CTA per SM)
-    launches_per_step = 1 if splits == 1 or (tc and _tc_ctas(case, splits, splits_req) <= _sm_count(dev)) else 2
-    peak, peak_kind = measured_peaks()
-    traffic, traffic_note = traffic_from_profiles(kernel_name)
-    achieved = kv / (ms_per_step * 1e-3) / 1e9
-
-    if rank != 0:
-        if dist:
-            dist.destroy_process_group()
-        return
-
-    clocks = sampler.summary(t_wall0, t_wall1)
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        t_step, n_rep, threads = time_oracle_full(case, args.cpu_budget)
-        cpu = {"value": kv / t_step / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{n_rep} full steps of layer 0 (all {case.q.shape[0] * case.q.shape[1]} rows, every "
-                         f"visible key), median {t_step * 1e3:.1f} ms per step"}
-    line = {
-        "metric": METRIC,
-        "value": value,
-        "unit": UNIT,
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": ms_per_step,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16" if case.q.dtype == torch.bfloat16 else "f32",
-        "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC if args.config == WORKLOAD else args.config,
-                   "global_batch": case.batch * world, "block_len": case.block_len,
-                   "seq_len": max(case.seq_lens_host()), "splits": splits, "kernel": kernel_name,
-                   "l2": f"inputs larger than L2: {layers} rotated page sets x {kv / 1e6:.1f} MB K/V",
-                   "timed_path": "one CUDA-graph replay of one dflash_block_attn call per step",
-                   "parallelism": f"replicas x{world}"},
-        "block_queries_per_s": bq,
-        "query_rows_per_s": bq * case.block_len * case.num_q_heads,
-        "eager_ms_per_step": eager_ms,
-        "e2e": {"value": world * kv / (e2e_ms * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "note": "public Python API, pinned host q/page_table/seq_lens in, out/lse back, every step; "
-                        "the KV cache is device-resident state"},
-        "gpu_launches": args.steps * launches_per_step,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": kernel_name,
-                     "achieved_basis": "algorithmic K/V bytes per launch / event-timed device time per step",
-                     "traffic_note": traffic_note},
-        "clocks": clocks,
-    }
-    if cpu:
-        line["cpu_baseline"] = cpu
-    print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    return {"value": world * kv_bytes_per_step(case) / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+            "note": "public Python API, pinned host q/page_table/seq_lens in, out/lse back, every step; "
+                    "the KV cache is device-resident state"}
 
 
-def _tc_ctas(case, splits, splits_req):
-    """CTAs of the tensor-core grid: chunk slots x KV heads x row groups, times the requests
-    unless the auto plan deals its slots over the requests by length (row groups: the largest
-    divisor of G whose G/rg query heads x T rows fit one 80-row tile)."""
-    G = case.num_q_heads // case.num_kv_heads
-    gc = max(d for d in range(1, G + 1) if G % d == 0 and d * case.block_len <= 80)
-    per = splits * case.num_kv_heads * (G // gc)
-    balanced = splits_req <= 0 and case.batch > 1 and splits >= case.batch
-    return per if balanced else per * case.batch
-
-
-def _sm_count(dev):
-    return torch.cuda.get_device_properties(dev).multi_processor_count
-
-
-def _tc_used(dfl, dims, case, splits_req):
-    try:
-        dfl.plan_splits(dims, case.block_len, case.window, max(0, splits_req), "tc")
-        return True
-    except dfl.DflashError:
-        return False
+def other_workload(name, args, dfl, dev, workloads, peak):
+    """Event-timed graph replays of another attention workload (its own split plan), for the
+    "workloads" key of the line: microseconds per call, K/V GB/s and the fraction of peak."""
+    sub = argparse.Namespace(**vars(args))
+    sub.splits = -1
+    st = attn_setup(name, sub, dfl, dev, workloads)
+    case, layers = st["case"], st["layers"]
+    kv = kv_bytes_per_step(case)
+    for k in range(10):
+        st["graphs"][k % layers].replay()
+    torch.cuda.synchronize()
+    n = max(200, min(5000, int(200e-3 / 40e-6)))
+    stream = torch.cuda.current_stream(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for k in range(n):
+        st["graphs"][k % layers].replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    assert dfl.read_error(st["ws"]) == 0, f"device-side check failed on {name}"
+    gbs = kv / (ms * 1e-3) / 1e9
+    rec = {"us_per_call": ms * 1e3, "kv_bytes": kv, "gbs": gbs, "frac": gbs / peak, "splits": st["splits"],
+           "kernel": st["plan"]["kernel_name"], "launches_per_call": st["plan"]["launches"], "replays": n,
+           "l2": f"{layers} rotated page sets"}
+    del st
+    return rec
 
 
 if __name__ == "__main__":

@@ -72,7 +72,7 @@ extern "C" {
 #define DFLASH_API
 #endif
 
-#define DFLASH_ABI_VERSION 1
+#define DFLASH_ABI_VERSION 2
 #define DFLASH_MAX_HEAD_DIM 512
 #define DFLASH_MAX_BLOCK_LEN 64
 #define DFLASH_MAX_SPLITS 256
@@ -91,14 +91,16 @@ typedef enum dflash_dtype {
     DFLASH_FP32 = 1  /* q, k_cache, v_cache, out in float32 */
 } dflash_dtype;
 
-/* Which kernel computes the attention. AUTO picks the single-CTA tensor-core
-   (tcgen05) kernel for bf16 where it covers the shape, else the SIMT kernel.
-   SIMT forces the CUDA-core kernel (any dtype). TC forces the single-CTA
-   tensor-core kernel and TC_PAIR the operand-split tensor-core kernel (a
-   2-CTA cluster: one CTA streams K and runs the softmax, the other streams V
-   and accumulates the output); both are bf16 only and return
-   DFLASH_ERR_UNSUPPORTED for shapes they do not cover (head_dim 128/256/512,
-   page size 16/32/64). All kernels compute the same definition. */
+/* Which kernel computes the attention. For bf16, AUTO packs each KV head's
+   query heads x block positions into tensor-core tiles: one CTA per tile
+   (TC, up to 80 rows) or, when that would split the rows into more groups
+   that each read all of the K/V (e.g. 8 heads x 16 positions at head_dim
+   512), a CTA pair sharing 2-SM MMAs (TC_PAIR, up to 128 rows, head_dim
+   256/512, uniform split plans). fp32, and shapes neither covers, run on the
+   CUDA-core kernel (SIMT). SIMT, TC and TC_PAIR force that kernel; TC and
+   TC_PAIR are bf16 only and return DFLASH_ERR_UNSUPPORTED for shapes they do
+   not cover (page size 16/32/64; TC: head_dim 128/256/512). All kernels
+   compute the same definition. */
 typedef enum dflash_kernel {
     DFLASH_KERNEL_AUTO = 0,
     DFLASH_KERNEL_SIMT = 1,
@@ -140,6 +142,10 @@ typedef struct dflash_opts {
                                its counters at zero between calls. */
     size_t workspace_bytes; /* size of workspace in bytes */
     void* stream;           /* cudaStream_t; NULL = legacy default stream */
+    uint32_t wait_limit_us; /* bound of every device-side wait of the tensor-core kernels
+                               (pipeline hand-offs and the in-kernel split combine's arrival
+                               wait), in microseconds; 0 = the default of 2 s. A wait that
+                               runs out sets DFLASH_DEVERR_TIMEOUT and the kernel returns. */
 } dflash_opts;
 
 /*
@@ -195,11 +201,30 @@ DFLASH_API dflash_status dflash_split_combine(const float* partial_out, const fl
 DFLASH_API int32_t dflash_plan_splits(const dflash_dims* dims, int32_t block_len, int32_t window,
                            int32_t requested, int32_t kernel);
 
+/* What a dflash_block_attn call with these sizes and options runs: the split
+   count, the kernel the selector resolves to, whether the splits are dealt to
+   the requests by length (partials sized for one request), the CTAs of the
+   attention launch and the number of kernel launches per call (the attention
+   kernel, plus the split combine unless the attention kernel combines in-kernel).
+   Assumes a workspace is passed. Host arithmetic plus cached device-attribute
+   and occupancy queries for the current device; no launch. */
+typedef struct dflash_plan {
+    int32_t num_splits; /* chunks per request, or chunk slots in all when balanced */
+    int32_t kernel;     /* dflash_kernel value actually run (never AUTO) */
+    int32_t balanced;   /* 1: length-balanced slots */
+    int32_t launches;   /* kernel launches per call */
+    int64_t ctas;       /* CTAs of the attention launch */
+} dflash_plan;
+DFLASH_API dflash_status dflash_plan_call(const dflash_dims* dims, int32_t block_len, int32_t window,
+                                          int32_t num_splits, int32_t kernel, dflash_plan* plan);
+
 /* Workspace bytes a call with these sizes and split count needs (split count
    as returned by dflash_plan_splits). Layout, each part 256-byte aligned: the
    error word (256 bytes), an 8 KB counter block (the arrival counters of the
    tensor-core kernel's in-kernel split combine; fixed size, zero between
-   calls, left non-zero only after a device timeout), then -- only when
+   calls; a call whose combine wait timed out resets its counters too, and
+   dflash_read_error clears the whole block when it reports
+   DFLASH_DEVERR_TIMEOUT), then -- only when
    splits > 1 --
    partial lse float32 [splits, B*T, Hq] and partial out float32
    [splits, B*T, Hq, D]. Returns 0 for invalid dims. */
@@ -207,8 +232,11 @@ DFLASH_API size_t dflash_workspace_bytes(const dflash_dims* dims, int32_t block_
 
 /* Copy the workspace error word to *device_error (device->host copy on
    `stream`, then a stream synchronisation; not for the hot path). With clear
-   != 0 the word is reset to zero afterwards. Returns DFLASH_ERR_DEVICE_CHECK
-   when the word is non-zero, DFLASH_OK when it is zero. */
+   != 0 the word is reset to zero afterwards. When the word carries
+   DFLASH_DEVERR_TIMEOUT the counter block is zeroed as well (whatever `clear`
+   says), so a workspace whose split combine gave up never feeds a later call
+   stale arrivals. Returns DFLASH_ERR_DEVICE_CHECK when the word is non-zero,
+   DFLASH_OK when it is zero. */
 DFLASH_API dflash_status dflash_read_error(const void* workspace, void* stream, uint32_t* device_error,
                                 int32_t clear);
 
@@ -220,9 +248,10 @@ DFLASH_API const char* dflash_last_error_message(void);
 
 /*
  * The pages have no counterpart of this entry point; it exists for callers
- * that cannot allocate device memory: code that runs while a CUDA graph is
- * being captured, inside a custom allocator, or in a runtime that owns all
- * device memory and forbids cudaMalloc. dflash_block_attn needs a caller-made
+ * that cannot allocate device memory: code that runs inside a custom
+ * allocator's own hooks (where calling back into the allocator would
+ * recurse), or in a runtime that owns all device memory and forbids
+ * cudaMalloc. dflash_block_attn needs a caller-made
  * workspace whenever it splits the keys; this variant keeps that scratch (the
  * error word, counters and split partials) in a fixed array of
  * DFLASH_NOALLOC_SCRATCH_BYTES bytes inside the library's device image,
@@ -242,7 +271,9 @@ DFLASH_API const char* dflash_last_error_message(void);
  * different host threads on the same device) race on it and must be ordered
  * by the caller. Device-side check bits land in the array's error word and are
  * not reported by this entry point (the checks still keep every access in
- * bounds).
+ * bounds: a bad page id is never dereferenced and its keys read as zero).
+ * The split plan may differ from dflash_block_attn's when the auto plan does
+ * not fit; the results then differ only by the fp32 summation order.
  */
 #define DFLASH_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 DFLASH_API dflash_status dflash_block_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,

@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     block_attn_noalloc,
     load_library,
     make_dims,
+    plan_info,
     plan_splits,
     read_error,
     split_combine,

@@ -33,6 +33,7 @@ EXPORTED = (
     "dflash_block_attn_noalloc",
     "dflash_split_combine",
     "dflash_plan_splits",
+    "dflash_plan_call",
     "dflash_workspace_bytes",
     "dflash_read_error",
     "dflash_status_string",
@@ -72,7 +73,21 @@ class Opts(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("stream", ctypes.c_void_p),
+        ("wait_limit_us", ctypes.c_uint32),
     ]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [
+        ("num_splits", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
+        ("balanced", ctypes.c_int32),
+        ("launches", ctypes.c_int32),
+        ("ctas", ctypes.c_int64),
+    ]
+
+
+KERNEL_NAMES = {1: "simt_attn_kernel", 2: "tc_attn_kernel", 3: "tc_pair_attn_kernel"}
 
 
 class DflashError(RuntimeError):
@@ -105,6 +120,8 @@ def load_library(path: Optional[str] = None):
         lib.dflash_split_combine.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp]
         lib.dflash_plan_splits.restype = i32
         lib.dflash_plan_splits.argtypes = [dims_p, i32, i32, i32, i32]
+        lib.dflash_plan_call.restype = ctypes.c_int
+        lib.dflash_plan_call.argtypes = [dims_p, i32, i32, i32, i32, ctypes.POINTER(Plan)]
         lib.dflash_workspace_bytes.restype = ctypes.c_size_t
         lib.dflash_workspace_bytes.argtypes = [dims_p, i32, i32]
         lib.dflash_read_error.restype = ctypes.c_int
@@ -178,11 +195,51 @@ def plan_splits(dims: Dims, block_len: int, window: int = 0, requested: int = 0,
     return n
 
 
+def plan_info(dims: Dims, block_len: int, window: int = 0, requested: int = 0, kernel: str = "auto") -> dict:
+    """What a call with these sizes runs (dflash_plan_call): split count, kernel, whether the
+    splits are length-balanced, CTAs of the attention launch and kernel launches per call."""
+    plan = Plan()
+    _check(load_library().dflash_plan_call(ctypes.byref(dims), int(block_len), int(window), int(requested),
+                                           KERNELS[kernel], ctypes.byref(plan)))
+    return {"num_splits": plan.num_splits, "kernel": plan.kernel, "kernel_name": KERNEL_NAMES[plan.kernel],
+            "balanced": bool(plan.balanced), "launches": plan.launches, "ctas": int(plan.ctas)}
+
+
 def workspace_bytes(dims: Dims, block_len: int, num_splits: int) -> int:
     n = load_library().dflash_workspace_bytes(ctypes.byref(dims), int(block_len), int(num_splits))
     if n == 0:
         raise DflashError(ERR_INVALID_ARG, "invalid dims for workspace size")
     return n
+
+
+def _check_attn_inputs(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
+                       seq_lens: torch.Tensor, block_len: int, out: Optional[torch.Tensor],
+                       lse: Optional[torch.Tensor]) -> None:
+    """Checks the library cannot make from the pointers and dims alone: the dims carry
+    k_cache's geometry only (the kernels and tensor maps read v_cache with it), and the
+    index tensors are read as int32. Shared by both attention entry points."""
+    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
+        raise ValueError("v_cache must match k_cache in shape and strides")
+    if v_cache.dtype != k_cache.dtype or q.dtype != k_cache.dtype:
+        raise TypeError("q, k_cache and v_cache must share one dtype")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous")
+    if page_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("page_table and seq_lens must be int32")
+    if page_table.dim() != 2 or not page_table.is_contiguous():
+        raise ValueError("page_table must be a contiguous [B, max_pages] tensor")
+    if seq_lens.dim() != 1 or seq_lens.shape[0] != page_table.shape[0] or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be a contiguous [B] tensor matching page_table's rows")
+    if q.dim() != 3 or q.shape[0] != page_table.shape[0] * int(block_len):
+        raise ValueError("q must be [B*block_len, Hq, D] with B = page_table.shape[0]")
+    if out is not None and (out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous tensor of q's shape and dtype")
+    if lse is not None and (tuple(lse.shape) != tuple(q.shape[:2]) or lse.dtype != torch.float32
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 [B*block_len, Hq] tensor")
+    devs = {t.device for t in (q, k_cache, v_cache, page_table, seq_lens, out, lse) if t is not None}
+    if len(devs) != 1 or next(iter(devs)).type != "cuda":
+        raise ValueError("every tensor must be on one CUDA device")
 
 
 _ws_cache = {}
@@ -211,20 +268,17 @@ def block_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pa
                scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                lse: Optional[torch.Tensor] = None, num_splits: int = 0, kernel: str = "auto",
                workspace: Optional[torch.Tensor] = None, max_seq_len: Optional[int] = None,
-               stream=None, want_lse: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+               stream=None, want_lse: bool = True,
+               wait_limit_us: int = 0) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """DFlash block attention (include/dflash_attn.h, dflash_block_attn).
 
     q [B*T, Hq, D]; k_cache, v_cache [num_pages, page_size, Hkv, D] (head_dim
     contiguous); page_table int32 [B, max_pages]; seq_lens int32 [B] on the
     device. Returns (out [B*T, Hq, D] in q's dtype, lse fp32 [B*T, Hq] or None).
+    wait_limit_us bounds every device-side wait of the tensor-core kernels (0 = 2 s).
     """
     lib = load_library()
-    if v_cache.shape != k_cache.shape or v_cache.stride() != k_cache.stride():
-        raise ValueError("v_cache must match k_cache in shape and strides")
-    if not q.is_contiguous():
-        raise ValueError("q must be contiguous")
-    if page_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
-        raise TypeError("page_table and seq_lens must be int32")
+    _check_attn_inputs(q, k_cache, v_cache, page_table, seq_lens, block_len, out, lse)
     dims = make_dims(q, k_cache, page_table, block_len, max_seq_len)
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[2])
@@ -242,6 +296,7 @@ def block_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, pa
     opts.workspace = workspace.data_ptr()
     opts.workspace_bytes = workspace.numel() * workspace.element_size()
     opts.stream = _stream_handle(stream)
+    opts.wait_limit_us = int(wait_limit_us)
     st = lib.dflash_block_attn(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), page_table.data_ptr(),
                                seq_lens.data_ptr(), ctypes.byref(dims), int(block_len), int(bool(causal)),
                                int(window), float(scale), out.data_ptr(),
@@ -254,18 +309,22 @@ def block_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
                        seq_lens: torch.Tensor, block_len: int, causal: bool = False, window: int = 0,
                        scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                        lse: Optional[torch.Tensor] = None, num_splits: int = 0, kernel: str = "auto",
-                       max_seq_len: Optional[int] = None, stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                       max_seq_len: Optional[int] = None, stream=None,
+                       want_lse: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """dflash_block_attn_noalloc: the same attention with the library's own fixed
     scratch instead of a workspace, for callers that cannot allocate device memory.
-    out/lse are allocated here only when not given."""
+    The library call allocates nothing; for convenience this wrapper allocates out
+    (and lse, when want_lse) with torch when they are not given, so a caller that
+    must not allocate passes both."""
     lib = load_library()
-    if not q.is_contiguous():
-        raise ValueError("q must be contiguous")
+    _check_attn_inputs(q, k_cache, v_cache, page_table, seq_lens, block_len, out, lse)
     dims = make_dims(q, k_cache, page_table, block_len, max_seq_len)
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[2])
     if out is None:
         out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device)
     st = lib.dflash_block_attn_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), page_table.data_ptr(),
                                        seq_lens.data_ptr(), ctypes.byref(dims), int(block_len), int(bool(causal)),
                                        int(window), float(scale), out.data_ptr(),

@@ -170,8 +170,12 @@ int choose_kernel(const dflash_dims* d, int32_t T, int32_t window, int32_t reque
         return DFLASH_KERNEL_TC_PAIR;
     }
     if (requested != DFLASH_KERNEL_AUTO) return -DFLASH_ERR_INVALID_ARG;
-    if (d->dtype == DFLASH_BF16 && tc_supports(p)) return DFLASH_KERNEL_TC;
-    if (d->dtype == DFLASH_BF16 && tc_pair_supports(p)) return DFLASH_KERNEL_TC_PAIR;
+    if (d->dtype != DFLASH_BF16) return DFLASH_KERNEL_SIMT;
+    // The packed rows of a KV head's query heads x block positions go to one CTA per tile
+    // (several row groups when they do not fit one); the CTA pair takes shapes the single-CTA
+    // kernel does not cover.
+    if (tc_supports(p)) return DFLASH_KERNEL_TC;
+    if (tc_pair_supports(p)) return DFLASH_KERNEL_TC_PAIR;
     return DFLASH_KERNEL_SIMT;
 }
 
@@ -293,6 +297,49 @@ int32_t dflash_plan_splits(const dflash_dims* dims, int32_t block_len, int32_t w
     return plan_splits_impl(dims, block_len, window, requested, k);
 }
 
+dflash_status dflash_plan_call(const dflash_dims* dims, int32_t block_len, int32_t window, int32_t num_splits,
+                               int32_t kernel, dflash_plan* plan)
+{
+    g_last_error.clear();
+    if (!plan) return fail(DFLASH_ERR_INVALID_ARG, "plan is NULL");
+    const dflash_status s = check_dims(dims, block_len);
+    if (s != DFLASH_OK) return s;
+    const int k = choose_kernel(dims, block_len, window, kernel);
+    if (k < 0) return fail((dflash_status)(-k), "the requested kernel does not cover these sizes/dtype");
+    const int32_t splits = plan_splits_impl(dims, block_len, window, num_splits, k);
+    if (splits < 1) return fail(DFLASH_ERR_INVALID_ARG, "num_splits %d outside [0, %d]", num_splits, DFLASH_MAX_SPLITS);
+    const bool balanced = num_splits == 0 && splits > 1 && balanced_slots(dims, block_len, window, k) == splits;
+    plan->num_splits = splits;
+    plan->kernel = k;
+    plan->balanced = balanced ? 1 : 0;
+    AttnParams p{};
+    p.B = dims->batch;
+    p.T = block_len;
+    p.Hq = dims->num_q_heads;
+    p.Hkv = dims->num_kv_heads;
+    p.G = dims->num_q_heads / dims->num_kv_heads;
+    p.D = dims->head_dim;
+    p.page_size = dims->page_size;
+    p.window = window;
+    p.dtype = dims->dtype;
+    p.sp = dims->kv_stride_page;
+    p.ss = dims->kv_stride_slot;
+    p.sh = dims->kv_stride_head;
+    p.num_pages = dims->num_pages;
+    p.splits = splits;
+    p.balanced = plan->balanced;
+    if (k == DFLASH_KERNEL_TC) {
+        bool fused = false;
+        const cudaError_t e = tc_grid_info(p, &plan->ctas, &fused);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core grid query");
+        plan->launches = (splits == 1 || fused) ? 1 : 2;
+    } else {
+        plan->ctas = work_units(dims, block_len, k) * splits;
+        plan->launches = splits == 1 ? 1 : 2;
+    }
+    return DFLASH_OK;
+}
+
 size_t dflash_workspace_bytes(const dflash_dims* dims, int32_t block_len, int32_t num_splits)
 {
     if (check_dims(dims, block_len) != DFLASH_OK || num_splits < 1 || num_splits > DFLASH_MAX_SPLITS) return 0;
@@ -396,6 +443,8 @@ dflash_status dflash::block_attn_planned(const void* q, const void* k_cache, con
     p.splits = splits;
     p.dtype = dims->dtype;
     p.balanced = balanced ? 1 : 0;
+    p.wait_ns = (opts && opts->wait_limit_us) ? (unsigned long long)opts->wait_limit_us * 1000ull
+                                              : DFLASH_DEFAULT_WAIT_NS;
 
     cudaStream_t stream = opts ? static_cast<cudaStream_t>(opts->stream) : nullptr;
     cudaError_t e = (kernel == DFLASH_KERNEL_TC)        ? launch_tc_attn(p, stream)
@@ -605,6 +654,14 @@ dflash_status dflash_read_error(const void* workspace, void* stream, uint32_t* d
         e = cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(word), st);
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+    }
+    if (word & DFLASH_DEVERR_TIMEOUT) {
+        // a split combine that gave up may have left arrivals behind: start the counters afresh
+        const WorkspaceLayout wl = workspace_layout(1, 1, 1, 16, 1);
+        e = cudaMemsetAsync(static_cast<char*>(const_cast<void*>(workspace)) + wl.counters_off, 0,
+                            DFLASH_COUNTER_BYTES, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the counter block");
     }
     *device_error = word;
     return word ? DFLASH_ERR_DEVICE_CHECK : DFLASH_OK;

@@ -33,7 +33,11 @@ struct AttnParams {
     int32_t dtype;        // dflash_dtype
     int32_t balanced;     // 1: the tensor-core kernel deals its `splits` slots to the requests in
                           // proportion to their key spans (partials laid out [slot][T][Hq][D])
+    unsigned long long wait_ns;  // bound of every device-side wait (pipeline and combine)
 };
+
+// Default bound of a device-side wait (dflash_opts.wait_limit_us == 0).
+constexpr unsigned long long DFLASH_DEFAULT_WAIT_NS = 2000000000ull;
 
 // Workspace carve-up (offsets in bytes from the workspace base). The counter block has a
 // fixed size, so a workspace zeroed once stays valid for calls of any size: two int32
@@ -95,10 +99,17 @@ cudaError_t launch_combine(const float* part_out, const float* part_lse, int32_t
 bool tc_supports(const AttnParams& p);
 int tc_ctas_per_split(const AttnParams& p);  // CTAs per split chunk (B * Hkv * row groups)
 cudaError_t launch_tc_attn(const AttnParams& p, cudaStream_t stream);
+// Grid of a launch_tc_attn call and whether it combines the splits in-kernel (the whole grid
+// resident: a cooperative launch). Assumes a workspace (counters) is given.
+cudaError_t tc_grid_info(const AttnParams& p, int64_t* ctas, bool* fused);
 
-// Operand-split tensor-core kernel (2-CTA cluster: one CTA streams K, the other V).
+int tc_row_groups(const AttnParams& p);       // CTAs per (request, KV head, chunk)
+
+// CTA-pair tensor-core kernel (tcgen05 cta_group::2 over a 2-CTA cluster; up to 128 packed rows
+// at head_dim 256/512, every K/V byte read by one SM). Uniform split plans only.
 bool tc_pair_supports(const AttnParams& p);
 int tc_pair_ctas_per_split(const AttnParams& p);  // CTAs per split chunk (2 * B * Hkv * row groups)
+int tc_pair_row_groups(const AttnParams& p);      // pairs per (request, KV head, chunk)
 cudaError_t launch_tc_pair_attn(const AttnParams& p, cudaStream_t stream);
 
 // SM count of the current device (cached per device).

@@ -1,9 +1,10 @@
 // dflash_block_attn_noalloc: block attention for callers that cannot allocate
-// device memory (for example code running inside a CUDA-graph capture region,
-// a custom allocator's critical section, or an embedding runtime that owns all
-// device memory and forbids cudaMalloc). The split-KV partials and the error
-// word normally live in a caller-provided workspace; here they live in a
-// fixed-size scratch array that is part of this library's device image.
+// device memory (for example code running inside a custom allocator's own
+// hooks, where calling back into the allocator would recurse, or an embedding
+// runtime that owns all device memory and forbids cudaMalloc). The split-KV
+// partials and the error word normally live in a caller-provided workspace;
+// here they live in a fixed-size scratch array that is part of this library's
+// device image.
 #include <mutex>
 
 #include "dflash_internal.h"

@@ -58,9 +58,10 @@
 // freed Q / P / ring shared memory by eight warps and written with bulk
 // asynchronous copies, one per block position (its Gc head rows are contiguous).
 //
-// Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the kernel
-// records DFLASH_DEVERR_TIMEOUT, drains its own TMA copies and MMAs (bounded),
-// frees TMEM and returns.
+// Every mbarrier wait is bounded (p.wait_ns of %globaltimer, 2 s unless the
+// caller sets dflash_opts.wait_limit_us); on expiry the kernel records
+// DFLASH_DEVERR_TIMEOUT, drains its own TMA copies and MMAs (bounded), frees
+// TMEM and returns.
 #include <cuda.h>
 
 #include <cmath>
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const RingSlot sl = ring_slot(seq, S, E);
                         uint64_t* fb = sl.extra ? xfull + sl.idx : full + sl.idx;
                         if (!sl.extra) {
-                            if (lane == 0) ok = ring_wait(empty + sl.idx, sl.phase ^ 1u, abort_flag, p.err);
+                            if (lane == 0) ok = ring_wait(empty + sl.idx, sl.phase ^ 1u, abort_flag, p.err, p.wait_ns);
                             ok = __shfl_sync(0xffffffffu, ok, 0);
                             if (!ok) break;
                         }
@@ -482,13 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < S; ++s) {
                 if (issued_parity[s] > 1) continue;
                 const unsigned long long t_start = globaltimer();
-                while (!mbar_try_wait(full + s, issued_parity[s]) && globaltimer() - t_start < kTimeoutNs) {
+                while (!mbar_try_wait(full + s, issued_parity[s]) && globaltimer() - t_start < p.wait_ns) {
                 }
             }
             for (int e = 0; e < E; ++e) {
                 if (!(issued_extra & (1u << e))) continue;
                 const unsigned long long t_start = globaltimer();
-                while (!mbar_try_wait(xfull + e, 0) && globaltimer() - t_start < kTimeoutNs) {
+                while (!mbar_try_wait(xfull + e, 0) && globaltimer() - t_start < p.wait_ns) {
                 }
             }
         }
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         auto wait_lane0 = [&](uint64_t* bar, uint32_t par) -> bool {
             bool got = true;
-            if (lane == 0) got = ring_wait(bar, par, abort_flag, p.err);
+            if (lane == 0) got = ring_wait(bar, par, abort_flag, p.err, p.wait_ns);
             return __shfl_sync(0xffffffffu, got, 0);
         };
         // wait for the next stage; its shared address (and whether it is an extra slot)
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tc_commit(drain);
             const unsigned long long t_start = globaltimer();
-            while (!mbar_try_wait(drain, 0) && globaltimer() - t_start < kTimeoutNs) {
+            while (!mbar_try_wait(drain, 0) && globaltimer() - t_start < p.wait_ns) {
             }
         }
         __syncwarp();
@@ -629,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // uniform across the 128 softmax threads (so none is left at a barrier).
         auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool got = true;
-            if (tid == 0) got = ring_wait(bar, parity, abort_flag, p.err);
+            if (tid == 0) got = ring_wait(bar, parity, abort_flag, p.err, p.wait_ns);
             return !named_bar_or_128(!got);
         };
 
@@ -869,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicAdd(cnt, 1);
                 const unsigned long long t_start = globaltimer();
                 while (ld_acquire_gpu(cnt) < n_split) {
-                    if (globaltimer() - t_start > kTimeoutNs) {
+                    if (globaltimer() - t_start > p.wait_ns) {
                         raise_error(p.err, DFLASH_DEVERR_TIMEOUT);
                         arrived = false;
                         break;
@@ -948,10 +949,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             named_bar_sync_256();
-            if (tid == 0 && arrived) {
+            if (tid == 0) {
+                // A CTA whose arrival wait ran out still counts itself here, so a group whose
+                // counters held stale arrivals (every CTA times out) is reset like any other.
                 __threadfence();
                 if (atomicAdd(cnt + 1, 1) == n_split - 1) {
-                    // every CTA of the group has passed the arrival wait and read its slice
+                    // every CTA of the group has passed (or given up) the arrival wait and read its slice
                     atomicExch(cnt, 0);
                     atomicExch(cnt + 1, 0);
                 }
@@ -1041,6 +1044,39 @@ cudaError_t launch_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     return e;
 }
 
+// Grid size and whether launch_dn would combine in-kernel (same rule, no launch).
+template <int D, int N>
+cudaError_t grid_info_dn(const AttnParams& p, const TcExtra& x, int64_t* ctas, bool* fused)
+{
+    using Lay = TcLayout<D, N>;
+    auto kern = tc_attn_kernel<D, N>;
+    const int64_t gx = p.splits, gy = (int64_t)p.Hkv * x.n_rg, gz = p.balanced ? 1 : p.B;
+    *ctas = gx * gy * gz;
+    *fused = false;
+    if (p.splits > 1) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, Lay::kAlloc);
+        if (e != cudaSuccess) return e;
+        *fused = *ctas <= (int64_t)per_sm * device_sm_count() && gy * gz <= DFLASH_MAX_COMBINE_GROUPS;
+    }
+    return cudaSuccess;
+}
+
+template <int D>
+cudaError_t grid_info_d(int n, const AttnParams& p, const TcExtra& x, int64_t* ctas, bool* fused)
+{
+    switch (n) {
+    case 16: return grid_info_dn<D, 16>(p, x, ctas, fused);
+    case 32: return grid_info_dn<D, 32>(p, x, ctas, fused);
+    case 48: return grid_info_dn<D, 48>(p, x, ctas, fused);
+    case 64: return grid_info_dn<D, 64>(p, x, ctas, fused);
+    case 80: return grid_info_dn<D, 80>(p, x, ctas, fused);
+    }
+    return cudaErrorNotSupported;
+}
+
 template <int D>
 cudaError_t launch_d(int n, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                      const TcExtra& x, cudaStream_t stream, bool* combined)
@@ -1067,10 +1103,33 @@ bool tc_supports(const AttnParams& p)
     return true;  // the tensor-map encoder is resolved from the driver at launch
 }
 
+int tc_row_groups(const AttnParams& p)
+{
+    const int gc = choose_gc(p.G, p.T);
+    return gc > 0 ? p.G / gc : 0;
+}
+
 int tc_ctas_per_split(const AttnParams& p)
 {
     const int gc = choose_gc(p.G, p.T);
     return gc > 0 ? p.B * p.Hkv * (p.G / gc) : 0;
+}
+
+cudaError_t tc_grid_info(const AttnParams& p, int64_t* ctas, bool* fused)
+{
+    if (!tc_supports(p)) return cudaErrorNotSupported;
+    TcExtra x;
+    x.fused = 0;
+    x.Gc = choose_gc(p.G, p.T);
+    x.n_rg = p.G / x.Gc;
+    x.R = x.Gc * p.T;
+    const int n = ((x.R + 15) / 16) * 16;
+    switch (p.D) {
+    case 128: return grid_info_d<128>(n, p, x, ctas, fused);
+    case 256: return grid_info_d<256>(n, p, x, ctas, fused);
+    case 512: return grid_info_d<512>(n, p, x, ctas, fused);
+    }
+    return cudaErrorNotSupported;
 }
 
 cudaError_t launch_tc_attn(const AttnParams& p, cudaStream_t stream)

@@ -1,27 +1,46 @@
-// Tensor-core block attention for bf16 on sm_103a, operand-split CTA pair.
+// Tensor-core block attention for bf16 on sm_103a, CTA-pair form (tcgen05 cta_group::2).
 //
-// Same mathematics as tc_attn.cu (transposed S^T = K.Q^T, O^T += V^T.P^T,
-// row sums l += 1.P^T on tcgen05 with TMEM accumulators; see that file). What
-// differs is the schedule. With head_dim 512 a 128-key tile is 256 KB of K and
-// V, more than the shared-memory ring of one CTA, and V(j) cannot be consumed
-// before the softmax of tile j has produced P: a single CTA's ring then sits
-// full of V(j) while the softmax runs, and HBM idles.
+// Same mathematics as tc_attn.cu (transposed S^T = K.Q^T and O^T += V^T.P^T on the tensor
+// cores, TMEM accumulators, lazily rescaled running maxima). This
+// form serves blocks whose packed rows do not fit one CTA. DFlash2 drafts 15 tokens by default
+// (prhub report on vLLM PR #52816 "DFlash2", risks), so a request's block is T = 16 queries
+// ("num_query_per_req = 1 + num_speculative_tokens", kenforever1 "dflash-gemma4-31b-notes"),
+// and the 8 query heads of a KV head at head_dim 512 make 128 rows. Their fp32 O^T alone is
+// 128 x 512 x 4 B = all of one SM's TMEM, so one CTA cannot hold it; two CTAs that each took
+// half of the heads would each read every K/V byte.
 //
-// Here a 2-CTA cluster shares one (request, KV head, row group, key chunk):
-//   K-CTA (rank 0): streams only K, computes S^T into a double-buffered TMEM
-//     region (QK of tile j+1 overlaps the softmax of tile j), runs the softmax
-//     and ships each tile's P^T (bf16, in the MMA's shared-memory layout) with
-//     the running row max and, when the max moved, the rescale factors, to the
-//     V-CTA with one shared-to-shared bulk copy completing on the V-CTA's
-//     mbarrier;
-//   V-CTA (rank 1): streams only V through a deep ring (no Q to hold),
-//     accumulates O^T and l, rescales them when told, and writes the output.
-// Each SM streams one operand continuously. Flow control: the V-CTA's PV
-// commit is multicast to the K-CTA's "message free" barrier of that buffer.
+// Here two CTAs of a cluster share one (request, KV head, key chunk) and every K/V byte
+// enters exactly one SM. A "pair tile" is 256 keys. The even CTA issues 2-SM MMAs:
+//   S^T [256 keys x 128 rows]  = K [256 x D] . Q^T          A = K: each CTA streams its own
+//                                                            128 keys; B = Q^T: each CTA holds
+//                                                            its 64 rows of Q
+//   O^T [256 dims x 128 rows] += V^T [256 x 256 keys] . P^T  per 256-dim output chunk: each CTA
+//                                                            streams V of all 256 keys for its
+//                                                            128 dims; B = P^T: each CTA holds
+//                                                            the P of its 64 rows
+// so CTA r's TMEM holds two S^T buffers of its 128 keys for all rows (S of tile j+1 is computed
+// while the softmax of tile j runs) and O^T of its 128 dims of every chunk for all rows:
+// 2*128 + (D/256)*128 = 512 columns at D = 512. The row sums l do not fit TMEM as well, so
+// the softmax forms them on the CUDA cores from the same bf16-rounded P the MMA reads (a
+// transposing shuffle reduction per 16 columns), each CTA over its own keys; the two partial
+// sums are added once at the end.
 //
-// Warps (288 threads) per CTA: 0-3 softmax (K-CTA) or rescale + epilogue
-// (V-CTA), 4-7 TMA producers (ring stages dealt round-robin), 8 MMA issuer.
-// Every wait is bounded (2 s of %globaltimer) and reports DFLASH_DEVERR_TIMEOUT.
+// Per pair tile each CTA's softmax (thread = key lane) turns its 128 keys x 128 rows into P.
+// The row maxima must agree across the pair: each CTA sends its 128 column maxima to the
+// other with asynchronous stores that count their bytes on the receiver's mbarrier, and both
+// take the same lazy update. Each CTA writes the P of rows 0-63 into the even CTA's P^T
+// buffer and of rows 64-127 into the odd CTA's (one half local, one half remote).
+//
+// Roles (416 threads): warps 0-7 softmax (warps w and w+4 share TMEM lanes 32(w%4).., and take
+// the rows 0-63 and 64-127), then the epilogue; warps 8-11 TMA producers (whole 16 KB ring
+// stages dealt round-robin); warp 12 the MMA issuer in the even CTA, and in the odd CTA the
+// forwarder that tells the even CTA when each of its own stages has landed. Both CTAs fill
+// their rings in the same order K(0) K(1) V(0) K(2) V(1) ... so a stage sits at the same
+// offset in both, as the pair MMA needs.
+//
+// Every wait is bounded (p.wait_ns); on expiry the kernel records DFLASH_DEVERR_TIMEOUT,
+// drains its own copies and MMAs, and both CTAs still meet at the final cluster barrier
+// before TMEM is freed, so neither exits while the other may still touch its memory.
 #include <cuda.h>
 
 #include <cmath>
@@ -35,125 +54,191 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 288;
-constexpr int kProducerWarp = 4;
+constexpr int kThreads = 416;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kProducerWarp = 8;
 constexpr int kNumProducers = 4;
-constexpr int kMmaWarp = 8;
-constexpr int kTileKeys = 128;
+constexpr int kMmaWarp = 12;
+constexpr int kPairKeys = 256;  // keys per pair tile
+constexpr int kOwnKeys = 128;   // keys of a pair tile whose K this CTA streams
+constexpr int kHalf = 64;       // Q / P rows held per CTA
+constexpr int kN = 128;         // columns (packed rows) of S^T and O^T
 constexpr int kStageBytes = 16384;
 constexpr int kMaxPids = 128;
-constexpr int kMaxRows = 80;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;
-constexpr int kOnesBytes = 4096;
-constexpr int kSmemCap = 227 * 1024;
 
 struct PairExtra {
     int32_t Gc;    // query heads per pair
-    int32_t n_rg;  // row groups per KV head
-    int32_t R;     // packed rows (Gc * T)
+    int32_t n_rg;  // row groups per KV head (G / Gc)
+    int32_t Tb;    // block positions per CTA (ceil(T / 2)); CTA r holds positions [r*Tb, r*Tb + Tb)
 };
 
-constexpr int pow2ceil32(int x)
+__host__ __device__ constexpr int pair_pow2ceil(int x)
 {
     int p = 32;
     while (p < x) p <<= 1;
     return p;
 }
 
-constexpr int round_up_c(int x, int a) { return (x + a - 1) / a * a; }
-
-// Cluster-visible barriers sit at the same offsets in both CTAs: [0..1] msg_full
-// (in the V-CTA: P^T of the buffer has landed), [2..3] msg_free (in the K-CTA:
-// the V-CTA has finished with the buffer).
-template <int D, int N>
+template <int D>
 struct PairLayout {
-    // message: P^T [2 key halves][N rows][128 B], alpha[N], m[N], flag word
-    static constexpr int kMsgBytes = N * 256 + 8 * N + 16;
-    static constexpr int kMsgStride = round_up_c(kMsgBytes, 1024);
-    static constexpr int kClusterBars = 0;   // 4 x uint64
-    static constexpr int kBase = 1024;       // rank-specific layout starts here
-
-    // ---- K-CTA
-    static constexpr int kKQ = kBase;                                  // [D/64][N][128 B]
-    static constexpr int kKStage = kKQ + N * D * 2;                    // 2 x message staging
-    static constexpr int kKTable = kKStage + 2 * kMsgStride;           // m, alpha, red[4], lo, hi
-    static constexpr int kKPid = kKTable + 8 * N * 4;                  // 4 x kMaxPids int
-    static constexpr int kKBars = kKPid + 4 * kMaxPids * 4;            // local barriers
-    static constexpr int kKMisc = kKBars + 64 * 8;                     // tmem slot, abort, flags
-    static constexpr int kKRing = round_up_c(kKMisc + 64, 1024);
-    static constexpr int kKStagesFit = (kSmemCap - 1024 - kKRing) / kStageBytes;
-    static constexpr int kKStages = kKStagesFit > 12 ? 12 : kKStagesFit;
-    static constexpr int kKTotal = kKRing + kKStages * kStageBytes;
-    static constexpr int kKTmemCols = pow2ceil32(2 * N);
-
-    // ---- V-CTA
-    static constexpr int kVMsg = kBase;                                // 2 x message
-    static constexpr int kVOnes = kVMsg + 2 * kMsgStride;
-    static constexpr int kVRow = kVOnes + kOnesBytes;                  // int64 orow[N]
-    static constexpr int kVPid = kVRow + N * 8;
-    static constexpr int kVBars = kVPid + 4 * kMaxPids * 4;
-    static constexpr int kVMisc = kVBars + 64 * 8;
-    static constexpr int kVRing = round_up_c(kVMisc + 64, 1024);
-    static constexpr int kVStagesFit = (kSmemCap - 1024 - kVRing) / kStageBytes;
-    static constexpr int kVStages = kVStagesFit > 12 ? 12 : kVStagesFit;
-    static constexpr int kVTotal = kVRing + kVStages * kStageBytes;
-    static constexpr int kVTmemCols = pow2ceil32(N * (1 + D / 128));
-
-    static constexpr int kAlloc = (kKTotal > kVTotal ? kKTotal : kVTotal) + 1024;
-    static_assert(kKStages >= 3 && kVStages >= 3, "ring too shallow");
-    static_assert(kAlloc <= kSmemCap, "shared memory budget");
-    static_assert(N * (1 + D / 128) <= 512, "TMEM budget");
-    static_assert(kMsgBytes % 16 == 0, "bulk copy size");
+    static constexpr int KC = D / 64;       // K stages per pair tile (64 dims each, own 128 keys)
+    static constexpr int VC2 = D / 256;     // output chunks of 256 dims (128 per CTA)
+    static constexpr int kQBytes = KC * kHalf * 128;
+    static constexpr int kPQuarter = kHalf * 128;           // P^T of 64 keys x 64 rows
+    static constexpr int kPBuf = 4 * kPQuarter;             // one pair tile
+    static constexpr int kQOff = 0;
+    static constexpr int kPOff = kQOff + kQBytes;           // [2 buffers][4 quarters][4 atoms][2 KB]
+    static constexpr int kRingOff = kPOff + 2 * kPBuf;
+    static constexpr int kSmallBytes = 12288;               // barriers, tables
+    static constexpr int kStagesFit = (227 * 1024 - 1024 - kRingOff - kSmallBytes) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
+    static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
+    // barriers: full[S] empty[S] pfull[S] s_full[2] p_full p_free[2] px_full[2] lx_full drain
+    static constexpr int kNumBars = 3 * kStages + 9;
+    static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;  // tmem base, abort flag
+    static constexpr int kMOff = kMiscOff + 16;             // float m_s[128]
+    static constexpr int kAOff = kMOff + kN * 4;            // float a_s[128] (1/l at the end)
+    static constexpr int kRedOff = kAOff + kN * 4;          // float red[8 warps][64]: column maxima
+    static constexpr int kSumOff = kRedOff + 8 * 64 * 4;    // float red2[8 warps][64]: column sums of P
+    static constexpr int kLaccOff = kSumOff + 8 * 64 * 4;   // float l_acc[128]: this CTA's keys' row sums
+    static constexpr int kPxOff = kLaccOff + kN * 4;        // float px[2][128]: the peer's maxima
+    static constexpr int kLxOff = kPxOff + 2 * kN * 4;      // float lx[128]: the peer's row sums
+    static constexpr int kLoOff = kLxOff + kN * 4;          // int lo_s[128]
+    static constexpr int kHiOff = kLoOff + kN * 4;          // int hi_s[128]
+    static constexpr int kRowOff = kHiOff + kN * 4;         // int64 orow_s[128]
+    static constexpr int kPidOff = kRowOff + kN * 8;        // int pid_s[4][kMaxPids]
+    static constexpr int kTotal = kPidOff + kNumProducers * kMaxPids * 4;
+    static constexpr int kAlloc = kTotal + 1024;
+    static constexpr int kTmemUsed = 2 * kN + VC2 * kN;     // S^T x 2, O^T chunks
+    static constexpr int kTmemCols = pair_pow2ceil(kTmemUsed);
+    static_assert(kStages >= 4, "ring too shallow");
+    static_assert(kTotal - kBarOff <= kSmallBytes, "small tables");
+    static_assert(kTotal + 1024 <= 227 * 1024, "shared memory budget");
+    static_assert(kTmemUsed <= 512, "TMEM budget");
 };
 
-template <int D, int N>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const AttnParams p, const PairExtra x)
+// The k-th unit (0 <= k < 2n) of the ring sequence K(0) K(1) V(0) K(2) V(1) ... V(n-1).
+__device__ __forceinline__ void pair_ring_unit(int k, int n, bool& is_k, int& tile)
 {
-    using Lay = PairLayout<D, N>;
-    constexpr int KC = D / 64;   // K stages per tile
-    constexpr int VC = D / 128;  // O^T chunks; V stages per 64-key half
-    constexpr int NQ = N / 16;
+    if (k == 0) {
+        is_k = true;
+        tile = 0;
+    } else if (k & 1) {
+        const int m = (k + 1) >> 1;
+        is_k = m < n;
+        tile = is_k ? m : n - 1;
+    } else {
+        is_k = false;
+        tile = (k - 2) >> 1;
+    }
+}
+
+// Column reductions over a warp: v holds 16 consecutive columns of this lane's key. Each step
+// swaps half of the live columns with the partner lane and keeps the combination of the half
+// it owns; after four steps lane l holds its 16-lane half's result for column l mod 16, and one
+// exchange across the halves completes it (16 shuffles for 16 columns).
+__device__ __forceinline__ float pair_transpose_max16(float (&v)[16], int lane)
+{
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+        }
+    }
+    return fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 16));
+}
+
+__device__ __forceinline__ float pair_transpose_sum16(float (&v)[16], int lane)
+{
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
+}
+
+// Named barrier 1 over the 256 softmax threads (warps 0-7), with an OR of a predicate.
+__device__ __forceinline__ bool bar_or_256(bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 256, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void bar_sync_256() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_pair_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p, const PairExtra x)
+{
+    using Lay = PairLayout<D>;
+    constexpr int S = Lay::kStages;
+    constexpr int KC = Lay::KC;
+    constexpr int VC2 = Lay::VC2;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t rank = cluster_ctarank();
-    const bool is_k = (rank == 0);
-    uint64_t* cbars = reinterpret_cast<uint64_t*>(smem + Lay::kClusterBars);
-    uint64_t* msg_full = cbars;      // [2], used in the V-CTA
-    uint64_t* msg_free = cbars + 2;  // [2], used in the K-CTA
+    uint8_t* q_s = smem + Lay::kQOff;
+    uint8_t* ring = smem + Lay::kRingOff;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+    uint64_t* full = bars;            // [S] own TMA landed
+    uint64_t* empty = bars + S;       // [S] the pair MMAs reading the slot are done (both CTAs)
+    uint64_t* pfull = bars + 2 * S;   // [S] even CTA only: the odd CTA's stage has landed
+    uint64_t* s_full = bars + 3 * S;  // [2] S^T of tile j is in TMEM buffer j mod 2 (both CTAs)
+    uint64_t* p_full = s_full + 2;    // even CTA: both CTAs wrote P (16 warp arrivals)
+    uint64_t* p_free = s_full + 3;    // [2] PV of the tile done: P^T buffer free, O^T final for it
+    uint64_t* px_full = s_full + 5;   // [2] the peer's 128 column maxima have landed (512 bytes)
+    uint64_t* lx_full = s_full + 7;   // the peer's 128 row sums have landed (512 bytes)
+    uint64_t* drain = s_full + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
+    float* m_s = reinterpret_cast<float*>(smem + Lay::kMOff);
+    float* a_s = reinterpret_cast<float*>(smem + Lay::kAOff);
+    float* red = reinterpret_cast<float*>(smem + Lay::kRedOff);
+    float* red2 = reinterpret_cast<float*>(smem + Lay::kSumOff);
+    float* l_acc = reinterpret_cast<float*>(smem + Lay::kLaccOff);
+    float* px = reinterpret_cast<float*>(smem + Lay::kPxOff);
+    float* lx = reinterpret_cast<float*>(smem + Lay::kLxOff);
+    int32_t* lo_s = reinterpret_cast<int32_t*>(smem + Lay::kLoOff);
+    int32_t* hi_s = reinterpret_cast<int32_t*>(smem + Lay::kHiOff);
+    int64_t* orow_s = reinterpret_cast<int64_t*>(smem + Lay::kRowOff);
+    int32_t* pid_s = reinterpret_cast<int32_t*>(smem + Lay::kPidOff);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const bool leader = (rank == 0);
     const int c_split = blockIdx.x >> 1;
+    const int b = blockIdx.z;
     const int g = blockIdx.y / x.n_rg;
     const int rg = blockIdx.y % x.n_rg;
-    const int b = blockIdx.z;
     const int T = p.T;
     const int Psz = p.page_size;
-    const int R = x.R;
     const int h0 = g * p.G + rg * x.Gc;
-
-    const int S = is_k ? Lay::kKStages : Lay::kVStages;
-    uint8_t* ring = smem + (is_k ? Lay::kKRing : Lay::kVRing);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (is_k ? Lay::kKBars : Lay::kVBars));
-    uint64_t* full = bars;            // [S]
-    uint64_t* empty = bars + 12;      // [S]
-    uint64_t* q_full = bars + 24;     // K-CTA
-    uint64_t* s_full = bars + 25;     // [2] K-CTA
-    uint64_t* s_free = bars + 27;     // [2] K-CTA (count 128)
-    uint64_t* drain = bars + 29;
-    uint64_t* rq = bars + 30;         // V-CTA: MMA -> rescale warps (count 1)
-    uint64_t* rd = bars + 31;         // V-CTA: rescale warps -> MMA (count 128)
-    uint8_t* misc = smem + (is_k ? Lay::kKMisc : Lay::kVMisc);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
-    volatile int* rq_cmd = reinterpret_cast<volatile int*>(misc + 8);  // V-CTA: buffer to rescale, -1 = finish
-    int32_t* pid_s = reinterpret_cast<int32_t*>(smem + (is_k ? Lay::kKPid : Lay::kVPid));
+    const int rows_mine = x.Gc * x.Tb;  // Q rows this CTA loads (of its kHalf)
 
     const int32_t L = __ldg(p.seq_lens + b);
     const bool len_ok = seq_len_ok(p, L);
@@ -162,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ch.ke = 0;
     if (len_ok) ch = split_chunk(L, T, p.window, Psz, p.splits, c_split);
     const int t0 = (ch.kb / Psz) * Psz;
-    const int ntiles = (ch.kb < ch.ke) ? (ch.ke - t0 + kTileKeys - 1) / kTileKeys : 0;
-    const int pages_per_tile = kTileKeys / Psz;
+    const int ntiles = (ch.kb < ch.ke) ? (ch.ke - t0 + kPairKeys - 1) / kPairKeys : 0;
+    const int pages_per_tile = kPairKeys / Psz;
     const int chunk_pages = ntiles * pages_per_tile;
     const int first_page = t0 / Psz;
 
@@ -172,12 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_window = [&](int base) {
         for (int k = lane; k < kMaxPids; k += 32) {
             const int pr = base + k;
-            int32_t id = p.num_pages;
+            int32_t id = p.num_pages;  // out-of-bounds coordinate: the copy fills zeros
             if (pr < chunk_pages && t0 + pr * Psz < ch.ke) {
                 const int32_t v = __ldg(p.page_table + (int64_t)b * p.max_pages + first_page + pr);
                 if (v >= 0 && v < p.num_pages)
                     id = v;
-                else if (is_k)
+                else
                     raise_error(p.err, DFLASH_DEVERR_PAGE_ID);
             }
             pid_w[k] = id;
@@ -187,124 +272,137 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------------- set-up
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(cbars + i, 1);
-        for (int i = 0; i < 32; ++i) {
-            uint64_t* bar = bars + i;
-            mbar_init(bar, (bar == s_free || bar == s_free + 1 || bar == rd) ? 128u : 1u);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(full + i, 1);
+            mbar_init(empty + i, 1);
+            mbar_init(pfull + i, 1);
         }
+        mbar_init(s_full, 1);
+        mbar_init(s_full + 1, 1);
+        mbar_init(p_full, 16);
+        mbar_init(p_free, 1);
+        mbar_init(p_free + 1, 1);
+        mbar_init(px_full, 1);
+        mbar_init(px_full + 1, 1);
+        mbar_init(lx_full, 1);
+        mbar_init(drain, 1);
         *abort_flag = 0;
-        *rq_cmd = 0;
-        if (!len_ok && is_k) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
+        if (!len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // the exchange barriers of tiles 0 and 1 and of the row sums expect the peer's bytes
+        mbar_expect_tx(px_full, kN * 4);
+        mbar_expect_tx(px_full + 1, kN * 4);
+        mbar_expect_tx(lx_full, kN * 4);
     }
     if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
         if (ntiles > 0) load_window(0);
     } else if (warp == kMmaWarp) {
-        if (!is_k) {
-            uint8_t* ones_s = smem + Lay::kVOnes;
-            for (int idx = lane; idx < kOnesBytes / 16; idx += 32)
-                *reinterpret_cast<uint4*>(ones_s + idx * 16) =
-                    make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // bf16 1.0
-            fence_proxy_async_smem();
+        tmem_alloc2(tmem_slot, Lay::kTmemCols);
+        tmem_relinquish2();
+    } else if (tid < kN) {
+        // column c of S^T / O^T: rows [0, 64) come from the even CTA's Q, [64, 128) from the odd's
+        const int hc = tid / kHalf, lr = tid % kHalf;
+        const int i = hc * x.Tb + lr / x.Gc, hh = lr % x.Gc;
+        int32_t lo = -(1 << 30), hi = (1 << 30);
+        int64_t orow = -1;
+        if (lr < rows_mine && i < T) {
+            const KeyRange kr = row_range(L, T, i, p.causal, p.window);
+            lo = kr.lo;
+            hi = kr.hi;
+            orow = (int64_t)(b * T + i) * p.Hq + (h0 + hh);
         }
-        tmem_alloc(tmem_slot, is_k ? Lay::kKTmemCols : Lay::kVTmemCols);
-        tmem_relinquish();
-    } else if (is_k) {
-        float* m_s = reinterpret_cast<float*>(smem + Lay::kKTable);
-        int32_t* lo_s = reinterpret_cast<int32_t*>(smem + Lay::kKTable + 6 * N * 4);
-        int32_t* hi_s = reinterpret_cast<int32_t*>(smem + Lay::kKTable + 7 * N * 4);
-        if (tid < N) {
-            int32_t lo = -(1 << 30), hi = (1 << 30);
-            if (tid < R) {
-                const KeyRange kr = row_range(L, T, tid / x.Gc, p.causal, p.window);
-                lo = kr.lo;
-                hi = kr.hi;
-            }
-            lo_s[tid] = lo;
-            hi_s[tid] = hi;
-            m_s[tid] = -INFINITY;
-        }
-        uint8_t* q_s = smem + Lay::kKQ;
-        for (int idx = tid; idx < KC * (N - R) * 8; idx += 128) {
-            const int kc = idx / ((N - R) * 8);
-            const int rem = idx - kc * (N - R) * 8;
-            *reinterpret_cast<uint4*>(q_s + kc * N * 128 + (R + rem / 8) * 128 + (rem % 8) * 16) =
+        lo_s[tid] = lo;
+        hi_s[tid] = hi;
+        orow_s[tid] = orow;
+        m_s[tid] = -INFINITY;
+        a_s[tid] = 1.f;
+        l_acc[tid] = 0.f;
+    } else if (tid < kSoftmaxThreads) {
+        // zero this CTA's Q rows [rows_mine, kHalf) of every 64-dim chunk (the copy writes the rest)
+        const int pad = kHalf - rows_mine;
+        for (int idx = tid - kN; idx < KC * pad * 8; idx += kSoftmaxThreads - kN) {
+            const int kc = idx / (pad * 8);
+            const int rem = idx - kc * pad * 8;
+            *reinterpret_cast<uint4*>(q_s + kc * kHalf * 128 + (rows_mine + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
-    } else {
-        int64_t* orow_s = reinterpret_cast<int64_t*>(smem + Lay::kVRow);
-        if (tid < N) {
-            int64_t orow = -1;
-            if (tid < R) {
-                const int i = tid / x.Gc;
-                orow = (int64_t)(b * T + i) * p.Hq + (h0 + tid - i * x.Gc);
-            }
-            orow_s[tid] = orow;
-        }
     }
     tc_fence_before();
-    // barriers of both CTAs initialised before any cross-CTA traffic
-    cluster_sync_all();
+    __syncthreads();
+    cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
     tc_fence_after();
     cudaTriggerProgrammaticLaunchCompletion();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t peer = rank ^ 1u;
+    const uint32_t tmem_s = tmem;                 // S^T buffers: columns [0, 128) and [128, 256)
+    const uint32_t tmem_o = tmem + 2 * kN;        // O^T chunk c: columns [256 + 128c, ..)
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    bool role_ok = true;
+
+    auto load16 = [&](uint32_t taddr, uint32_t (&r16)[16]) {
+        tmem_ld16(taddr, r16);
+        tmem_ld_wait();
+        reg_fence16(r16);
+    };
+    // cluster address of a shared-memory location at the same offset in CTA `r`
+    auto in_cta = [&](const void* ptr, uint32_t r) -> uint32_t { return mapa_shared(smem_u32(ptr), r); };
 
     if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
-        // ------------------------------------------------------------ TMA producers (one operand each)
-        int stage = 0;
-        uint32_t phase = 0;
+        // ------------------------------------------------------------ TMA producers
         bool ok = true;
         int wbase = 0;
-        uint32_t issued_parity[12];
+        uint32_t issued_parity[S];
 #pragma unroll
-        for (int s = 0; s < 12; ++s) issued_parity[s] = 2;
+        for (int s = 0; s < S; ++s) issued_parity[s] = 2;  // 2 = nothing outstanding
         if (ntiles > 0) {
-            if (is_k && pw == 0 && lane == 0) {
-                uint8_t* q_s = smem + Lay::kKQ;
-                mbar_expect_tx(q_full, (uint32_t)(R * 128 * KC));
-                for (int kc = 0; kc < KC; ++kc) tma_load_3d(q_s + kc * N * 128, &tm_q, q_full, kc * 64, h0, b * T);
-            }
-            const int box = Psz * 128;
-            const int per_tile = is_k ? KC : 2 * VC;
+            const int box = Psz * 128;  // bytes of one page x 64 dims
             int seq = 0;
-            for (int j = 0; j < ntiles && ok; ++j) {
-                const int rel0 = j * pages_per_tile;
-                for (int st = 0; st < per_tile && ok; ++st, ++seq) {
-                    if ((seq & 3) == pw) {
-                        if (rel0 + pages_per_tile > wbase + kMaxPids) {
-                            wbase = rel0;
-                            load_window(wbase);
-                        }
-                        if (lane == 0) ok = wait_bounded(empty + stage, phase ^ 1u, abort_flag, p.err);
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok) break;
-                        if (lane == 0) {
-                            uint8_t* dst = ring + stage * kStageBytes;
-                            mbar_expect_tx(full + stage, kStageBytes);
-                            if (is_k) {
-                                for (int pg = 0; pg < pages_per_tile; ++pg)
-                                    tma_load_4d(dst + pg * box, &tm_k, full + stage, st * 64, g, 0,
-                                                pid_w[rel0 + pg - wbase]);
-                            } else {
-                                const int h = st / VC, c = st % VC;
-                                const int ppg = 64 / Psz;
-                                for (int pg = 0; pg < ppg; ++pg) {
-                                    const int32_t page = pid_w[rel0 + h * ppg + pg - wbase];
-                                    for (int m = 0; m < 2; ++m)
-                                        tma_load_4d(dst + m * 8192 + pg * box, &tm_v, full + stage, c * 128 + m * 64,
-                                                    g, 0, page);
-                                }
+            for (int k = 0; k < 2 * ntiles && ok; ++k) {
+                bool is_k;
+                int tile;
+                pair_ring_unit(k, ntiles, is_k, tile);
+                const int n_st = is_k ? KC : 4 * VC2;
+                for (int sq = 0; sq < n_st && ok; ++sq, ++seq) {
+                    if ((seq & 3) != pw) continue;
+                    // relative pages this stage reads: K: own 128 keys; V: quarter of 64 keys
+                    const int rel0 = tile * pages_per_tile +
+                                     (is_k ? (int)rank * (kOwnKeys / Psz) : (sq / VC2) * (64 / Psz));
+                    const int npg = (is_k ? kOwnKeys : 64) / Psz;
+                    if (rel0 < wbase || rel0 + npg > wbase + kMaxPids) {
+                        wbase = rel0;
+                        load_window(wbase);
+                    }
+                    const int slot = seq % S;
+                    const uint32_t ph = (uint32_t)((seq / S) & 1);
+                    if (lane == 0) ok = ring_wait_cluster(empty + slot, ph ^ 1u, abort_flag, p.err, p.wait_ns);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        uint8_t* dst = ring + slot * kStageBytes;
+                        const bool with_q = (seq == 0);
+                        mbar_expect_tx(full + slot,
+                                       kStageBytes + (with_q ? (uint32_t)(x.Gc * x.Tb * 128 * KC) : 0u));
+                        if (with_q)
+                            for (int kc = 0; kc < KC; ++kc)
+                                tma_load_3d(q_s + kc * kHalf * 128, &tm_q, full + slot, kc * 64, h0,
+                                            b * T + (int)rank * x.Tb);
+                        if (is_k) {
+                            for (int pg = 0; pg < npg; ++pg)
+                                tma_load_4d(dst + pg * box, &tm_k, full + slot, sq * 64, g, 0,
+                                            pid_w[rel0 + pg - wbase]);
+                        } else {
+                            const int c = sq % VC2;
+                            const int d0 = c * 256 + (int)rank * 128;
+                            for (int pg = 0; pg < npg; ++pg) {
+                                const int32_t page = pid_w[rel0 + pg - wbase];
+                                for (int m = 0; m < 2; ++m)
+                                    tma_load_4d(dst + m * 8192 + pg * box, &tm_v, full + slot, d0 + m * 64, g, 0,
+                                                page);
                             }
-                            issued_parity[stage] = phase;
                         }
-                        __syncwarp();
+                        issued_parity[slot] = ph;
                     }
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    __syncwarp();
                 }
             }
         }
@@ -312,393 +410,364 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < S; ++s) {
                 if (issued_parity[s] > 1) continue;
                 const unsigned long long t_start = globaltimer();
-                while (!mbar_try_wait(full + s, issued_parity[s]) && globaltimer() - t_start < kTimeoutNs) {
+                while (!mbar_try_wait(full + s, issued_parity[s]) && globaltimer() - t_start < p.wait_ns) {
                 }
-            }
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        const uint32_t ring_addr = smem_u32(ring);
-        auto wait_lane0 = [&](uint64_t* bar, uint32_t par, bool cluster_scope) -> bool {
-            bool got = true;
-            if (lane == 0)
-                got = cluster_scope ? wait_bounded_cluster(bar, par, abort_flag, p.err)
-                                    : wait_bounded(bar, par, abort_flag, p.err);
-            return __shfl_sync(0xffffffffu, got, 0);
-        };
-        auto advance = [&]() {
-            if (++stage == S) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        };
-        if (is_k) {
-            constexpr uint32_t idesc_s = make_idesc(128, N, 0, 0);
-            const uint32_t q_addr = smem_u32(smem + Lay::kKQ);
-            if (ntiles > 0) {
-                ok = wait_lane0(q_full, 0, false);
-                tc_fence_after();
-            }
-            for (int j = 0; j < ntiles && ok; ++j) {
-                const int bf = j & 1;
-                if (j >= 2) {
-                    ok = wait_lane0(s_free + bf, (uint32_t)(((j >> 1) - 1) & 1), false);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                const uint32_t tmem_s = tmem + bf * N;
-                for (int kc = 0; kc < KC && ok; ++kc) {
-                    ok = wait_lane0(full + stage, phase, false);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t st = ring_addr + stage * kStageBytes;
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc_mma(tmem_s, sw128_desc(st + kk * 32, 16, 1024),
-                                   sw128_desc(q_addr + kc * N * 128 + kk * 32, 16, 1024), idesc_s,
-                                   (kc > 0 || kk > 0) ? 1u : 0u);
-                        tc_commit(empty + stage);
-                    }
-                    __syncwarp();
-                    advance();
-                }
-                if (!ok) break;
-                if (lane == 0) tc_commit(s_full + bf);
-                __syncwarp();
-            }
-        } else {
-            constexpr uint32_t idesc_o = make_idesc(128, N, 1, 0);
-            constexpr uint32_t idesc_l = make_idesc(128, N, 0, 0);
-            const uint32_t ones_addr = smem_u32(smem + Lay::kVOnes);
-            const uint32_t tmem_o = tmem;
-            const uint32_t tmem_l = tmem + VC * N;
-            uint32_t rq_phase = 0;
-            for (int j = 0; j < ntiles && ok; ++j) {
-                const int bf = j & 1;
-                uint8_t* msg = smem + Lay::kVMsg + bf * Lay::kMsgStride;
-                if (lane == 0) mbar_expect_tx(msg_full + bf, (uint32_t)Lay::kMsgBytes);
-                ok = wait_lane0(msg_full + bf, (uint32_t)((j >> 1) & 1), true);
-                if (!ok) break;
-                tc_fence_after();
-                const int rescale = *reinterpret_cast<volatile int*>(msg + N * 256 + 8 * N);
-                if (rescale) {
-                    // O^T and l must be scaled by alpha before this tile's PV: wait for the
-                    // previous PV, then hand the TMEM rescale to warps 0-3
-                    if (lane == 0) {
-                        tc_commit(drain);
-                        const unsigned long long t_start = globaltimer();
-                        while (!mbar_try_wait(drain, (uint32_t)(rq_phase & 1)) &&
-                               globaltimer() - t_start < kTimeoutNs) {
-                        }
-                        *rq_cmd = bf;
-                        mbar_arrive(rq);
-                    }
-                    ok = wait_lane0(rd, rq_phase & 1, false);
-                    ++rq_phase;
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                const uint32_t p_addr = smem_u32(msg);
-                const int tile_key0 = t0 + j * kTileKeys;
-                for (int h = 0; h < 2 && ok; ++h) {
-                    for (int c = 0; c < VC && ok; ++c) {
-                        ok = wait_lane0(full + stage, phase, false);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const int key0 = tile_key0 + h * 64;
-                        const int zlo = L - key0;
-                        if (L % Psz != 0 && zlo > 0 && zlo < 64 && ch.ke == L) {
-                            const int zhi = min(64, ((L + Psz - 1) / Psz) * Psz - key0);
-                            uint8_t* st = ring + stage * kStageBytes;
-                            const int rows = zhi - zlo;
-                            for (int idx = lane; idx < rows * 16; idx += 32) {
-                                const int m = idx / (rows * 8);
-                                const int rem = idx - m * rows * 8;
-                                *reinterpret_cast<uint4*>(st + m * 8192 + (zlo + rem / 8) * 128 + (rem % 8) * 16) =
-                                    make_uint4(0, 0, 0, 0);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                        }
-                        if (lane == 0) {
-                            const uint32_t st = ring_addr + stage * kStageBytes;
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                tc_mma(tmem_o + c * N, sw128_desc(st + kk * 2048, 8192, 1024),
-                                       sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024), idesc_o,
-                                       (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                            tc_commit(empty + stage);
-                        }
-                        __syncwarp();
-                        advance();
-                    }
-                    if (lane == 0) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            tc_mma(tmem_l, noswz_desc(ones_addr, 2048, 128),
-                                   sw128_desc(p_addr + h * N * 128 + kk * 32, 16, 1024), idesc_l,
-                                   (j > 0 || h > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    __syncwarp();
-                }
-                if (!ok) break;
-                // the K-CTA may refill this message buffer once these MMAs have read it
-                if (lane == 0) tc_commit_multicast(msg_free + bf, (uint16_t)1u);
-                __syncwarp();
-            }
-            // all PV done, then release the rescale/epilogue warps
-            if (lane == 0) {
-                tc_commit(drain);
-                const unsigned long long t_start = globaltimer();
-                while (!mbar_try_wait(drain, (uint32_t)(rq_phase & 1)) && globaltimer() - t_start < kTimeoutNs) {
-                }
-                *rq_cmd = -1;
-                mbar_arrive(rq);
-            }
-            __syncwarp();
-        }
-        if (is_k && lane == 0) {
-            tc_commit(drain);
-            const unsigned long long t_start = globaltimer();
-            while (!mbar_try_wait(drain, 0) && globaltimer() - t_start < kTimeoutNs) {
             }
         }
         __syncwarp();
-    } else if (is_k) {
-        // ------------------------------------------------------------ K-CTA softmax (thread = key lane)
-        float* m_s = reinterpret_cast<float*>(smem + Lay::kKTable);
-        float* a_s = m_s + N;
-        float* red = m_s + 2 * N;
-        int32_t* lo_s = reinterpret_cast<int32_t*>(smem + Lay::kKTable + 6 * N * 4);
-        int32_t* hi_s = reinterpret_cast<int32_t*>(smem + Lay::kKTable + 7 * N * 4);
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        role_ok = ok;
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer (even) / forwarder (odd)
+        bool ok = true;
+        int seq = 0;
+        // V rows past seq_len in the sequence's last, partial page are zeroed before PV (the
+        // zero probabilities there must not meet non-finite garbage)
+        auto zero_tail = [&](int tile, int q, uint8_t* st) {
+            const int key0 = t0 + tile * kPairKeys + q * 64;
+            const int zlo = L - key0;
+            if (L % Psz != 0 && zlo > 0 && zlo < 64 && ch.ke == L) {
+                const int zhi = min(64, ((L + Psz - 1) / Psz) * Psz - key0);
+                const int rows = zhi - zlo;
+                for (int idx = lane; idx < rows * 16; idx += 32) {
+                    const int m = idx / (rows * 8);
+                    const int rem = idx - m * rows * 8;
+                    *reinterpret_cast<uint4*>(st + m * 8192 + (zlo + rem / 8) * 128 + (rem % 8) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+        };
+        if (!leader) {
+            // forwarder: each own stage, once landed (and its V tail zeroed), is announced to the
+            // even CTA, whose MMAs read it
+            const uint32_t pfull0 = in_cta(pfull, 0);
+            for (int k = 0; k < 2 * ntiles && ok; ++k) {
+                bool is_k;
+                int tile;
+                pair_ring_unit(k, ntiles, is_k, tile);
+                const int n_st = is_k ? KC : 4 * VC2;
+                for (int sq = 0; sq < n_st && ok; ++sq, ++seq) {
+                    const int slot = seq % S;
+                    bool got = true;
+                    if (lane == 0)
+                        got = ring_wait(full + slot, (uint32_t)((seq / S) & 1), abort_flag, p.err, p.wait_ns);
+                    ok = __shfl_sync(0xffffffffu, got, 0);
+                    if (!ok) break;
+                    if (!is_k) zero_tail(tile, sq / VC2, ring + slot * kStageBytes);
+                    if (lane == 0) mbar_arrive_cluster(pfull0 + (uint32_t)(slot * 8));
+                    __syncwarp();
+                }
+            }
+        } else {
+            constexpr uint32_t idesc_s = make_idesc(256, kN, 0, 0);  // S^T  = K . Q^T
+            constexpr uint32_t idesc_o = make_idesc(256, kN, 1, 1);  // O^T += V^T . P^T
+            const uint32_t q_addr = smem_u32(q_s);
+            const uint32_t p_addr = smem_u32(smem + Lay::kPOff);
+            const uint32_t ring_addr = smem_u32(ring);
+            auto wait_lane0 = [&](uint64_t* bar, uint32_t par) -> bool {
+                bool got = true;
+                if (lane == 0) got = ring_wait_cluster(bar, par, abort_flag, p.err, p.wait_ns);
+                return __shfl_sync(0xffffffffu, got, 0);
+            };
+            // both CTAs' copies of the next stage have landed
+            auto next_stage = [&](uint32_t& addr, int& slot) -> bool {
+                slot = seq % S;
+                const uint32_t ph = (uint32_t)((seq / S) & 1);
+                bool got = wait_lane0(full + slot, ph);
+                if (got) got = wait_lane0(pfull + slot, ph);
+                addr = ring_addr + slot * kStageBytes;
+                return got;
+            };
+            auto release = [&](int slot) {
+                if (lane == 0) tc_commit2_both(empty + slot);
+                __syncwarp();
+                ++seq;
+            };
+            for (int k = 0; k < 2 * ntiles && ok; ++k) {
+                bool is_k;
+                int j;
+                pair_ring_unit(k, ntiles, is_k, j);
+                if (is_k) {
+                    // S^T(j) into buffer j mod 2: its previous tile j - 2 has been read by both
+                    // softmaxes (their P(j-2) was waited for by the V(j-2) unit)
+                    const uint32_t sb = tmem_s + (uint32_t)(j & 1) * kN;
+                    for (int kc = 0; kc < KC && ok; ++kc) {
+                        uint32_t st;
+                        int slot;
+                        ok = next_stage(st, slot);
+                        if (!ok) break;
+                        tc_fence_after();
+                        if (lane == 0) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc_mma2(sb, sw128_desc(st + kk * 32, 16, 1024),
+                                        sw128_desc(q_addr + kc * kHalf * 128 + kk * 32, 16, 1024), idesc_s,
+                                        (kc > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        release(slot);
+                    }
+                    if (!ok) break;
+                    if (lane == 0) tc_commit2_both(s_full + (j & 1));
+                    __syncwarp();
+                    continue;
+                }
+                ok = wait_lane0(p_full, (uint32_t)(j & 1));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t pb_addr = p_addr + (uint32_t)(j & 1) * Lay::kPBuf;
+                for (int q = 0; q < 4 && ok; ++q) {
+                    for (int c = 0; c < VC2 && ok; ++c) {
+                        uint32_t st;
+                        int slot;
+                        ok = next_stage(st, slot);
+                        if (!ok) break;
+                        zero_tail(j, q, smem + (st - smem_u32(smem)));
+                        tc_fence_after();
+                        if (lane == 0) {
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                tc_mma2(tmem_o + c * kN, sw128_desc(st + kk * 2048, 8192, 1024),
+                                        sw32_desc(pb_addr + q * Lay::kPQuarter + kk * 512, 2048, 256), idesc_o,
+                                        (j > 0 || q > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        release(slot);
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) tc_commit2_both(p_free + (j & 1));
+                __syncwarp();
+            }
+            // drain our MMAs before either CTA frees TMEM or leaves (they read both CTAs' memory)
+            if (lane == 0) {
+                tc_commit2_local(drain);
+                const unsigned long long t_start = globaltimer();
+                while (!mbar_try_wait(drain, 0) && globaltimer() - t_start < p.wait_ns) {
+                }
+            }
+            __syncwarp();
+        }
+        role_ok = ok;
+    } else {
+        // ------------------------------------------------------------ softmax (warps 0-7)
         const float sl2 = p.scale * kLog2e;
         const bool plain = (p.causal == 0 && p.window == 0);
-        const int pchunk = (tid & 63) >> 3;
-        const int pbyte = (tid & 7) * 2;
+        const int kl = tid & 127;         // key lane of this CTA's 128 keys (TMEM lane)
+        const int chh = tid >> 7;         // rows [64 chh, 64 chh + 64): the P^T buffer of CTA chh
+        const int col0 = chh * kHalf;
+        const int pk = (int)rank * kOwnKeys + kl;  // key index within the pair tile
+        // P^T (MN-major, 32-byte swizzle): quarter of 64 keys, 16-row atoms of 2 KB, 8-key
+        // groups of 256 B, 32 B per key with the 16-byte halves swapped for keys 4-7 of a group
+        const int kig = pk & 7;
+        const uint32_t prow_off = (uint32_t)(Lay::kPOff + (pk >> 6) * Lay::kPQuarter + ((pk & 63) >> 3) * 256 +
+                                             kig * 32);
+        const uint32_t pswz0 = (uint32_t)((0 ^ (kig >> 2)) << 4);
+        const uint32_t pswz1 = (uint32_t)((1 ^ (kig >> 2)) << 4);
+        const bool p_local = (chh == (int)rank);
+        const uint32_t p_base = p_local ? smem_u32(smem) : mapa_shared(smem_u32(smem), (uint32_t)chh);
+        const uint32_t p_full_bar = in_cta(p_full, 0);
         bool ok = true;
-        auto group_wait = [&](uint64_t* bar, uint32_t parity, bool cluster_scope) -> bool {
+        auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool got = true;
-            if (tid == 0)
-                got = cluster_scope ? wait_bounded_cluster(bar, parity, abort_flag, p.err)
-                                    : wait_bounded(bar, parity, abort_flag, p.err);
-            return !named_bar_or_128(!got);
+            if (tid == 0) got = ring_wait_cluster(bar, parity, abort_flag, p.err, p.wait_ns);
+            return !bar_or_256(!got);
         };
-        auto load16 = [&](uint32_t taddr, uint32_t (&r16)[16]) {
-            tmem_ld16(taddr, r16);
-            tmem_ld_wait();
-            reg_fence16(r16);
+        // column sums of a finished tile (over this CTA's 128 keys) into l_acc, after the old
+        // sums were scaled by that tile's rescale factor (threads 0-127, one column each)
+        auto fold_sums = [&]() {
+            if (tid < kN) {
+                const int hc = tid >> 6, cl = tid & 63;
+                const float s4 = (red2[(hc * 4 + 0) * 64 + cl] + red2[(hc * 4 + 1) * 64 + cl]) +
+                                 (red2[(hc * 4 + 2) * 64 + cl] + red2[(hc * 4 + 3) * 64 + cl]);
+                l_acc[tid] = l_acc[tid] * a_s[tid] + s4;
+            }
         };
-        const uint32_t msg_peer0 = mapa_shared(smem_u32(smem + Lay::kVMsg), peer);
-        const uint32_t full_peer0 = mapa_shared(smem_u32(msg_full), peer);
-        int sent = 0;
         for (int j = 0; j < ntiles && ok; ++j) {
-            const int bf = j & 1;
-            const uint32_t tmem_s = tmem + bf * N;
-            if (!group_wait(s_full + bf, (uint32_t)((j >> 1) & 1), false)) {
+            if (!group_wait(s_full + (j & 1), (uint32_t)((j >> 1) & 1))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int key = t0 + j * kTileKeys + tid;
+            const uint32_t sb = tmem_s + (uint32_t)(j & 1) * kN + lane_base + (uint32_t)col0;
+            const int key = t0 + j * kPairKeys + pk;
             const bool kvalid = key >= ch.kb && key < ch.ke;
             auto score = [&](uint32_t raw, int col) -> float {
                 bool vis = kvalid;
                 if (!plain) vis = vis && key >= lo_s[col] && key <= hi_s[col];
                 return vis ? u2f(raw) * sl2 : -INFINITY;
             };
+            // pass 1: this warp's column maxima over its 32 keys, one column per lane
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                uint32_t r16[16];
+                load16(sb + q * 16, r16);
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) v[u] = score(r16[u], col0 + q * 16 + u);
+                const float mx = pair_transpose_max16(v, lane);
+                if (lane < 16) red[warp * 64 + q * 16 + lane] = mx;
+            }
+            bar_sync_256();
+            float mloc = -INFINITY;
+            // the previous tile's sums are final now (its rescale factor is still in a_s)
+            if (j > 0) fold_sums();
+            if (tid < kN) {
+                // column tid over this CTA's 128 keys: warps hc*4 .. hc*4+3 of the rows' half
+                const int hc = tid >> 6, cl = tid & 63;
+                mloc = fmaxf(fmaxf(red[(hc * 4 + 0) * 64 + cl], red[(hc * 4 + 1) * 64 + cl]),
+                             fmaxf(red[(hc * 4 + 2) * 64 + cl], red[(hc * 4 + 3) * 64 + cl]));
+                st_async_f32(in_cta(px + (j & 1) * kN + tid, peer), mloc, in_cta(px_full + (j & 1), peer));
+            }
+            // the peer's maxima of the same columns: both CTAs then take the same lazy update
+            if (!group_wait(px_full + (j & 1), (uint32_t)((j >> 1) & 1))) {
+                ok = false;
+                break;
+            }
             bool need = false;
-#pragma unroll 1
-            for (int q = 0; q < NQ; ++q) {
-                float mv[16];
-                load_row16(m_s + q * 16, mv);
-                uint32_t r16[16];
-                load16(tmem_s + lane_base + q * 16, r16);
-#pragma unroll
-                for (int u = 0; u < 16; ++u) need |= score(r16[u], q * 16 + u) > mv[u] + kRescaleThresh;
+            if (tid < kN) {
+                const float mx = fmaxf(mloc, px[(j & 1) * kN + tid]);
+                const float mo = m_s[tid];
+                if (mx > mo + kRescaleThresh) {
+                    m_s[tid] = mx;
+                    a_s[tid] = (mo == -INFINITY) ? 0.f : ex2(mo - mx);
+                    need = true;
+                } else {
+                    a_s[tid] = 1.f;
+                }
             }
-            need = named_bar_or_128(need);
-            if (need) {
+            need = bar_or_256(need);
+            // px of this tile has been read by everyone: expect the peer's maxima of tile j + 2
+            if (tid == 0) mbar_expect_tx(px_full + (j & 1), kN * 4);
+            if (j > 0 && need) {
+                // O^T holds tiles < j once PV(j-1) is done: rescale it in TMEM
+                if (!group_wait(p_free + ((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                constexpr int nsplit = 2 / VC2;  // warps w and w+4: one chunk each, or half the columns
+                const int c = (warp >> 2) % VC2;
 #pragma unroll 1
-                for (int q = 0; q < NQ; ++q) {
+                for (int q = (warp >> 2) / VC2; q < kN / 16; q += nsplit) {
                     uint32_t r16[16];
-                    load16(tmem_s + lane_base + q * 16, r16);
+                    const uint32_t ta = tmem_o + c * kN + lane_base + q * 16;
+                    load16(ta, r16);
+                    float av[16];
+                    load_row16(a_s + q * 16, av);
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        float v = score(r16[u], q * 16 + u);
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-                        if (((q * 16 + u) & 31) == lane) red[warp * N + q * 16 + u] = v;
-                    }
+                    for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * av[u]);
+                    tmem_st16(ta, r16);
                 }
-                named_bar_sync_128();
-                if (tid < N) {
-                    const float mo = m_s[tid];
-                    const float mn =
-                        fmaxf(fmaxf(mo, fmaxf(red[tid], red[N + tid])), fmaxf(red[2 * N + tid], red[3 * N + tid]));
-                    m_s[tid] = mn;
-                    a_s[tid] = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
-                }
-                named_bar_sync_128();
+                tmem_st_wait();
             }
-            // the staging buffer of this tile was last sent two tiles ago: that copy must have read it
-            uint8_t* stg = smem + Lay::kKStage + bf * Lay::kMsgStride;
-            if (j >= 2 && tid == 0) bulk_wait_read_1();
-            named_bar_sync_128();
-            uint8_t* pcol = stg + (tid >> 6) * (N * 128);
+            if (j > 1) {
+                if (!group_wait(p_free + (j & 1), (uint32_t)(((j - 2) >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            // pass 2: P = exp2(s - m) as bf16 pairs into the P^T buffer (j mod 2) of CTA chh,
+            // and this warp's column sums of the rounded P
+            const uint32_t prow = p_base + prow_off + (uint32_t)((j & 1) * Lay::kPBuf);
 #pragma unroll 1
-            for (int q = 0; q < NQ; ++q) {
+            for (int q = 0; q < 4; ++q) {
                 float mv[16];
-                load_row16(m_s + q * 16, mv);
+                load_row16(m_s + col0 + q * 16, mv);
                 uint32_t r16[16];
-                load16(tmem_s + lane_base + q * 16, r16);
-                __nv_bfloat16 pb[16];
+                load16(sb + q * 16, r16);
+                uint32_t pk2[8];
+                float pv[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float sc = score(r16[u], q * 16 + u);
-                    pb[u] = __float2bfloat16_rn((sc == -INFINITY) ? 0.f : ex2(sc - mv[u]));
+                for (int u = 0; u < 8; ++u) {
+                    const float s0 = score(r16[2 * u], col0 + q * 16 + 2 * u);
+                    const float s1 = score(r16[2 * u + 1], col0 + q * 16 + 2 * u + 1);
+                    const float e0 = (s0 == -INFINITY) ? 0.f : ex2(s0 - mv[2 * u]);
+                    const float e1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - mv[2 * u + 1]);
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+                    pk2[u] = *reinterpret_cast<const uint32_t*>(&h2);
+                    pv[2 * u] = __low2float(h2);
+                    pv[2 * u + 1] = __high2float(h2);
                 }
-                uint8_t* prow = pcol + q * 16 * 128 + pbyte;
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    *reinterpret_cast<__nv_bfloat16*>(prow + u * 128 + ((pchunk ^ (u & 7)) << 4)) = pb[u];
-            }
-            // S^T of this buffer is no longer needed: QK of tile j+2 may overwrite it
-            tc_fence_before();
-            mbar_arrive(s_free + bf);
-            if (tid < N) {
-                reinterpret_cast<float*>(stg + N * 256)[tid] = (need && j > 0) ? a_s[tid] : 1.f;
-                reinterpret_cast<float*>(stg + N * 256 + 4 * N)[tid] = m_s[tid];
-            }
-            if (tid == 0) {
-                int* fl = reinterpret_cast<int*>(stg + N * 256 + 8 * N);
-                fl[0] = (need && j > 0) ? 1 : 0;
-                fl[1] = 0;
-                fl[2] = 0;
-                fl[3] = 0;
-            }
-            fence_proxy_async_smem();
-            named_bar_sync_128();
-            bool go = true;
-            if (tid == 0) {
-                if (j >= 2) go = wait_bounded_cluster(msg_free + bf, (uint32_t)(((j >> 1) - 1) & 1), abort_flag, p.err);
-                if (go) {
-                    bulk_copy_to_peer(msg_peer0 + bf * Lay::kMsgStride, stg, (uint32_t)Lay::kMsgBytes,
-                                      full_peer0 + bf * 8);
-                    bulk_commit_group();
+                const uint32_t dst = prow + (uint32_t)(q * 2048);
+                const uint4 lo4 = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
+                const uint4 hi4 = make_uint4(pk2[4], pk2[5], pk2[6], pk2[7]);
+                if (p_local) {
+                    uint8_t* d8 = smem + (dst - smem_u32(smem));
+                    *reinterpret_cast<uint4*>(d8 + pswz0) = lo4;
+                    *reinterpret_cast<uint4*>(d8 + pswz1) = hi4;
+                } else {
+                    st_cluster_v4(dst + pswz0, lo4);
+                    st_cluster_v4(dst + pswz1, hi4);
                 }
+                const float sm = pair_transpose_sum16(pv, lane);
+                if (lane < 16) red2[warp * 64 + q * 16 + lane] = sm;
             }
-            ok = !named_bar_or_128(!go);
-            if (ok) ++sent;
-        }
-        // every copy has left our shared memory, and the V-CTA has released every buffer
-        if (tid == 0) {
-            bulk_wait_read_0();
-            for (int j = (sent >= 2 ? sent - 2 : 0); j < sent; ++j)
-                if (!wait_bounded_cluster(msg_free + (j & 1), (uint32_t)((j >> 1) & 1), abort_flag, p.err)) break;
-        }
-    } else {
-        // ------------------------------------------------------------ V-CTA rescale + epilogue
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const uint32_t tmem_o = tmem;
-        const uint32_t tmem_l = tmem + VC * N;
-        int64_t* orow_s = reinterpret_cast<int64_t*>(smem + Lay::kVRow);
-        bool ok = true;
-        auto load16 = [&](uint32_t taddr, uint32_t (&r16)[16]) {
-            tmem_ld16(taddr, r16);
-            tmem_ld_wait();
-            reg_fence16(r16);
-        };
-        uint32_t rq_phase = 0;
-        for (;;) {
-            bool got = true;
-            if (tid == 0) got = wait_bounded(rq, rq_phase & 1, abort_flag, p.err);
-            ok = !named_bar_or_128(!got);
-            ++rq_phase;
-            if (!ok) break;
-            const int cmd = *rq_cmd;
-            if (cmd < 0) break;
-            tc_fence_after();
-            const float* alpha = reinterpret_cast<const float*>(smem + Lay::kVMsg + cmd * Lay::kMsgStride + N * 256);
-#pragma unroll 1
-            for (int cq = 0; cq < (VC + 1) * NQ; ++cq) {  // O^T chunks, then the row sums
-                const int c = cq / NQ, q = cq % NQ;
-                uint32_t r16[16];
-                const uint32_t ta = tmem_o + c * N + lane_base + q * 16;
-                load16(ta, r16);
-                float av[16];
-                load_row16(alpha + q * 16, av);
-#pragma unroll
-                for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * av[u]);
-                tmem_st16(ta, r16);
-            }
-            tmem_st_wait();
+            fence_proxy_async_cluster();
             tc_fence_before();
-            mbar_arrive(rd);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(p_full_bar);
         }
+        // the last tile's sums
+        bar_sync_256();
+        if (ok && ntiles > 0) fold_sums();
+        bool good = ok && ntiles > 0;
+        if (good) good = group_wait(p_free + ((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1));
+        role_ok = good;
+    }
+
+    // ---------------------------------------------------------------- epilogue (warps 0-7)
+    if (warp < 8) {
+        const bool have_o = !bar_or_256(!role_ok) && ntiles > 0;
         tc_fence_after();
-        // ---------------------------------------------------------------- epilogue
-        const bool have_o = ok && ntiles > 0;
-        const float* m_fin = reinterpret_cast<const float*>(smem + Lay::kVMsg + ((ntiles - 1) & 1) * Lay::kMsgStride +
-                                                            N * 256 + 4 * N);
-        const int64_t part_base = (int64_t)c_split * p.B * T * p.Hq;
+        // row sums: this CTA's keys' part to the peer, the peer's part from it
+        if (tid < kN) st_async_f32(in_cta(lx + tid, peer), have_o ? l_acc[tid] : 0.f, in_cta(lx_full, peer));
+        {
+            bool got = true;
+            if (tid == 0) got = ring_wait_cluster(lx_full, 0, abort_flag, p.err, p.wait_ns);
+            bar_or_256(!got);
+        }
+        const int64_t part_base = (int64_t)c_split * p.B * p.T * p.Hq;
         const bool final_out = (p.splits == 1);
-        __nv_bfloat16* __restrict__ out_bf = reinterpret_cast<__nv_bfloat16*>(p.out);
-        float* __restrict__ part_out = p.part_out;
-#pragma unroll 1
-        for (int q = 0; q < NQ; ++q) {
-            int64_t orow[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) orow[u] = orow_s[q * 16 + u];
-            uint32_t l16[16];
-            if (have_o) {
-                load16(tmem_l + lane_base + q * 16, l16);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 16; ++u) l16[u] = 0u;
-            }
-            float inv[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const float tot = u2f(l16[u]);
-                inv[u] = tot > 0.f ? __frcp_rn(tot) : 0.f;
-            }
-            const int my = tid - q * 16;
-            if (my >= 0 && my < 16 && tid < R) {
-                float tot = 0.f;
-#pragma unroll
-                for (int u = 0; u < 16; ++u)
-                    if (u == my) tot = u2f(l16[u]);
-                const float lse_v = tot > 0.f ? (m_fin[tid] + __log2f(tot)) * kLn2 : -INFINITY;
+        if (tid < kN) {
+            const float tot = (have_o ? l_acc[tid] : 0.f) + lx[tid];
+            a_s[tid] = tot > 0.f ? 1.f / tot : 0.f;
+            // each CTA writes the lse of half of the rows
+            if ((tid >> 6) == (int)rank && orow_s[tid] >= 0) {
+                const float lse_v = tot > 0.f ? (m_s[tid] + __log2f(tot)) * kLn2 : -INFINITY;
                 if (final_out) {
                     if (p.lse) p.lse[orow_s[tid]] = lse_v;
                 } else {
                     p.part_lse[part_base + orow_s[tid]] = lse_v;
                 }
             }
+        }
+        bar_sync_256();
+        // O^T: warp w reads TMEM lanes 32(w%4).. = dims of chunk c; each column is one output
+        // row, and the warp's 32 lanes store 32 consecutive dims of it
+        constexpr int nsplit = 2 / VC2;
+        const int c = (warp >> 2) % VC2;
+        const int d = c * 256 + (int)rank * 128 + (warp & 3) * 32 + lane;
 #pragma unroll 1
-            for (int c = 0; c < VC; ++c) {
-                const int d = c * 128 + tid;
-                uint32_t r16[16];
-                if (have_o) {
-                    load16(tmem_o + c * N + lane_base + q * 16, r16);
-                } else {
+        for (int q = (warp >> 2) / VC2; q < kN / 16; q += nsplit) {
+            uint32_t r16[16];
+            if (have_o) {
+                load16(tmem_o + c * kN + lane_base + q * 16, r16);
+            } else {
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) r16[u] = 0u;
-                }
-                if (final_out) {
+                for (int u = 0; u < 16; ++u) r16[u] = 0u;
+            }
+            float iv[16];
+            load_row16(a_s + q * 16, iv);
 #pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        if (q * 16 + u < R) out_bf[orow[u] * D + d] = __float2bfloat16_rn(u2f(r16[u]) * inv[u]);
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        if (q * 16 + u < R) part_out[(part_base + orow[u]) * D + d] = u2f(r16[u]) * inv[u];
-                }
+            for (int u = 0; u < 16; ++u) {
+                const int64_t orow = orow_s[q * 16 + u];
+                if (orow < 0) continue;
+                const float v = u2f(r16[u]) * iv[u];
+                if (final_out)
+                    static_cast<__nv_bfloat16*>(p.out)[orow * D + d] = __float2bfloat16_rn(v);
+                else
+                    p.part_out[(part_base + orow) * D + d] = v;
             }
         }
     }
@@ -706,12 +775,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // no CTA leaves while the pair MMAs or the peer may still touch its memory
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, is_k ? Lay::kKTmemCols : Lay::kVTmemCols);
+        tmem_dealloc2(tmem, Lay::kTmemCols);
     }
-    // no CTA of the pair leaves while its peer may still address its shared memory
-    cluster_sync_all();
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -720,7 +788,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn()
+EncodeTiledFn pair_encode_fn()
 {
     static EncodeTiledFn fn = nullptr;
     static std::once_flag once;
@@ -735,19 +803,12 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-int choose_gc(int G, int T)
+template <int D>
+cudaError_t launch_pair_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                          const PairExtra& x, cudaStream_t stream)
 {
-    for (int gc = G; gc >= 1; --gc)
-        if (G % gc == 0 && gc * T <= kMaxRows) return gc;
-    return 0;
-}
-
-template <int D, int N>
-cudaError_t launch_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                      const PairExtra& x, cudaStream_t stream)
-{
-    using Lay = PairLayout<D, N>;
-    auto kern = tc_pair_kernel<D, N>;
+    using Lay = PairLayout<D>;
+    auto kern = tc_pair_attn_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -765,54 +826,55 @@ cudaError_t launch_dn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p, x);
 }
 
-template <int D>
-cudaError_t launch_d(int n, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                     const PairExtra& x, cudaStream_t stream)
-{
-    switch (n) {
-    case 16: return launch_dn<D, 16>(tq, tk, tv, p, x, stream);
-    case 32: return launch_dn<D, 32>(tq, tk, tv, p, x, stream);
-    case 48: return launch_dn<D, 48>(tq, tk, tv, p, x, stream);
-    case 64: return launch_dn<D, 64>(tq, tk, tv, p, x, stream);
-    case 80: return launch_dn<D, 80>(tq, tk, tv, p, x, stream);
-    }
-    return cudaErrorNotSupported;
-}
-
 }  // namespace
+
+// Query heads per pair: the largest divisor of G whose rows fit 64 per CTA (ceil(T/2) block
+// positions each), or 0.
+int pair_choose_gc(int G, int T)
+{
+    const int tb = (T + 1) / 2;
+    for (int gc = G; gc >= 1; --gc)
+        if (G % gc == 0 && gc * tb <= kHalf) return gc;
+    return 0;
+}
 
 bool tc_pair_supports(const AttnParams& p)
 {
     if (p.dtype != DFLASH_BF16) return false;
-    if (p.D != 128 && p.D != 256 && p.D != 512) return false;
+    if (p.D != 256 && p.D != 512) return false;
     if (p.page_size != 16 && p.page_size != 32 && p.page_size != 64) return false;
-    if (choose_gc(p.G, p.T) == 0) return false;
+    if (p.T < 2 || pair_choose_gc(p.G, p.T) == 0) return false;
     if (p.sh % 8 || p.ss % 8 || p.sp % 8) return false;
     return true;
 }
 
 int tc_pair_ctas_per_split(const AttnParams& p)
 {
-    const int gc = choose_gc(p.G, p.T);
+    const int gc = pair_choose_gc(p.G, p.T);
     return gc > 0 ? 2 * p.B * p.Hkv * (p.G / gc) : 0;
+}
+
+int tc_pair_row_groups(const AttnParams& p)
+{
+    const int gc = pair_choose_gc(p.G, p.T);
+    return gc > 0 ? p.G / gc : 0;
 }
 
 cudaError_t launch_tc_pair_attn(const AttnParams& p, cudaStream_t stream)
 {
-    if (!tc_pair_supports(p)) return cudaErrorNotSupported;
-    EncodeTiledFn enc = encode_fn();
+    if (!tc_pair_supports(p) || p.balanced) return cudaErrorNotSupported;
+    EncodeTiledFn enc = pair_encode_fn();
     if (!enc) return cudaErrorNotSupported;
     PairExtra x;
-    x.Gc = choose_gc(p.G, p.T);
+    x.Gc = pair_choose_gc(p.G, p.T);
     x.n_rg = p.G / x.Gc;
-    x.R = x.Gc * p.T;
-    const int n = ((x.R + 15) / 16) * 16;
+    x.Tb = (p.T + 1) / 2;
 
     CUtensorMap tq, tk, tv;
     {
         const cuuint64_t dims[3] = {(cuuint64_t)p.D, (cuuint64_t)p.Hq, (cuuint64_t)p.B * p.T};
         const cuuint64_t strides[2] = {(cuuint64_t)p.D * 2, (cuuint64_t)p.Hq * p.D * 2};
-        const cuuint32_t box[3] = {64, (cuuint32_t)x.Gc, (cuuint32_t)p.T};
+        const cuuint32_t box[3] = {64, (cuuint32_t)x.Gc, (cuuint32_t)x.Tb};
         const cuuint32_t es[3] = {1, 1, 1};
         if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p.q), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -836,9 +898,8 @@ cudaError_t launch_tc_pair_attn(const AttnParams& p, cudaStream_t stream)
     }
     cudaError_t e;
     switch (p.D) {
-    case 128: e = launch_d<128>(n, tq, tk, tv, p, x, stream); break;
-    case 256: e = launch_d<256>(n, tq, tk, tv, p, x, stream); break;
-    case 512: e = launch_d<512>(n, tq, tk, tv, p, x, stream); break;
+    case 256: e = launch_pair_d<256>(tq, tk, tv, p, x, stream); break;
+    case 512: e = launch_pair_d<512>(tq, tk, tv, p, x, stream); break;
     default: e = cudaErrorNotSupported;
     }
     if (e != cudaSuccess || p.splits == 1) return e;

@@ -59,14 +59,15 @@ __device__ __forceinline__ unsigned long long globaltimer()
 }
 
 // Bounded wait: false on timeout (recorded) or when another warp aborted.
-static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err)
+static __device__ __noinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err,
+                                                 unsigned long long limit = kTimeoutNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
+        if (globaltimer() - t0 > limit) {
             *abort_flag = 1;
             raise_error(err, DFLASH_DEVERR_TIMEOUT);
             return false;
@@ -92,7 +93,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity)
 // suspends resumes some time after the phase completes; on these hand-offs, taken several
 // hundred times per tile, that latency added 10-30 % to the kernels' times. Same outcome and
 // error reporting as wait_bounded.
-__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err)
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err,
+                                          unsigned long long limit = kTimeoutNs)
 {
     if (mbar_test_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
@@ -100,7 +102,7 @@ __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volati
         for (int k = 0; k < 64; ++k)
             if (mbar_test_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kTimeoutNs) {
+        if (globaltimer() - t0 > limit) {
             *abort_flag = 1;
             raise_error(err, DFLASH_DEVERR_TIMEOUT);
             return false;
@@ -395,6 +397,125 @@ __device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t cta_
             smem_u32(bar)),
         "h"(cta_mask)
         : "memory");
+}
+
+// ---------------------------------------------------------------- CTA pair (cta_group::2)
+// A pair of CTAs in a 2-CTA cluster shares each MMA: the A operand's 256 rows are 128 from
+// each CTA's shared memory (same offset in both), the B operand's N columns are split in
+// halves (the first N/2 from the even CTA), and each CTA's TMEM receives its 128 rows of D.
+// The even CTA issues the MMAs; TMEM is allocated and freed by one warp of each CTA together.
+
+__device__ __forceinline__ void tmem_alloc2(uint32_t* dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish2()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma2(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accum)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at this offset in both CTAs of the pair when every earlier
+// pair MMA of this thread has completed.
+__device__ __forceinline__ void tc_commit2_both(uint64_t* bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+// Arrive once on this CTA's own mbarrier when every earlier pair MMA of this thread has completed.
+__device__ __forceinline__ void tc_commit2_local(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Generic stores into the peer CTA's shared memory (cluster addresses from mapa_shared).
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Asynchronous 4-byte store into the peer CTA's shared memory that counts its bytes on the
+// peer's mbarrier (both given as cluster addresses); the peer sees the value once that
+// barrier's phase completes.
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t mbar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+                 "r"(__float_as_uint(v)), "r"(mbar)
+                 : "memory");
+}
+
+// Arrive (release at cluster scope) on an mbarrier given by its cluster address (own or peer).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+
+// Make this thread's generic shared-memory writes (own and peer CTA) visible to the async
+// proxy (the tensor cores read the P operand through it).
+__device__ __forceinline__ void fence_proxy_async_cluster()
+{
+    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// ring_wait with cluster-scope acquire, for barriers the peer CTA (or a pair MMA commit) completes.
+__device__ __forceinline__ bool ring_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint32_t* err, unsigned long long limit)
+{
+    if (mbar_test_wait_cluster(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        for (int k = 0; k < 64; ++k)
+            if (mbar_test_wait_cluster(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) {
+            *abort_flag = 1;
+            raise_error(err, DFLASH_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
 }
 
 }  // namespace ptx

@@ -337,3 +337,38 @@ def test_auto_plan_takes_uniform_waves_for_long_spans(lib):
     assert lib.dflash_plan_splits(ctypes.byref(sweep), 9, 0, 0, 0) == sms // 4
     # an explicit count is taken as given
     assert lib.dflash_plan_splits(ctypes.byref(long), 16, 0, 5, 0) == 5
+
+
+def _cpu_inputs(B=2, T=9, Hq=4, Hkv=2, D=64, P=16, pages=8):
+    q = torch.zeros((B * T, Hq, D), dtype=torch.bfloat16)
+    k = torch.zeros((pages, P, Hkv, D), dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    pt = torch.zeros((B, 4), dtype=torch.int32)
+    sl = torch.full((B,), 20, dtype=torch.int32)
+    return q, k, v, pt, sl
+
+
+@pytest.mark.parametrize("entry", ["block_attn", "block_attn_noalloc"])
+@pytest.mark.parametrize("bad", ["v_shape", "v_stride", "pt_int64", "sl_int64", "pt_slice", "q_rows", "out_dtype"])
+def test_attention_entry_points_reject_mismatched_inputs_before_launch(lib, entry, bad):
+    # v_cache is read with k_cache's geometry and the index tensors as int32, so both entry
+    # points must refuse these before the library (or any kernel) sees a pointer
+    q, k, v, pt, sl = _cpu_inputs()
+    out = None
+    if bad == "v_shape":
+        v = torch.zeros((4,) + tuple(k.shape[1:]), dtype=k.dtype)
+    elif bad == "v_stride":
+        v = torch.zeros((k.shape[0], k.shape[1], k.shape[3], k.shape[2]), dtype=k.dtype).transpose(2, 3)
+    elif bad == "pt_int64":
+        pt = pt.to(torch.int64)
+    elif bad == "sl_int64":
+        sl = sl.to(torch.int64)
+    elif bad == "pt_slice":
+        pt = torch.zeros((2, 8), dtype=torch.int32)[:, :4]
+    elif bad == "q_rows":
+        q = q[:-1]
+    elif bad == "out_dtype":
+        out = torch.zeros(q.shape, dtype=torch.float32)
+    fn = getattr(dfl, entry)
+    with pytest.raises((ValueError, TypeError)):
+        fn(q, k, v, pt, sl, 9, out=out)

@@ -14,7 +14,8 @@ sys.path.insert(0, ROOT)
 
 import bench  # noqa: E402
 
-KERNELS = ("tc_attn_kernel", "project_kv_kernel", "accept_kernel", "grouped_conv_kernel", "selector_kernel")
+KERNELS = ("tc_attn_kernel@global_verify", "project_kv_kernel", "accept_kernel", "grouped_conv_kernel",
+           "selector_kernel")
 
 
 def test_every_recorded_traffic_is_current_or_reported_stale():
@@ -23,7 +24,8 @@ def test_every_recorded_traffic_is_current_or_reported_stale():
     for name in KERNELS:
         for f in rec[name]["sources"]:
             assert os.path.exists(os.path.join(ROOT, f)), f
-        traffic, note = bench.traffic_from_profiles(name)
+        kernel, _, workload = name.partition("@")
+        traffic, note = bench.traffic_from_profiles(kernel, workload or None)
         if rec[name]["source_sha256"] == bench.kernel_source_sha(rec[name]["sources"]):
             assert traffic == rec[name]["dram_bytes_per_launch"] and traffic > 0, name
         else:
@@ -32,8 +34,10 @@ def test_every_recorded_traffic_is_current_or_reported_stale():
 
 def test_traffic_is_null_once_a_source_changes(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_sha", lambda files: "0" * 64)
-    traffic, note = bench.traffic_from_profiles("tc_attn_kernel")
+    traffic, note = bench.traffic_from_profiles("tc_attn_kernel", "global_verify")
     assert traffic is None and "changed" in note
+    # a record of the kernel on another workload never stands for this one
+    assert bench.traffic_from_profiles("tc_attn_kernel", "long_draft")[0] is None
     assert bench.traffic_from_profiles("no_such_kernel") == (None, None)
 
 

@@ -14,6 +14,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 CONFIGS = {
+    "long_draft": ("kv_hbm_gbs", "GB/s"),
     "global_verify": ("kv_hbm_gbs", "GB/s"),
     "accept_verify": ("logits_hbm_gbs", "GB/s"),
     "project_prefill": ("projection_tflops", "TFLOP/s"),

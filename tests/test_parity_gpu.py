@@ -40,13 +40,42 @@ def _tc_available(case, kernel="tc"):
         return False
 
 
+GUARD = 4096  # elements of canary before and after each output buffer (16-byte multiples)
+
+
+def _canary(dtype):
+    # a finite bit pattern no kernel writes by chance (bf16 ~3.3e38, fp32 ~3.3e38)
+    return (torch.int16, 0x7F7A) if dtype == torch.bfloat16 else (torch.int32, 0x7F7A5A5A)
+
+
+def guarded(shape, dtype):
+    """A contiguous view of `shape` in the middle of a larger buffer whose guard regions hold a
+    canary pattern; check_guards() then proves the call wrote nothing outside the view."""
+    n = int(np.prod(shape))
+    buf = torch.empty(n + 2 * GUARD, dtype=dtype, device="cuda")
+    itype, pat = _canary(dtype)
+    buf.view(itype).fill_(pat)
+    return buf, buf[GUARD:GUARD + n].view(shape)
+
+
+def check_guards(buf, what):
+    itype, pat = _canary(buf.dtype)
+    bits = buf.view(itype)
+    assert (bits[:GUARD] == pat).all().item() and (bits[-GUARD:] == pat).all().item(), \
+        f"{what}: a write landed outside the output buffer"
+
+
 def run(case, kernel="auto", num_splits=None, page_table=None, **kw):
-    out, lse = dfl.block_attn(case.q, case.k_cache, case.v_cache,
-                              case.page_table if page_table is None else page_table,
-                              case.seq_lens, case.block_len, causal=case.causal, window=case.window,
-                              scale=case.scale, kernel=kernel,
-                              num_splits=case.num_splits if num_splits is None else num_splits, **kw)
+    obuf, out = guarded(tuple(case.q.shape), case.q.dtype)
+    lbuf, lse = guarded(tuple(case.q.shape[:2]), torch.float32)
+    dfl.block_attn(case.q, case.k_cache, case.v_cache,
+                   case.page_table if page_table is None else page_table,
+                   case.seq_lens, case.block_len, causal=case.causal, window=case.window,
+                   scale=case.scale, kernel=kernel, out=out, lse=lse,
+                   num_splits=case.num_splits if num_splits is None else num_splits, **kw)
     torch.cuda.synchronize()
+    check_guards(obuf, f"{case.name} out")
+    check_guards(lbuf, f"{case.name} lse")
     return out, lse
 
 
@@ -83,6 +112,30 @@ def sample_rows(case, per_request=6, seed=0):
             picks.add((int(rng.integers(case.num_q_heads)), int(rng.integers(case.block_len))))
         rows += [(b, h, i) for h, i in sorted(picks)]
     return np.array(rows, dtype=np.int32)
+
+
+def group_rows(case, seed=0):
+    """Every output row of one (request, KV head) group per request: all G query heads x all T
+    block positions, which at T = 16 and GQA 8 spans both halves of the tensor-core CTA pair
+    (or both row groups of the single-CTA kernel)."""
+    G = case.num_q_heads // case.num_kv_heads
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b in range(case.batch):
+        g = int(rng.integers(case.num_kv_heads))
+        rows += [(b, g * G + hh, i) for hh in range(G) for i in range(case.block_len)]
+    return np.array(rows, dtype=np.int32)
+
+
+def check_rows(case, out, lse, rows, what):
+    ref_o, ref_l = oracle.block_attn_rows(case.q, case.k_cache, case.v_cache, case.page_table,
+                                          case.seq_lens, case.block_len, rows, causal=case.causal,
+                                          window=case.window, scale=case.scale)
+    idx = torch.tensor(rows[:, 0] * case.block_len + rows[:, 2], device=out.device, dtype=torch.long)
+    hh = torch.tensor(rows[:, 1], device=out.device, dtype=torch.long)
+    ta, tr = tols(case)
+    check_close(out[idx, hh], ref_o, ta, tr, f"{case.name} {what} out")
+    check_close(lse[idx, hh], ref_l, ta, tr, f"{case.name} {what} lse")
 
 
 def check_sampled(case, out, lse, per_request=6):
@@ -187,17 +240,65 @@ def test_batch_sweep_sampled(kernel, B):
     maybe_skip(case, kernel)
     out, lse = run(case, kernel=kernel)
     check_sampled(case, out, lse)
+    if B == 8:
+        check_rows(case, out, lse, group_rows(case, seed=B), "whole groups")
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_long_draft_split16_sampled(kernel):
+def test_long_draft_split16_groups(kernel):
     case = workloads.make_case("long_draft", device="cuda")
     maybe_skip(case, kernel)
     assert case.num_splits == 16
     out, lse = run(case, kernel=kernel)
     check_sampled(case, out, lse, per_request=4)
+    # one whole (request, KV head) group per request: 128 rows x 131072 keys each
+    check_rows(case, out, lse, group_rows(case, seed=5), "whole groups")
     del case
     torch.cuda.empty_cache()
+
+
+def test_cta_pair_agrees_with_the_single_cta_kernel():
+    # 8 heads x 16 positions at head_dim 512: one CTA pair per KV head, or two single-CTA row
+    # groups that both read the K/V
+    case = workloads.make_custom("pair_vs_tc", 2, 16, 32, 4, 512, [3000, 9000], seed=41, device="cuda")
+    dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
+    plan = dfl.plan_info(dims, case.block_len, 0, 0, "tc_pair")
+    assert plan["kernel_name"] == "tc_pair_attn_kernel" and not plan["balanced"]
+    assert plan["ctas"] == 2 * case.batch * case.num_kv_heads * plan["num_splits"]
+    out, lse = run(case, kernel="tc_pair", num_splits=0)
+    check_full(case, out, lse)
+    a, la = run(case, kernel="tc", num_splits=plan["num_splits"])
+    torch.testing.assert_close(out.float(), a.float(), atol=1e-2, rtol=1e-2)
+    torch.testing.assert_close(lse, la, atol=1e-3, rtol=1e-3)
+
+
+@pytest.mark.parametrize("T,Hq,Hkv,D", [(16, 16, 2, 512), (11, 16, 2, 256), (32, 16, 4, 256), (2, 8, 1, 512)])
+@pytest.mark.parametrize("causal,window", [(False, 0), (True, 0), (False, 700), (True, 300)])
+def test_cta_pair_shapes(T, Hq, Hkv, D, causal, window):
+    # odd and even blocks, GQA 4 and 8, both head dims, ragged key tails, every mask
+    if window and window < T:
+        pytest.skip("window shorter than the block")
+    case = workloads.make_custom("pair", 2, T, Hq, Hkv, D, [T + 5, 1337], causal=causal, window=window,
+                                 seed=43 + T + D, device="cuda")
+    maybe_skip(case, "tc_pair")
+    for splits in (1, 3):
+        out, lse = run(case, kernel="tc_pair", num_splits=splits)
+        check_full(case, out, lse)
+
+
+def test_cta_pair_garbage_beyond_seq_len_does_not_leak():
+    """The pair reads V of the last, partial page in both CTAs: NaN/Inf there must not leak."""
+    case = workloads.make_custom("pairnan", 2, 16, 16, 2, 512, [461, 790], seed=44, device="cuda")
+    ref_o, ref_l = oracle.block_attn(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens, 16,
+                                     scale=case.scale)
+    for b, L in enumerate(case.seq_lens_host()):
+        last = int(case.page_table[b, (L - 1) // 16])
+        case.k_cache[last, L % 16:] = float("nan")
+        case.v_cache[last, L % 16:] = float("inf")
+    for splits in (1, 2):
+        out, lse = run(case, kernel="tc_pair", num_splits=splits)
+        check_close(out, ref_o, BF16_TOL, BF16_TOL, "nan-poisoned pair out")
+        check_close(lse, ref_l, BF16_TOL, BF16_TOL, "nan-poisoned pair lse")
 
 
 # ----------------------------------------------------------------------------- exactness / invariants

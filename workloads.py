@@ -165,6 +165,8 @@ def _projected_kv(case: Case, hidden: int, seed: int, chunk: int = 16384) -> Non
                 case.v_cache[pages, pos % P] = vv
 
 
+LONG_DRAFT = dict(B=8, T=16, Hq=32, Hkv=4, D=512, L=131072, splits=16)
+
 CONFIG_NAMES = ["tiny", "global_verify", "batch_sweep_b1", "batch_sweep_b2", "batch_sweep_b4",
                 "batch_sweep_b8", "sliding", "sliding_causal", "long_draft"]
 
@@ -188,10 +190,48 @@ def make_case(name: str, device="cuda", layers: int = 1) -> Case:
                            pool_factor=1.0, layers=layers, window=1024,
                            causal=(name == "sliding_causal"), seed=1234 + 3, device=device)
     if name == "long_draft":
-        case = make_custom(name, 8, 16, 32, 4, 512, [131072] * 8, dtype=torch.bfloat16,
-                           pool_factor=1.0, layers=layers, seed=1234 + 4, device=device,
-                           num_splits=16)
+        sh = LONG_DRAFT
+        case = make_custom(name, sh["B"], sh["T"], sh["Hq"], sh["Hkv"], sh["D"], [sh["L"]] * sh["B"],
+                           dtype=torch.bfloat16, pool_factor=1.0, layers=layers, seed=1234 + 4, device=device,
+                           num_splits=sh["splits"])
         _projected_kv(case, hidden=5376, seed=1234 + 4)
         return case
     raise KeyError(name)
 
+
+
+def make_group_sample(name: str, keys: int, device="cpu", seed: int = 0) -> Case:
+    """One (request, KV head) group of a named workload, restricted to its last `keys` keys.
+
+    Same shapes per group (block_len, head_dim, the G query heads that share a KV head,
+    page size) and the same value distributions as make_case(name), at batch 1 with a single
+    KV head and seq_len = keys: what a CPU timing of the oracle on a bounded sample of that
+    workload needs, without generating the whole K/V pool. For long_draft the K/V rows are a
+    projection of N(0,1) hidden states of width 5376 through N(0, 0.02^2) weights of one head.
+    Only the non-causal global workloads (global_verify, batch_sweep_b*, long_draft) are
+    offered: their work is linear in the keys seen, so a sample scales to the full step.
+    """
+    shapes = {
+        "global_verify": dict(T=9, Hq=32, Hkv=4, D=512),
+        "long_draft": dict(T=16, Hq=32, Hkv=4, D=512),
+    }
+    if name.startswith("batch_sweep_b"):
+        shapes[name] = dict(T=9, Hq=32, Hkv=4, D=512)
+    sh = shapes[name]
+    G = sh["Hq"] // sh["Hkv"]
+    case = make_custom(name + "_group", 1, sh["T"], G, 1, sh["D"], [int(keys)], dtype=torch.bfloat16,
+                       pool_factor=1.0, seed=seed, device=device)
+    if name == "long_draft":
+        dev = case.q.device
+        gen = _gen(dev, seed + 7)
+        hidden, D, P = 5376, sh["D"], case.page_size
+        w_k = torch.randn((hidden, D), generator=gen, device=dev) * 0.02
+        w_v = torch.randn((hidden, D), generator=gen, device=dev) * 0.02
+        for t0 in range(0, int(keys), 4096):
+            t1 = min(int(keys), t0 + 4096)
+            h = torch.randn((t1 - t0, hidden), generator=gen, device=dev).to(torch.bfloat16).float()
+            pos = torch.arange(t0, t1, device=dev)
+            pages = case.page_table[0].long()[pos // P]
+            case.k_cache[pages, pos % P, 0] = (h @ w_k).to(torch.bfloat16)
+            case.v_cache[pages, pos % P, 0] = (h @ w_v).to(torch.bfloat16)
+    return case
