@@ -171,11 +171,14 @@ int choose_kernel(const dflash_dims* d, int32_t T, int32_t window, int32_t reque
     }
     if (requested != DFLASH_KERNEL_AUTO) return -DFLASH_ERR_INVALID_ARG;
     if (d->dtype != DFLASH_BF16) return DFLASH_KERNEL_SIMT;
-    // The packed rows of a KV head's query heads x block positions go to one CTA per tile
-    // (several row groups when they do not fit one); the CTA pair takes shapes the single-CTA
-    // kernel does not cover.
-    if (tc_supports(p)) return DFLASH_KERNEL_TC;
-    if (tc_pair_supports(p)) return DFLASH_KERNEL_TC_PAIR;
+    // The packed rows of a KV head's query heads x block positions go to one CTA when they fit
+    // its tile; when one CTA would need several row groups (each reading all of the K/V), the
+    // CTA pair takes them with fewer groups (8 heads x 16 positions at head_dim 512: one pair,
+    // every K/V byte read once, against two CTAs that each read it all).
+    const bool tc = tc_supports(p);
+    const bool pair = tc_pair_supports(p);
+    if (pair && (!tc || tc_pair_row_groups(p) < tc_row_groups(p))) return DFLASH_KERNEL_TC_PAIR;
+    if (tc) return DFLASH_KERNEL_TC;
     return DFLASH_KERNEL_SIMT;
 }
 
@@ -230,7 +233,14 @@ int32_t plan_splits_impl(const dflash_dims* d, int32_t T, int32_t window, int32_
     if (span / std::max<int64_t>(1, s) > kLongChunkKeys) s = (span + kTargetChunkKeys - 1) / kTargetChunkKeys;
     s = std::min<int64_t>(s, max_by_len);
     s = std::min<int64_t>(s, DFLASH_MAX_SPLITS);
-    return (int32_t)std::max<int64_t>(1, s);
+    s = std::max<int64_t>(1, s);
+    // Whole 128-key tiles per chunk: a chunk of 1.75 tiles costs its CTA a second, mostly
+    // empty tile (global_verify: 38 chunks of 224 keys against 32 of 256, which ran faster).
+    if (kernel == DFLASH_KERNEL_TC && s > 1) {
+        const int64_t chunk = ((span + s - 1) / s + 127) / 128 * 128;
+        s = std::max<int64_t>(1, (span + chunk - 1) / chunk);
+    }
+    return (int32_t)s;
 }
 
 }  // namespace

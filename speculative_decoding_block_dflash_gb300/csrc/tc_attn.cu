@@ -137,7 +137,9 @@ struct TcLayout {
     static constexpr int kAlloc = kTotal + 1024;
     static constexpr int kTmemUsed = 2 * N + (D / 128) * N + 16;        // S^T x 2, O^T, l^T
     static constexpr int kTmemCols = pow2ceil(kTmemUsed);
-    static_assert(kStages >= 3, "ring too shallow");
+    // each producer warp fills every kNumProducers-th stage; with fewer slots than producers
+    // a warp could pass a slot two phases ahead (the parity wait cannot tell them apart)
+    static_assert(kStages >= kNumProducers, "ring too shallow for the producer warps");
     static_assert(kOnesOff - kQOff >= N * D * 4, "output tile staging (Q, P and the ring)");
     static_assert(kPOff + kPBytes + N * 128 + 128 * 128 <= kOnesOff, "128-row P operand of the row-sum MMA");
     static_assert(kTmemUsed <= 512, "TMEM budget");
@@ -454,19 +456,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (with_q)
                                 for (int kc = 0; kc < KC; ++kc)
                                     tma_load_3d(q_s + kc * N * 128, &tm_q, fb, kc * 64, h0, b * T);
+                            // The stage's page ids go to registers before its copies are issued:
+                            // each copy instruction is also a compiler memory barrier, so reading
+                            // an id between two copies made every box wait for a shared-memory
+                            // load, which halved the rate at which a warp issues copies.
                             if (is_k) {
-                                for (int pg = 0; pg < pages_per_tile; ++pg)
-                                    tma_load_4d(dst + pg * box, &tm_k, fb, sq * 64, g, 0,
-                                                pid_w[rel0 + pg - wbase]);
+                                int32_t ids[8];
+#pragma unroll
+                                for (int pg = 0; pg < 8; ++pg)
+                                    ids[pg] = pg < pages_per_tile ? pid_w[rel0 + pg - wbase] : 0;
+#pragma unroll
+                                for (int pg = 0; pg < 8; ++pg)
+                                    if (pg < pages_per_tile)
+                                        tma_load_4d(dst + pg * box, &tm_k, fb, sq * 64, g, 0, ids[pg]);
                             } else {
                                 const int h = sq / VC, c = sq % VC;
                                 const int ppg = 64 / Psz;  // pages per 64-key half
-                                for (int pg = 0; pg < ppg; ++pg) {
-                                    const int32_t page = pid_w[rel0 + h * ppg + pg - wbase];
-                                    for (int m = 0; m < 2; ++m)
-                                        tma_load_4d(dst + m * 8192 + pg * box, &tm_v, fb, c * 128 + m * 64,
-                                                    g, 0, page);
-                                }
+                                int32_t ids[4];
+#pragma unroll
+                                for (int pg = 0; pg < 4; ++pg)
+                                    ids[pg] = pg < ppg ? pid_w[rel0 + h * ppg + pg - wbase] : 0;
+#pragma unroll
+                                for (int pg = 0; pg < 4; ++pg)
+                                    if (pg < ppg)
+#pragma unroll
+                                        for (int m = 0; m < 2; ++m)
+                                            tma_load_4d(dst + m * 8192 + pg * box, &tm_v, fb, c * 128 + m * 64,
+                                                        g, 0, ids[pg]);
                             }
                             if (sl.extra)
                                 issued_extra |= 1u << sl.idx;
@@ -618,6 +634,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ softmax warps 0-3 (thread = key lane)
         const float sl2 = p.scale * kLog2e;
         const bool plain = (p.causal == 0 && p.window == 0);
+        // A key inside every row's range [max lo, min hi] needs no test per row: with a window
+        // or the causal switch only a few keys (the window's first, the block's own) fall
+        // outside it, and the per-row test (two shared-memory reads per score) made the
+        // masked softmax several times slower than the plain one.
+        int lo_all = -(1 << 30), hi_all = (1 << 30);
+        if (!plain) {
+            for (int r = 0; r < N; ++r) {
+                lo_all = max(lo_all, lo_s[r]);
+                hi_all = min(hi_all, hi_s[r]);
+            }
+        }
         // P^T is MN-major with a 32-byte swizzle: per key half, 16-row groups (atoms) of
         // 2048 B = 8 key groups x (8 keys x 32 B); this key lane owns one 32-byte row of
         // every atom, the two 16-byte halves swapped for keys 4-7 of a group.
@@ -652,10 +679,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int key = t0 + j * kTileKeys + tid;
             const bool kvalid = !dry && key >= ch.kb && key < ch.ke;
+            const bool allvis = plain || (key >= lo_all && key <= hi_all);
             // masked, log2-scaled score of column col from raw S^T bits
             auto score = [&](uint32_t raw, int col) -> float {
                 bool vis = kvalid;
-                if (!plain) vis = vis && key >= lo_s[col] && key <= hi_s[col];
+                if (!allvis) vis = vis && key >= lo_s[col] && key <= hi_s[col];
                 return vis ? u2f(raw) * sl2 : -INFINITY;
             };
             // pass 1: does any score exceed the running max by more than the threshold?

@@ -29,14 +29,19 @@
 // The row maxima must agree across the pair: each CTA sends its 128 column maxima to the
 // other with asynchronous stores that count their bytes on the receiver's mbarrier, and both
 // take the same lazy update. Each CTA writes the P of rows 0-63 into the even CTA's P^T
-// buffer and of rows 64-127 into the odd CTA's (one half local, one half remote).
+// buffer and of rows 64-127 into the odd CTA's (one half local, one half remote). With one
+// P^T buffer, the ring order K(j+1) V(j) K(j+2) V(j+1) leaves the softmax of tile j+1 the whole
+// of S(j+2)'s K stream between PV(j) and PV(j+1) to write it, and the 32 KB of a second buffer
+// go to the ring.
 //
-// Roles (416 threads): warps 0-7 softmax (warps w and w+4 share TMEM lanes 32(w%4).., and take
-// the rows 0-63 and 64-127), then the epilogue; warps 8-11 TMA producers (whole 16 KB ring
-// stages dealt round-robin); warp 12 the MMA issuer in the even CTA, and in the odd CTA the
-// forwarder that tells the even CTA when each of its own stages has landed. Both CTAs fill
-// their rings in the same order K(0) K(1) V(0) K(2) V(1) ... so a stage sits at the same
-// offset in both, as the pair MMA needs.
+// Roles (384 threads): warps 0-7 softmax (warps w and w+4 share TMEM lanes 32(w%4).., and take
+// the rows 0-63 and 64-127), then the epilogue; warps 8-10 TMA producers (whole 16 KB ring
+// stages dealt round-robin); warp 11 the MMA issuer in the even CTA. (Three producer warps keep
+// the block at 384 threads, which leaves each softmax thread the registers for its 64 running
+// row sums.) Both CTAs fill their rings
+// in the same order K(0) K(1) V(0) K(2) V(1) ... so a stage sits at the same offset in both, as
+// the pair MMA needs, and both CTAs' copies of a stage count their bytes on one barrier in the
+// even CTA (the 2-CTA form of the tensor copy), which alone waits on it.
 //
 // Every wait is bounded (p.wait_ns); on expiry the kernel records DFLASH_DEVERR_TIMEOUT,
 // drains its own copies and MMAs, and both CTAs still meet at the final cluster barrier
@@ -54,17 +59,19 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 416;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
-constexpr int kNumProducers = 4;
-constexpr int kMmaWarp = 12;
+constexpr int kNumProducers = 3;
+constexpr int kMmaWarp = 11;
+constexpr int kPBufs = 1;       // P^T buffers (1: the 32 KB of a second one go to the ring)
 constexpr int kPairKeys = 256;  // keys per pair tile
 constexpr int kOwnKeys = 128;   // keys of a pair tile whose K this CTA streams
 constexpr int kHalf = 64;       // Q / P rows held per CTA
 constexpr int kN = 128;         // columns (packed rows) of S^T and O^T
 constexpr int kStageBytes = 16384;
 constexpr int kMaxPids = 128;
+constexpr unsigned long long kCopyGraceNs = 200000ull;  // after an abort: time for copies in flight to land
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;
@@ -90,14 +97,14 @@ struct PairLayout {
     static constexpr int kPQuarter = kHalf * 128;           // P^T of 64 keys x 64 rows
     static constexpr int kPBuf = 4 * kPQuarter;             // one pair tile
     static constexpr int kQOff = 0;
-    static constexpr int kPOff = kQOff + kQBytes;           // [2 buffers][4 quarters][4 atoms][2 KB]
-    static constexpr int kRingOff = kPOff + 2 * kPBuf;
+    static constexpr int kPOff = kQOff + kQBytes;           // [kPBufs][4 quarters][4 atoms][2 KB]
+    static constexpr int kRingOff = kPOff + kPBufs * kPBuf;
     static constexpr int kSmallBytes = 12288;               // barriers, tables
     static constexpr int kStagesFit = (227 * 1024 - 1024 - kRingOff - kSmallBytes) / kStageBytes;
     static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
     static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-    // barriers: full[S] empty[S] pfull[S] s_full[2] p_full p_free[2] px_full[2] lx_full drain
-    static constexpr int kNumBars = 3 * kStages + 9;
+    // barriers: full[S] empty[S] s_full[2] p_full p_free[kPBufs] nf_full[2] px_full[2] lx_full drain
+    static constexpr int kNumBars = 2 * kStages + 9 + kPBufs;
     static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;  // tmem base, abort flag
     static constexpr int kMOff = kMiscOff + 16;             // float m_s[128]
     static constexpr int kAOff = kMOff + kN * 4;            // float a_s[128] (1/l at the end)
@@ -105,7 +112,8 @@ struct PairLayout {
     static constexpr int kSumOff = kRedOff + 8 * 64 * 4;    // float red2[8 warps][64]: column sums of P
     static constexpr int kLaccOff = kSumOff + 8 * 64 * 4;   // float l_acc[128]: this CTA's keys' row sums
     static constexpr int kPxOff = kLaccOff + kN * 4;        // float px[2][128]: the peer's maxima
-    static constexpr int kLxOff = kPxOff + 2 * kN * 4;      // float lx[128]: the peer's row sums
+    static constexpr int kNfOff = kPxOff + 2 * kN * 4;      // float nflag[2] (16 B): the peer's flags
+    static constexpr int kLxOff = kNfOff + 16;              // float lx[128]: the peer's row sums
     static constexpr int kLoOff = kLxOff + kN * 4;          // int lo_s[128]
     static constexpr int kHiOff = kLoOff + kN * 4;          // int hi_s[128]
     static constexpr int kRowOff = kHiOff + kN * 4;         // int64 orow_s[128]
@@ -114,7 +122,9 @@ struct PairLayout {
     static constexpr int kAlloc = kTotal + 1024;
     static constexpr int kTmemUsed = 2 * kN + VC2 * kN;     // S^T x 2, O^T chunks
     static constexpr int kTmemCols = pair_pow2ceil(kTmemUsed);
-    static_assert(kStages >= 4, "ring too shallow");
+    // each producer warp fills every kNumProducers-th stage; with fewer slots than producers
+    // a warp could pass a slot two phases ahead (the parity wait cannot tell them apart)
+    static_assert(kStages >= kNumProducers, "ring too shallow for the producer warps");
     static_assert(kTotal - kBarOff <= kSmallBytes, "small tables");
     static_assert(kTotal + 1024 <= 227 * 1024, "shared memory budget");
     static_assert(kTmemUsed <= 512, "TMEM budget");
@@ -202,15 +212,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* q_s = smem + Lay::kQOff;
     uint8_t* ring = smem + Lay::kRingOff;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
-    uint64_t* full = bars;            // [S] own TMA landed
+    uint64_t* full = bars;            // [S] even CTA: both CTAs' copies of the stage have landed
     uint64_t* empty = bars + S;       // [S] the pair MMAs reading the slot are done (both CTAs)
-    uint64_t* pfull = bars + 2 * S;   // [S] even CTA only: the odd CTA's stage has landed
-    uint64_t* s_full = bars + 3 * S;  // [2] S^T of tile j is in TMEM buffer j mod 2 (both CTAs)
-    uint64_t* p_full = s_full + 2;    // even CTA: both CTAs wrote P (16 warp arrivals)
-    uint64_t* p_free = s_full + 3;    // [2] PV of the tile done: P^T buffer free, O^T final for it
-    uint64_t* px_full = s_full + 5;   // [2] the peer's 128 column maxima have landed (512 bytes)
-    uint64_t* lx_full = s_full + 7;   // the peer's 128 row sums have landed (512 bytes)
-    uint64_t* drain = s_full + 8;
+    uint64_t* s_full = bars + 2 * S;  // [2] S^T of tile j is in TMEM buffer j mod 2 (both CTAs)
+    uint64_t* p_full = s_full + 2;    // even CTA: both CTAs wrote P (one arrival each)
+    uint64_t* p_free = s_full + 3;    // [kPBufs] PV of tile j done: P^T buffer j mod kPBufs is free
+    uint64_t* nf_full = p_free + kPBufs;  // [2] the peer's "raise the maxima" flag of the tile (4 bytes)
+    uint64_t* px_full = nf_full + 2;  // [2] the peer's 128 column maxima have landed (512 bytes)
+    uint64_t* lx_full = nf_full + 4;  // the peer's 128 row sums have landed (512 bytes)
+    uint64_t* drain = nf_full + 5;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
     float* m_s = reinterpret_cast<float*>(smem + Lay::kMOff);
@@ -220,6 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* l_acc = reinterpret_cast<float*>(smem + Lay::kLaccOff);
     float* px = reinterpret_cast<float*>(smem + Lay::kPxOff);
     float* lx = reinterpret_cast<float*>(smem + Lay::kLxOff);
+    float* nflag = reinterpret_cast<float*>(smem + Lay::kNfOff);
     int32_t* lo_s = reinterpret_cast<int32_t*>(smem + Lay::kLoOff);
     int32_t* hi_s = reinterpret_cast<int32_t*>(smem + Lay::kHiOff);
     int64_t* orow_s = reinterpret_cast<int64_t*>(smem + Lay::kRowOff);
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int first_page = t0 / Psz;
 
     const int pw = warp - kProducerWarp;
-    int32_t* pid_w = pid_s + (pw & 3) * kMaxPids;
+    int32_t* pid_w = pid_s + (pw >= 0 && pw < kNumProducers ? pw : 0) * kMaxPids;
     auto load_window = [&](int base) {
         for (int k = lane; k < kMaxPids; k += 32) {
             const int pr = base + k;
@@ -275,13 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < S; ++i) {
             mbar_init(full + i, 1);
             mbar_init(empty + i, 1);
-            mbar_init(pfull + i, 1);
         }
         mbar_init(s_full, 1);
         mbar_init(s_full + 1, 1);
-        mbar_init(p_full, 16);
-        mbar_init(p_free, 1);
-        mbar_init(p_free + 1, 1);
+        mbar_init(p_full, 2);
+        for (int i = 0; i < kPBufs; ++i) mbar_init(p_free + i, 1);
+        mbar_init(nf_full, 1);
+        mbar_init(nf_full + 1, 1);
         mbar_init(px_full, 1);
         mbar_init(px_full + 1, 1);
         mbar_init(lx_full, 1);
@@ -290,6 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         // the exchange barriers of tiles 0 and 1 and of the row sums expect the peer's bytes
+        mbar_expect_tx(nf_full, 4);
+        mbar_expect_tx(nf_full + 1, 4);
         mbar_expect_tx(px_full, kN * 4);
         mbar_expect_tx(px_full + 1, kN * 4);
         mbar_expect_tx(lx_full, kN * 4);
@@ -349,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
         // ------------------------------------------------------------ TMA producers
+        const uint32_t full0 = in_cta(full, 0);
         bool ok = true;
         int wbase = 0;
         uint32_t issued_parity[S];
@@ -363,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pair_ring_unit(k, ntiles, is_k, tile);
                 const int n_st = is_k ? KC : 4 * VC2;
                 for (int sq = 0; sq < n_st && ok; ++sq, ++seq) {
-                    if ((seq & 3) != pw) continue;
+                    if (seq % kNumProducers != pw) continue;
                     // relative pages this stage reads: K: own 128 keys; V: quarter of 64 keys
                     const int rel0 = tile * pages_per_tile +
                                      (is_k ? (int)rank * (kOwnKeys / Psz) : (sq / VC2) * (64 / Psz));
@@ -374,31 +388,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const int slot = seq % S;
                     const uint32_t ph = (uint32_t)((seq / S) & 1);
-                    if (lane == 0) ok = ring_wait_cluster(empty + slot, ph ^ 1u, abort_flag, p.err, p.wait_ns);
+                    // a polling wait with a short sleep between polls: producers spinning flat out
+                    // beside the softmax warps slow it down, and a suspending wait wakes late
+                    if (lane == 0) ok = backoff_wait(empty + slot, ph ^ 1u, abort_flag, p.err, p.wait_ns);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     if (lane == 0) {
                         uint8_t* dst = ring + slot * kStageBytes;
                         const bool with_q = (seq == 0);
-                        mbar_expect_tx(full + slot,
-                                       kStageBytes + (with_q ? (uint32_t)(x.Gc * x.Tb * 128 * KC) : 0u));
+                        // the even CTA expects both CTAs' bytes of the stage on its barrier
+                        const uint32_t qbytes = with_q ? (uint32_t)(x.Gc * x.Tb * 128 * KC) : 0u;
+                        if (leader) mbar_expect_tx(full + slot, 2u * (kStageBytes + qbytes));
+                        const uint32_t fb = full0 + (uint32_t)(slot * 8);
                         if (with_q)
                             for (int kc = 0; kc < KC; ++kc)
-                                tma_load_3d(q_s + kc * kHalf * 128, &tm_q, full + slot, kc * 64, h0,
-                                            b * T + (int)rank * x.Tb);
+                                tma_load_3d_pair(q_s + kc * kHalf * 128, &tm_q, fb, kc * 64, h0,
+                                                 b * T + (int)rank * x.Tb);
+                        // the stage's page ids go to registers before its copies are issued (each
+                        // copy instruction is also a compiler memory barrier)
+                        int32_t ids[8];
+#pragma unroll
+                        for (int pg = 0; pg < 8; ++pg) ids[pg] = pg < npg ? pid_w[rel0 + pg - wbase] : 0;
                         if (is_k) {
-                            for (int pg = 0; pg < npg; ++pg)
-                                tma_load_4d(dst + pg * box, &tm_k, full + slot, sq * 64, g, 0,
-                                            pid_w[rel0 + pg - wbase]);
+#pragma unroll
+                            for (int pg = 0; pg < 8; ++pg)
+                                if (pg < npg) tma_load_4d_pair(dst + pg * box, &tm_k, fb, sq * 64, g, 0, ids[pg]);
                         } else {
                             const int c = sq % VC2;
                             const int d0 = c * 256 + (int)rank * 128;
-                            for (int pg = 0; pg < npg; ++pg) {
-                                const int32_t page = pid_w[rel0 + pg - wbase];
-                                for (int m = 0; m < 2; ++m)
-                                    tma_load_4d(dst + m * 8192 + pg * box, &tm_v, full + slot, d0 + m * 64, g, 0,
-                                                page);
-                            }
+#pragma unroll
+                            for (int pg = 0; pg < 4; ++pg)
+                                if (pg < npg)
+#pragma unroll
+                                    for (int m = 0; m < 2; ++m)
+                                        tma_load_4d_pair(dst + m * 8192 + pg * box, &tm_v, fb, d0 + m * 64, g, 0,
+                                                         ids[pg]);
                         }
                         issued_parity[slot] = ph;
                     }
@@ -407,58 +431,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (lane == 0 && !ok) {
-            for (int s = 0; s < S; ++s) {
-                if (issued_parity[s] > 1) continue;
-                const unsigned long long t_start = globaltimer();
-                while (!mbar_try_wait(full + s, issued_parity[s]) && globaltimer() - t_start < p.wait_ns) {
+            // Copies of ours may still be landing. The even CTA waits for the stages it armed;
+            // both CTAs then give copies in flight a grace period (a copy lands within
+            // microseconds while the memory system works) before this CTA may leave.
+            if (leader) {
+                for (int s = 0; s < S; ++s) {
+                    if (issued_parity[s] > 1) continue;
+                    const unsigned long long t_start = globaltimer();
+                    while (!mbar_try_wait(full + s, issued_parity[s]) && globaltimer() - t_start < p.wait_ns) {
+                    }
                 }
+            }
+            const unsigned long long t_start = globaltimer();
+            while (globaltimer() - t_start < kCopyGraceNs) {
             }
         }
         __syncwarp();
         role_ok = ok;
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer (even) / forwarder (odd)
+        // ------------------------------------------------------------ MMA issuer (even CTA)
         bool ok = true;
         int seq = 0;
-        // V rows past seq_len in the sequence's last, partial page are zeroed before PV (the
-        // zero probabilities there must not meet non-finite garbage)
-        auto zero_tail = [&](int tile, int q, uint8_t* st) {
+        // V rows past seq_len in the sequence's last, partial page are zeroed before PV in both
+        // CTAs' copies of the stage (the zero probabilities there must not meet non-finite
+        // garbage); the peer's copy through distributed shared memory
+        auto zero_tail = [&](int tile, int q, uint32_t st_off) {
             const int key0 = t0 + tile * kPairKeys + q * 64;
             const int zlo = L - key0;
             if (L % Psz != 0 && zlo > 0 && zlo < 64 && ch.ke == L) {
                 const int zhi = min(64, ((L + Psz - 1) / Psz) * Psz - key0);
                 const int rows = zhi - zlo;
+                const uint32_t peer_st = in_cta(smem + st_off, peer);
                 for (int idx = lane; idx < rows * 16; idx += 32) {
                     const int m = idx / (rows * 8);
                     const int rem = idx - m * rows * 8;
-                    *reinterpret_cast<uint4*>(st + m * 8192 + (zlo + rem / 8) * 128 + (rem % 8) * 16) =
-                        make_uint4(0, 0, 0, 0);
+                    const uint32_t off = (uint32_t)(m * 8192 + (zlo + rem / 8) * 128 + (rem % 8) * 16);
+                    *reinterpret_cast<uint4*>(smem + st_off + off) = make_uint4(0, 0, 0, 0);
+                    st_cluster_v4(peer_st + off, make_uint4(0, 0, 0, 0));
                 }
-                fence_proxy_async_smem();
+                fence_proxy_async_cluster();
             }
             __syncwarp();
         };
         if (!leader) {
-            // forwarder: each own stage, once landed (and its V tail zeroed), is announced to the
-            // even CTA, whose MMAs read it
-            const uint32_t pfull0 = in_cta(pfull, 0);
-            for (int k = 0; k < 2 * ntiles && ok; ++k) {
-                bool is_k;
-                int tile;
-                pair_ring_unit(k, ntiles, is_k, tile);
-                const int n_st = is_k ? KC : 4 * VC2;
-                for (int sq = 0; sq < n_st && ok; ++sq, ++seq) {
-                    const int slot = seq % S;
-                    bool got = true;
-                    if (lane == 0)
-                        got = ring_wait(full + slot, (uint32_t)((seq / S) & 1), abort_flag, p.err, p.wait_ns);
-                    ok = __shfl_sync(0xffffffffu, got, 0);
-                    if (!ok) break;
-                    if (!is_k) zero_tail(tile, sq / VC2, ring + slot * kStageBytes);
-                    if (lane == 0) mbar_arrive_cluster(pfull0 + (uint32_t)(slot * 8));
-                    __syncwarp();
-                }
-            }
+            // the odd CTA's MMA warp has no role: the even CTA issues the pair MMAs
         } else {
             constexpr uint32_t idesc_s = make_idesc(256, kN, 0, 0);  // S^T  = K . Q^T
             constexpr uint32_t idesc_o = make_idesc(256, kN, 1, 1);  // O^T += V^T . P^T
@@ -470,12 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) got = ring_wait_cluster(bar, par, abort_flag, p.err, p.wait_ns);
                 return __shfl_sync(0xffffffffu, got, 0);
             };
-            // both CTAs' copies of the next stage have landed
+            // both CTAs' copies of the next stage have landed (one barrier counts both)
             auto next_stage = [&](uint32_t& addr, int& slot) -> bool {
                 slot = seq % S;
                 const uint32_t ph = (uint32_t)((seq / S) & 1);
-                bool got = wait_lane0(full + slot, ph);
-                if (got) got = wait_lane0(pfull + slot, ph);
+                const bool got = wait_lane0(full + slot, ph);
                 addr = ring_addr + slot * kStageBytes;
                 return got;
             };
@@ -515,14 +530,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = wait_lane0(p_full, (uint32_t)(j & 1));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t pb_addr = p_addr + (uint32_t)(j & 1) * Lay::kPBuf;
+                const uint32_t pb_addr = p_addr + (uint32_t)((j % kPBufs) * Lay::kPBuf);
                 for (int q = 0; q < 4 && ok; ++q) {
                     for (int c = 0; c < VC2 && ok; ++c) {
                         uint32_t st;
                         int slot;
                         ok = next_stage(st, slot);
                         if (!ok) break;
-                        zero_tail(j, q, smem + (st - smem_u32(smem)));
+                        zero_tail(j, q, st - smem_u32(smem));
                         tc_fence_after();
                         if (lane == 0) {
 #pragma unroll
@@ -535,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (lane == 0) tc_commit2_both(p_free + (j & 1));
+                if (lane == 0) tc_commit2_both(p_free + j % kPBufs);
                 __syncwarp();
             }
             // drain our MMAs before either CTA frees TMEM or leaves (they read both CTAs' memory)
@@ -552,6 +567,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ softmax (warps 0-7)
         const float sl2 = p.scale * kLog2e;
         const bool plain = (p.causal == 0 && p.window == 0);
+        // a key inside every row's range [max lo, min hi] needs no test per row
+        int lo_all = -(1 << 30), hi_all = (1 << 30);
+        if (!plain) {
+            for (int r = 0; r < kN; ++r) {
+                lo_all = max(lo_all, lo_s[r]);
+                hi_all = min(hi_all, hi_s[r]);
+            }
+        }
         const int kl = tid & 127;         // key lane of this CTA's 128 keys (TMEM lane)
         const int chh = tid >> 7;         // rows [64 chh, 64 chh + 64): the P^T buffer of CTA chh
         const int col0 = chh * kHalf;
@@ -564,23 +587,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t pswz0 = (uint32_t)((0 ^ (kig >> 2)) << 4);
         const uint32_t pswz1 = (uint32_t)((1 ^ (kig >> 2)) << 4);
         const bool p_local = (chh == (int)rank);
-        const uint32_t p_base = p_local ? smem_u32(smem) : mapa_shared(smem_u32(smem), (uint32_t)chh);
+        const uint32_t prow0 = (p_local ? smem_u32(smem) : mapa_shared(smem_u32(smem), (uint32_t)chh)) + prow_off;
         const uint32_t p_full_bar = in_cta(p_full, 0);
         bool ok = true;
+        int nx = 0;     // maxima exchanges so far (they happen only on tiles that raise a row max)
+        float lp[64];   // this key lane's share of the 64 rows' sums, over all tiles so far
+#pragma unroll
+        for (int u = 0; u < 64; ++u) lp[u] = 0.f;
         auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool got = true;
             if (tid == 0) got = ring_wait_cluster(bar, parity, abort_flag, p.err, p.wait_ns);
             return !bar_or_256(!got);
         };
-        // column sums of a finished tile (over this CTA's 128 keys) into l_acc, after the old
-        // sums were scaled by that tile's rescale factor (threads 0-127, one column each)
-        auto fold_sums = [&]() {
-            if (tid < kN) {
-                const int hc = tid >> 6, cl = tid & 63;
-                const float s4 = (red2[(hc * 4 + 0) * 64 + cl] + red2[(hc * 4 + 1) * 64 + cl]) +
-                                 (red2[(hc * 4 + 2) * 64 + cl] + red2[(hc * 4 + 3) * 64 + cl]);
-                l_acc[tid] = l_acc[tid] * a_s[tid] + s4;
-            }
+        // PV of tile t done (its P^T buffer is free and O^T holds every tile up to t)
+        auto wait_pv = [&](int t) -> bool {
+            return group_wait(p_free + t % kPBufs, (uint32_t)((t / kPBufs) & 1));
         };
         for (int j = 0; j < ntiles && ok; ++j) {
             if (!group_wait(s_full + (j & 1), (uint32_t)((j >> 1) & 1))) {
@@ -591,93 +612,121 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sb = tmem_s + (uint32_t)(j & 1) * kN + lane_base + (uint32_t)col0;
             const int key = t0 + j * kPairKeys + pk;
             const bool kvalid = key >= ch.kb && key < ch.ke;
+            const bool allvis = plain || (key >= lo_all && key <= hi_all);
             auto score = [&](uint32_t raw, int col) -> float {
                 bool vis = kvalid;
-                if (!plain) vis = vis && key >= lo_s[col] && key <= hi_s[col];
+                if (!allvis) vis = vis && key >= lo_s[col] && key <= hi_s[col];
                 return vis ? u2f(raw) * sl2 : -INFINITY;
             };
-            // pass 1: this warp's column maxima over its 32 keys, one column per lane
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                uint32_t r16[16];
-                load16(sb + q * 16, r16);
-                float v[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) v[u] = score(r16[u], col0 + q * 16 + u);
-                const float mx = pair_transpose_max16(v, lane);
-                if (lane < 16) red[warp * 64 + q * 16 + lane] = mx;
-            }
-            bar_sync_256();
-            float mloc = -INFINITY;
-            // the previous tile's sums are final now (its rescale factor is still in a_s)
-            if (j > 0) fold_sums();
-            if (tid < kN) {
-                // column tid over this CTA's 128 keys: warps hc*4 .. hc*4+3 of the rows' half
-                const int hc = tid >> 6, cl = tid & 63;
-                mloc = fmaxf(fmaxf(red[(hc * 4 + 0) * 64 + cl], red[(hc * 4 + 1) * 64 + cl]),
-                             fmaxf(red[(hc * 4 + 2) * 64 + cl], red[(hc * 4 + 3) * 64 + cl]));
-                st_async_f32(in_cta(px + (j & 1) * kN + tid, peer), mloc, in_cta(px_full + (j & 1), peer));
-            }
-            // the peer's maxima of the same columns: both CTAs then take the same lazy update
-            if (!group_wait(px_full + (j & 1), (uint32_t)((j >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            bool need = false;
-            if (tid < kN) {
-                const float mx = fmaxf(mloc, px[(j & 1) * kN + tid]);
-                const float mo = m_s[tid];
-                if (mx > mo + kRescaleThresh) {
-                    m_s[tid] = mx;
-                    a_s[tid] = (mo == -INFINITY) ? 0.f : ex2(mo - mx);
-                    need = true;
-                } else {
-                    a_s[tid] = 1.f;
-                }
-            }
-            need = bar_or_256(need);
-            // px of this tile has been read by everyone: expect the peer's maxima of tile j + 2
-            if (tid == 0) mbar_expect_tx(px_full + (j & 1), kN * 4);
-            if (j > 0 && need) {
-                // O^T holds tiles < j once PV(j-1) is done: rescale it in TMEM
-                if (!group_wait(p_free + ((j - 1) & 1), (uint32_t)(((j - 1) >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                constexpr int nsplit = 2 / VC2;  // warps w and w+4: one chunk each, or half the columns
-                const int c = (warp >> 2) % VC2;
-#pragma unroll 1
-                for (int q = (warp >> 2) / VC2; q < kN / 16; q += nsplit) {
-                    uint32_t r16[16];
-                    const uint32_t ta = tmem_o + c * kN + lane_base + q * 16;
-                    load16(ta, r16);
-                    float av[16];
-                    load_row16(a_s + q * 16, av);
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * av[u]);
-                    tmem_st16(ta, r16);
-                }
-                tmem_st_wait();
-            }
-            if (j > 1) {
-                if (!group_wait(p_free + (j & 1), (uint32_t)(((j - 2) >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
-            // pass 2: P = exp2(s - m) as bf16 pairs into the P^T buffer (j mod 2) of CTA chh,
-            // and this warp's column sums of the rounded P
-            const uint32_t prow = p_base + prow_off + (uint32_t)((j & 1) * Lay::kPBuf);
+            // pass 1: does any score of this CTA exceed its row's running max by more than the
+            // threshold? Both CTAs exchange the answer (one word); only when either says yes
+            // do they form and exchange the column maxima, so both take the same update.
+            bool nd = false;
 #pragma unroll 1
             for (int q = 0; q < 4; ++q) {
                 float mv[16];
                 load_row16(m_s + col0 + q * 16, mv);
                 uint32_t r16[16];
                 load16(sb + q * 16, r16);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) nd |= score(r16[u], col0 + q * 16 + u) > mv[u] + kRescaleThresh;
+            }
+            nd = bar_or_256(nd);
+            if (tid == 0) st_async_f32(in_cta(nflag + (j & 1), peer), nd ? 1.f : 0.f, in_cta(nf_full + (j & 1), peer));
+            if (!group_wait(nf_full + (j & 1), (uint32_t)((j >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            const bool need = nd || nflag[j & 1] != 0.f;
+            // the flag of tile j has been read: expect the peer's flag of tile j + 2
+            if (tid == 0) mbar_expect_tx(nf_full + (j & 1), 4);
+            if (need) {
+                // column maxima over this warp's 32 keys (transposing shuffle reduction), then
+                // over this CTA's 128 keys, then with the peer's
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t r16[16];
+                    load16(sb + q * 16, r16);
+                    float v[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) v[u] = score(r16[u], col0 + q * 16 + u);
+                    const float mx = pair_transpose_max16(v, lane);
+                    if (lane < 16) red[warp * 64 + q * 16 + lane] = mx;
+                }
+                bar_sync_256();
+                float mloc = -INFINITY;
+                if (tid < kN) {
+                    const int hc = tid >> 6, cl = tid & 63;
+                    mloc = fmaxf(fmaxf(red[(hc * 4 + 0) * 64 + cl], red[(hc * 4 + 1) * 64 + cl]),
+                                 fmaxf(red[(hc * 4 + 2) * 64 + cl], red[(hc * 4 + 3) * 64 + cl]));
+                    st_async_f32(in_cta(px + (nx & 1) * kN + tid, peer), mloc, in_cta(px_full + (nx & 1), peer));
+                }
+                if (!group_wait(px_full + (nx & 1), (uint32_t)((nx >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                if (tid < kN) {
+                    const float mx = fmaxf(mloc, px[(nx & 1) * kN + tid]);
+                    const float mo = m_s[tid];
+                    if (mx > mo + kRescaleThresh) {
+                        m_s[tid] = mx;
+                        a_s[tid] = (mo == -INFINITY) ? 0.f : ex2(mo - mx);
+                    } else {
+                        a_s[tid] = 1.f;
+                    }
+                }
+                bar_sync_256();
+                // px of this exchange has been read: expect the peer's maxima of exchange nx + 2
+                if (tid == 0) mbar_expect_tx(px_full + (nx & 1), kN * 4);
+                ++nx;
+                // the row sums so far follow the new maxima
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float av[16];
+                    load_row16(a_s + col0 + q * 16, av);
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) lp[q * 16 + u] *= av[u];
+                }
+                if (j > 0) {
+                    // O^T holds tiles < j once PV(j-1) is done: rescale it in TMEM
+                    if (!wait_pv(j - 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    constexpr int nsplit = 2 / VC2;  // warps w and w+4: one chunk each, or half the columns
+                    const int c = (warp >> 2) % VC2;
+#pragma unroll 1
+                    for (int q = (warp >> 2) / VC2; q < kN / 16; q += nsplit) {
+                        uint32_t r16[16];
+                        const uint32_t ta = tmem_o + c * kN + lane_base + q * 16;
+                        load16(ta, r16);
+                        float av[16];
+                        load_row16(a_s + q * 16, av);
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * av[u]);
+                        tmem_st16(ta, r16);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            if (j >= kPBufs) {
+                // the P^T buffer of tile j: PV(j - kPBufs) must have read it
+                if (!wait_pv(j - kPBufs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            // pass 2: P = exp2(s - m) as bf16 pairs into the P^T buffer of CTA chh, and the
+            // rounded P (what the PV MMA reads) into this key lane's row sums
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float mv[16];
+                load_row16(m_s + col0 + q * 16, mv);
+                uint32_t r16[16];
+                load16(sb + q * 16, r16);
                 uint32_t pk2[8];
-                float pv[16];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const float s0 = score(r16[2 * u], col0 + q * 16 + 2 * u);
@@ -686,10 +735,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float e1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - mv[2 * u + 1]);
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
                     pk2[u] = *reinterpret_cast<const uint32_t*>(&h2);
-                    pv[2 * u] = __low2float(h2);
-                    pv[2 * u + 1] = __high2float(h2);
+                    lp[q * 16 + 2 * u] += __low2float(h2);
+                    lp[q * 16 + 2 * u + 1] += __high2float(h2);
                 }
-                const uint32_t dst = prow + (uint32_t)(q * 2048);
+                const uint32_t dst = prow0 + (uint32_t)((j % kPBufs) * Lay::kPBuf + q * 2048);
                 const uint4 lo4 = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
                 const uint4 hi4 = make_uint4(pk2[4], pk2[5], pk2[6], pk2[7]);
                 if (p_local) {
@@ -700,19 +749,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st_cluster_v4(dst + pswz0, lo4);
                     st_cluster_v4(dst + pswz1, hi4);
                 }
-                const float sm = pair_transpose_sum16(pv, lane);
-                if (lane < 16) red2[warp * 64 + q * 16 + lane] = sm;
             }
+            // every thread's P stores (own and peer CTA) are made visible to the tensor cores,
+            // and its TMEM reads are ordered before the next MMAs; one thread of each CTA then
+            // tells the even CTA
             fence_proxy_async_cluster();
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(p_full_bar);
+            bar_sync_256();
+            if (tid == 0) mbar_arrive_cluster(p_full_bar);
         }
-        // the last tile's sums
+        // the row sums over this CTA's keys: across the 32 keys of each warp (transposing
+        // shuffle reduction), then across the 4 warps of each half of the rows
+        if (ok && ntiles > 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) v[u] = lp[q * 16 + u];
+                const float sm = pair_transpose_sum16(v, lane);
+                if (lane < 16) red2[warp * 64 + q * 16 + lane] = sm;
+            }
+        }
         bar_sync_256();
-        if (ok && ntiles > 0) fold_sums();
+        if (ok && ntiles > 0 && tid < kN) {
+            const int hc = tid >> 6, cl = tid & 63;
+            l_acc[tid] = (red2[(hc * 4 + 0) * 64 + cl] + red2[(hc * 4 + 1) * 64 + cl]) +
+                         (red2[(hc * 4 + 2) * 64 + cl] + red2[(hc * 4 + 3) * 64 + cl]);
+        }
         bool good = ok && ntiles > 0;
-        if (good) good = group_wait(p_free + ((ntiles - 1) & 1), (uint32_t)(((ntiles - 1) >> 1) & 1));
+        if (good) good = wait_pv(ntiles - 1);
         role_ok = good;
     }
 

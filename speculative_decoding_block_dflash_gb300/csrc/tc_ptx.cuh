@@ -110,6 +110,28 @@ __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Bounded wait that polls the non-suspending test_wait with a short sleep between polls: it
+// reacts within a fraction of a microsecond without taking the issue slots and the shared-
+// memory pipe from busy warps of the same SM.
+__device__ __forceinline__ bool backoff_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err,
+                                             unsigned long long limit)
+{
+    if (mbar_test_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (;;) {
+        for (int k = 0; k < 8; ++k) {
+            __nanosleep(64);
+            if (mbar_test_wait(bar, parity)) return true;
+        }
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > limit) {
+            *abort_flag = 1;
+            raise_error(err, DFLASH_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -449,6 +471,29 @@ __device__ __forceinline__ void tc_commit2_local(uint64_t* bar)
 {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// Tensor copies of a CTA pair: the destination is this CTA's shared memory, and the bytes are
+// counted on an mbarrier given by its cluster address, which may be the even CTA's (so one
+// barrier in the even CTA tracks both CTAs' halves of a stage).
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, uint32_t mbar_cluster, int c0,
+                                                 int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* map, uint32_t mbar_cluster, int c0,
+                                                 int c1, int c2, int c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
 }
 
 // Generic stores into the peer CTA's shared memory (cluster addresses from mapa_shared).

@@ -258,10 +258,11 @@ def test_long_draft_split16_groups(kernel):
 
 
 def test_cta_pair_agrees_with_the_single_cta_kernel():
-    # 8 heads x 16 positions at head_dim 512: one CTA pair per KV head, or two single-CTA row
-    # groups that both read the K/V
+    # 8 heads x 16 positions at head_dim 512: one CTA pair per KV head (AUTO's choice), or two
+    # single-CTA row groups that both read the K/V
     case = workloads.make_custom("pair_vs_tc", 2, 16, 32, 4, 512, [3000, 9000], seed=41, device="cuda")
     dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
+    assert dfl.plan_info(dims, case.block_len, 0, 0, "auto")["kernel_name"] == "tc_pair_attn_kernel"
     plan = dfl.plan_info(dims, case.block_len, 0, 0, "tc_pair")
     assert plan["kernel_name"] == "tc_pair_attn_kernel" and not plan["balanced"]
     assert plan["ctas"] == 2 * case.batch * case.num_kv_heads * plan["num_splits"]
@@ -486,6 +487,8 @@ def test_auto_plan_spreads_long_spans_over_waves():
     # up to 32768 keys over 8 requests keeps the one-wave length-balanced plan
     sweep = _plan_dims(8, 9, 32, 4, 512, 16, 32768 // 16)
     assert dfl.plan_splits(sweep, 9, 0, 0, "tc") == sms // 4
-    # one request of 8192 keys: one wave of 38 chunks on 152 SMs
+    # one request of 8192 keys: one wave (38 chunks on 152 SMs), each chunk rounded up to whole
+    # 128-key tiles (256 keys), which leaves 32 chunks
     one = _plan_dims(1, 9, 32, 4, 512, 16, 8192 // 16)
-    assert dfl.plan_splits(one, 9, 0, 0, "tc") == sms // 4
+    chunk = -(-(-(-8192 // (sms // 4))) // 128) * 128
+    assert dfl.plan_splits(one, 9, 0, 0, "tc") == -(-8192 // chunk)
