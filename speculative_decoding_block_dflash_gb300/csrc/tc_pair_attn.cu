@@ -21,9 +21,9 @@
 // so CTA r's TMEM holds two S^T buffers of its 128 keys for all rows (S of tile j+1 is computed
 // while the softmax of tile j runs) and O^T of its 128 dims of every chunk for all rows:
 // 2*128 + (D/256)*128 = 512 columns at D = 512. The row sums l do not fit TMEM as well, so
-// the softmax forms them on the CUDA cores from the same bf16-rounded P the MMA reads (a
-// transposing shuffle reduction per 16 columns), each CTA over its own keys; the two partial
-// sums are added once at the end.
+// the softmax forms them on the CUDA cores from the same bf16-rounded P the MMA reads: per
+// tile and 16 columns, a transposing shuffle reduction over the warp's 32 keys, kept in four
+// registers per lane; the warps' and the two CTAs' partial sums are added once at the end.
 //
 // Per pair tile each CTA's softmax (thread = key lane) turns its 128 keys x 128 rows into P.
 // The row maxima must agree across the pair: each CTA sends its 128 column maxima to the
@@ -36,12 +36,12 @@
 //
 // Roles (384 threads): warps 0-7 softmax (warps w and w+4 share TMEM lanes 32(w%4).., and take
 // the rows 0-63 and 64-127), then the epilogue; warps 8-10 TMA producers (whole 16 KB ring
-// stages dealt round-robin); warp 11 the MMA issuer in the even CTA. (Three producer warps keep
-// the block at 384 threads, which leaves each softmax thread the registers for its 64 running
-// row sums.) Both CTAs fill their rings
-// in the same order K(0) K(1) V(0) K(2) V(1) ... so a stage sits at the same offset in both, as
-// the pair MMA needs, and both CTAs' copies of a stage count their bytes on one barrier in the
-// even CTA (the 2-CTA form of the tensor copy), which alone waits on it.
+// stages dealt round-robin); warp 11 the MMA issuer in the even CTA. Every role's loops are
+// rolled: fully unrolled stage loops made the kernel 230 KB of code, and its steady state then
+// stalled on instruction fetch (an SM instruction cache hit rate near 47 %). Both CTAs fill
+// their rings in the same order K(0) K(1) V(0) K(2) V(1) ... so a stage sits at the same
+// offset in both, as the pair MMA needs, and both CTAs' copies of a stage count their bytes on
+// one barrier in the even CTA (the 2-CTA form of the tensor copy), which alone waits on it.
 //
 // Every wait is bounded (p.wait_ns); on expiry the kernel records DFLASH_DEVERR_TIMEOUT,
 // drains its own copies and MMAs, and both CTAs still meet at the final cluster barrier
@@ -376,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int tile;
                 pair_ring_unit(k, ntiles, is_k, tile);
                 const int n_st = is_k ? KC : 4 * VC2;
+#pragma unroll 1
                 for (int sq = 0; sq < n_st && ok; ++sq, ++seq) {
                     if (seq % kNumProducers != pw) continue;
                     // relative pages this stage reads: K: own 128 keys; V: quarter of 64 keys
@@ -435,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // both CTAs then give copies in flight a grace period (a copy lands within
             // microseconds while the memory system works) before this CTA may leave.
             if (leader) {
+#pragma unroll 1
                 for (int s = 0; s < S; ++s) {
                     if (issued_parity[s] > 1) continue;
                     const unsigned long long t_start = globaltimer();
@@ -507,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // S^T(j) into buffer j mod 2: its previous tile j - 2 has been read by both
                     // softmaxes (their P(j-2) was waited for by the V(j-2) unit)
                     const uint32_t sb = tmem_s + (uint32_t)(j & 1) * kN;
+#pragma unroll 1
                     for (int kc = 0; kc < KC && ok; ++kc) {
                         uint32_t st;
                         int slot;
@@ -531,7 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t pb_addr = p_addr + (uint32_t)((j % kPBufs) * Lay::kPBuf);
+#pragma unroll 1
                 for (int q = 0; q < 4 && ok; ++q) {
+#pragma unroll 1
                     for (int c = 0; c < VC2 && ok; ++c) {
                         uint32_t st;
                         int slot;
@@ -591,9 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t p_full_bar = in_cta(p_full, 0);
         bool ok = true;
         int nx = 0;     // maxima exchanges so far (they happen only on tiles that raise a row max)
-        float lp[64];   // this key lane's share of the 64 rows' sums, over all tiles so far
-#pragma unroll
-        for (int u = 0; u < 64; ++u) lp[u] = 0.f;
+        // row sums over this warp's 32 keys and all tiles so far: lane l holds the sum of row
+        // col0 + 16q + (l mod 16) in ls[q]
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        const int lcol = col0 + (lane & 15);
         auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool got = true;
             if (tid == 0) got = ring_wait_cluster(bar, parity, abort_flag, p.err, p.wait_ns);
@@ -681,12 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++nx;
                 // the row sums so far follow the new maxima
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float av[16];
-                    load_row16(a_s + col0 + q * 16, av);
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) lp[q * 16 + u] *= av[u];
-                }
+                for (int q = 0; q < 4; ++q) ls[q] *= a_s[lcol + q * 16];
                 if (j > 0) {
                     // O^T holds tiles < j once PV(j-1) is done: rescale it in TMEM
                     if (!wait_pv(j - 1)) {
@@ -719,14 +720,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             // pass 2: P = exp2(s - m) as bf16 pairs into the P^T buffer of CTA chh, and the
-            // rounded P (what the PV MMA reads) into this key lane's row sums
-#pragma unroll
+            // rounded P (what the PV MMA reads) summed over the warp's keys into the row sums.
+            // A rolled loop: the softmax's steady-state code stays small enough for the
+            // instruction cache.
+#pragma unroll 1
             for (int q = 0; q < 4; ++q) {
                 float mv[16];
                 load_row16(m_s + col0 + q * 16, mv);
                 uint32_t r16[16];
                 load16(sb + q * 16, r16);
                 uint32_t pk2[8];
+                float pr[16];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const float s0 = score(r16[2 * u], col0 + q * 16 + 2 * u);
@@ -735,8 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float e1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - mv[2 * u + 1]);
                     const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
                     pk2[u] = *reinterpret_cast<const uint32_t*>(&h2);
-                    lp[q * 16 + 2 * u] += __low2float(h2);
-                    lp[q * 16 + 2 * u + 1] += __high2float(h2);
+                    pr[2 * u] = __low2float(h2);
+                    pr[2 * u + 1] = __high2float(h2);
                 }
                 const uint32_t dst = prow0 + (uint32_t)((j % kPBufs) * Lay::kPBuf + q * 2048);
                 const uint4 lo4 = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
@@ -749,6 +753,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st_cluster_v4(dst + pswz0, lo4);
                     st_cluster_v4(dst + pswz1, hi4);
                 }
+                const float sm = pair_transpose_sum16(pr, lane);
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                    if (qq == q) ls[qq] += sm;
             }
             // every thread's P stores (own and peer CTA) are made visible to the tensor cores,
             // and its TMEM reads are ordered before the next MMAs; one thread of each CTA then
@@ -758,17 +766,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bar_sync_256();
             if (tid == 0) mbar_arrive_cluster(p_full_bar);
         }
-        // the row sums over this CTA's keys: across the 32 keys of each warp (transposing
-        // shuffle reduction), then across the 4 warps of each half of the rows
-        if (ok && ntiles > 0) {
+        // the row sums over this CTA's keys: across the 4 warps of each half of the rows
+        if (ok && ntiles > 0 && lane < 16) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float v[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) v[u] = lp[q * 16 + u];
-                const float sm = pair_transpose_sum16(v, lane);
-                if (lane < 16) red2[warp * 64 + q * 16 + lane] = sm;
-            }
+            for (int q = 0; q < 4; ++q) red2[warp * 64 + q * 16 + lane] = ls[q];
         }
         bar_sync_256();
         if (ok && ntiles > 0 && tid < kN) {

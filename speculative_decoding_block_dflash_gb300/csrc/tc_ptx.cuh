@@ -99,6 +99,7 @@ __device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_test_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
+#pragma unroll 1
         for (int k = 0; k < 64; ++k)
             if (mbar_test_wait(bar, parity)) return true;
         if (*abort_flag) return false;
@@ -119,6 +120,7 @@ __device__ __forceinline__ bool backoff_wait(uint64_t* bar, uint32_t parity, vol
     if (mbar_test_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
+#pragma unroll 1
         for (int k = 0; k < 8; ++k) {
             __nanosleep(64);
             if (mbar_test_wait(bar, parity)) return true;
@@ -552,6 +554,7 @@ __device__ __forceinline__ bool ring_wait_cluster(uint64_t* bar, uint32_t parity
     if (mbar_test_wait_cluster(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {
+#pragma unroll 1
         for (int k = 0; k < 64; ++k)
             if (mbar_test_wait_cluster(bar, parity)) return true;
         if (*abort_flag) return false;
