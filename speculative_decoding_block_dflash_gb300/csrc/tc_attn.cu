@@ -24,14 +24,15 @@
 // the softmax of tile j runs, and the TMA copies only wait for a softmax when
 // the ring is full of V(j) stages.
 //
-// Softmax (thread = one key lane of the tile, warps 0-3): S^T is read from TMEM
+// Softmax (thread = one key lane of the tile, warps 0-7; warps w and w + 4 share
+// the TMEM lanes of w mod 4 and take alternate 16-column groups): S^T is read from TMEM
 // in 16-column groups in rolled loops; this code runs once or twice per SM per
 // call, so it is kept small, and a dry run over fully masked scores executes it
 // once while the first K tile is still in flight so that the first real tile
 // does not stall on instruction fetches. Scores are masked by select
 // (non-causal rows see every key up to L-1, causal rows keys up to their own
 // position, a window W keeps the last W keys -- vLLM PR #43445 "Allow causal
-// DFlash"). The running row max m is shared by the 128 softmax threads and only
+// DFlash"). The running row max m is shared by the 256 softmax threads and only
 // raised when a score exceeds it by more than 2^8 in the exp2 domain (a
 // transposing shuffle reduction leaves each lane with one column's maximum over
 // its warp, then the four warps meet in shared memory; O^T and l^T are then
@@ -41,11 +42,12 @@
 // 16-byte stores. P^T has two buffers: the softmax of tile j+1 writes while
 // PV(j) still reads.
 //
-// Warp roles (288 threads): warps 0-3 softmax, warps 4-7 TMA producers, warp 8
-// MMA issuer; warps 0-7 share the epilogue. One warp's tensor copies are
-// processed in order, so a single producer warp caps a CTA near 26 GB/s with
-// 2 KB boxes; the ring stages are dealt round-robin to the four producer warps
-// (stage i of the sequence to warp i mod 4), each filling whole stages. Ring
+// Warp roles (384 threads): warps 0-7 softmax, then the epilogue; warps 8-10 TMA
+// producers; warp 11 MMA issuer. Every role's loops are rolled: with unrolled stage
+// loops the kernel was about 150 KB of code and its warps stalled on instruction fetch.
+// One warp's tensor copies are processed in order, so a single producer warp caps a CTA
+// near 26 GB/s with 2 KB boxes; the ring stages are dealt round-robin to the three
+// producer warps (stage i of the sequence to warp i mod 3), each filling whole stages. Ring
 // stages are 16 KB: a K stage is 128 keys x 64 dims (K-major, 128-byte
 // swizzle), a V stage 64 keys x 128 dims (MN-major). One TMA box is one page's
 // tokens of one KV head x 64 dims; the page id comes from the page table
@@ -75,10 +77,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 288;
-constexpr int kProducerWarp = 4;  // warps 4..7 issue TMA copies
-constexpr int kNumProducers = 4;
-constexpr int kMmaWarp = 8;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;  // warps 0..7
+constexpr int kProducerWarp = 8;      // warps 8..10 issue TMA copies
+constexpr int kNumProducers = 3;
+constexpr int kMmaWarp = 11;
 constexpr int kTileKeys = 128;
 constexpr int kStageBytes = 16384;
 constexpr int kMaxPids = 128;  // page ids held per producer warp (one window)
@@ -132,7 +135,7 @@ struct TcLayout {
     static constexpr int kLoOff = kRedOff + 4 * N * 4;                  // int lo_s[N]
     static constexpr int kHiOff = kLoOff + N * 4;                       // int hi_s[N]
     static constexpr int kRowOff = kHiOff + N * 4;                      // int64 orow_s[N]
-    static constexpr int kPidOff = kRowOff + N * 8;                     // int pid_s[4][kMaxPids]
+    static constexpr int kPidOff = kRowOff + N * 8;                     // int pid_s[kNumProducers][kMaxPids]
     static constexpr int kTotal = kPidOff + kNumProducers * kMaxPids * 4;
     static constexpr int kAlloc = kTotal + 1024;
     static constexpr int kTmemUsed = 2 * N + (D / 128) * N + 16;        // S^T x 2, O^T, l^T
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Page ids of relative pages [base, base + kMaxPids) -> this producer warp's pid_w.
     // Pages past the chunk and invalid ids map to the out-of-bounds coordinate num_pages.
     const int pw = warp - kProducerWarp;
-    int32_t* pid_w = pid_s + (pw & 3) * kMaxPids;
+    int32_t* pid_w = pid_s + (pw >= 0 && pw < kNumProducers ? pw : 0) * kMaxPids;
     auto load_window = [&](int base) {
         for (int k = lane; k < kMaxPids; k += 32) {
             const int pr = base + k;
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < Lay::kNumBars; ++i) {
             uint64_t* bar = bars + i;
-            mbar_init(bar, bar == p_full ? 128u : 1u);
+            mbar_init(bar, bar == p_full ? (uint32_t)kSoftmaxThreads : 1u);
         }
         *abort_flag = 0;
         if (!len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             a_s[tid] = 1.f;
         }
         // zero the padding rows [R, N) of Q (the TMA writes rows [0, R) of every 64-dim chunk)
-        for (int idx = tid; idx < KC * (N - R) * 8; idx += 128) {
+        for (int idx = tid; idx < KC * (N - R) * 8; idx += kSoftmaxThreads) {
             const int kc = idx / ((N - R) * 8);
             const int rem = idx - kc * (N - R) * 8;
             *reinterpret_cast<uint4*>(q_s + kc * N * 128 + (R + rem / 8) * 128 + (rem % 8) * 16) =
@@ -424,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < S; ++s) issued_parity[s] = 2;  // 2 = nothing outstanding
         if (ntiles > 0) {
             const int box = Psz * 128;  // bytes of one page x 64 dims
-            int seq = 0;                // index of the stage in the whole sequence; this warp fills seq = pw (mod 4)
+            int seq = 0;                // index of the stage in the whole sequence; this warp fills seq = pw (mod kNumProducers)
             for (int k = 0; k < 2 * ntiles && ok; ++k) {
                 bool is_k;
                 int tile;
@@ -432,8 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rel0 = tile * pages_per_tile;
                 const int n_st = is_k ? KC : 2 * VC;
                 // K: KC stages of 128 keys x 64 dims; V: 2 x VC stages of 64 keys x 128 dims
+                // (rolled, like every loop of the roles: unrolled, they made the kernel's code
+                // too large for the instruction cache)
+#pragma unroll 1
                 for (int sq = 0; sq < n_st && ok; ++sq, ++seq) {
-                    if ((seq & 3) == pw) {
+                    if (seq % kNumProducers == pw) {
                         if (rel0 < wbase || rel0 + pages_per_tile > wbase + kMaxPids) {
                             wbase = (tile > 0 ? tile - 1 : 0) * pages_per_tile;
                             load_window(wbase);
@@ -496,12 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Drain: no TMA copy of ours may still be landing when the ring is reused or the CTA exits.
         if (lane == 0 && !ok) {
+#pragma unroll 1
             for (int s = 0; s < S; ++s) {
                 if (issued_parity[s] > 1) continue;
                 const unsigned long long t_start = globaltimer();
                 while (!mbar_try_wait(full + s, issued_parity[s]) && globaltimer() - t_start < p.wait_ns) {
                 }
             }
+#pragma unroll 1
             for (int e = 0; e < E; ++e) {
                 if (!(issued_extra & (1u << e))) continue;
                 const unsigned long long t_start = globaltimer();
@@ -548,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // S^T(j) = K(j) . Q^T into buffer j mod 2, whose previous tile j - 2 the
                 // softmax has finished with (its p_full was waited for by the V(j-2) unit)
                 const uint32_t sb = tmem_s + (uint32_t)(j & 1) * N;
+#pragma unroll 1
                 for (int kc = 0; kc < KC && ok; ++kc) {
                     uint32_t st;
                     RingSlot sl;
@@ -574,7 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int tile_key0 = t0 + j * kTileKeys;
             const uint32_t pb_addr = p_addr + (uint32_t)(j & 1) * Lay::kPBytes;
+#pragma unroll 1
             for (int h = 0; h < 2 && ok; ++h) {
+#pragma unroll 1
                 for (int c = 0; c < VC && ok; ++c) {
                     uint32_t st_addr;
                     RingSlot sl;
@@ -631,8 +642,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax warps 0-3 (thread = key lane)
+        // ------------------------------------------------------------ softmax warps 0-7
+        // Thread = key lane kl of the tile; warps w and w + 4 share TMEM lanes 32 (w mod 4) ..
+        // and take alternate 16-column groups of S^T (half 0: groups 0, 2, ..; half 1: 1, 3, ..).
         const float sl2 = p.scale * kLog2e;
+        const int kl = tid & 127;
+        const int half = tid >> 7;
         const bool plain = (p.causal == 0 && p.window == 0);
         // A key inside every row's range [max lo, min hi] needs no test per row: with a window
         // or the causal switch only a few keys (the window's first, the block's own) fall
@@ -648,17 +663,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P^T is MN-major with a 32-byte swizzle: per key half, 16-row groups (atoms) of
         // 2048 B = 8 key groups x (8 keys x 32 B); this key lane owns one 32-byte row of
         // every atom, the two 16-byte halves swapped for keys 4-7 of a group.
-        const int pr = tid & 7;
-        uint8_t* prow0 = p_s + (tid >> 6) * (N * 128) + ((tid & 63) >> 3) * 256 + pr * 32;
+        const int pr = kl & 7;
+        uint8_t* prow0 = p_s + (kl >> 6) * (N * 128) + ((kl & 63) >> 3) * 256 + pr * 32;
         const int pswz0 = (0 ^ (pr >> 2)) << 4;
         const int pswz1 = (1 ^ (pr >> 2)) << 4;
         bool ok = true;
         // One thread waits on the mbarrier; the named barrier makes the outcome
-        // uniform across the 128 softmax threads (so none is left at a barrier).
+        // uniform across the 256 softmax threads (so none is left at a barrier).
         auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool got = true;
             if (tid == 0) got = ring_wait(bar, parity, abort_flag, p.err, p.wait_ns);
-            return !named_bar_or_128(!got);
+            return !named_bar_or_256(!got);
         };
 
         // Iteration j = -1 is a dry run over fully masked scores while the first K tile is
@@ -677,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
             }
-            const int key = t0 + j * kTileKeys + tid;
+            const int key = t0 + j * kTileKeys + kl;
             const bool kvalid = !dry && key >= ch.kb && key < ch.ke;
             const bool allvis = plain || (key >= lo_all && key <= hi_all);
             // masked, log2-scaled score of column col from raw S^T bits
@@ -689,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // pass 1: does any score exceed the running max by more than the threshold?
             bool need = false;
 #pragma unroll 1
-            for (int q = 0; q < NQ; ++q) {
+            for (int q = half; q < NQ; q += 2) {
                 float mv[16];
                 load_row16(m_s + q * 16, mv);
                 uint32_t r16[16];
@@ -697,21 +712,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 16; ++u) need |= score(r16[u], q * 16 + u) > mv[u] + kRescaleThresh;
             }
-            need = named_bar_or_128(need || dry);
+            need = named_bar_or_256(need || dry);
             if (need) {
                 // new row maxima: each warp's column maxima (transposing shuffle reduction,
-                // one column per lane), then the maximum over the 4 warps
+                // one column per lane), then the maximum over the 4 warps of the column's half
 #pragma unroll 1
-                for (int q = 0; q < NQ; ++q) {
+                for (int q = half; q < NQ; q += 2) {
                     uint32_t r16[16];
                     load16(sb + q * 16, r16);
                     float v[16];
 #pragma unroll
                     for (int u = 0; u < 16; ++u) v[u] = score(r16[u], q * 16 + u);
                     const float mx = transpose_max16(v, lane);
-                    if (lane < 16) red[warp * N + q * 16 + lane] = mx;
+                    if (lane < 16) red[(warp & 3) * N + q * 16 + lane] = mx;
                 }
-                named_bar_sync_128();
+                named_bar_sync_256();
                 if (tid < N) {
                     const float mo = m_s[tid];
                     const float mn =
@@ -719,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m_s[tid] = mn;
                     a_s[tid] = (mo == -INFINITY) ? 0.f : ex2(mo - mn);
                 }
-                named_bar_sync_128();
+                named_bar_sync_256();
             }
             // O^T and l^T hold tile j-1 once its PV has completed: only a rescale waits for it.
             // P^T buffer j mod 2 is free once PV(j-2) has completed. (p_free[b] completes once
@@ -732,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 {
 #pragma unroll 1
-                    for (int cq = 0; cq < VC * NQ; ++cq) {
+                    for (int cq = half; cq < VC * NQ; cq += 2) {
                         const int c = cq / NQ, q = cq % NQ;
                         uint32_t r16[16];
                         const uint32_t ta = tmem_o + c * N + lane_base + q * 16;
@@ -743,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * av[u]);
                         tmem_st16(ta, r16);
                     }
-                    {
+                    if (half == 0) {
                         // l^T: this thread's lane is row tid
                         uint32_t r16[16];
                         load16(tmem_l + lane_base, r16);
@@ -765,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // pass 2: P = exp2(s - m), bf16 pairs, into P^T buffer j mod 2
             uint8_t* prow = prow0 + (j & 1) * Lay::kPBytes;
 #pragma unroll 1
-            for (int q = 0; q < NQ; ++q) {
+            for (int q = half; q < NQ; q += 2) {
                 // row maxima into registers first: the P^T stores below must not be ordered
                 // against these loads (both are shared-memory accesses the compiler cannot separate)
                 float mv[16];
@@ -800,14 +815,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------- epilogue (warps 0-7)
-    // Softmax warps 0-3 and the producer warps 4-7 (idle by now) share the read-out: TMEM
-    // lanes 32 (w mod 4) .. +31 are open to warp w, so warps w and w + 4 take alternate
-    // 128-dim chunks of O^T. The output tile (R rows x D, bf16 for the final output,
+    // The softmax warps 0-7 do the read-out: TMEM lanes 32 (w mod 4) .. +31 are open to
+    // warp w, so warps w and w + 4 take alternate 128-dim chunks of O^T. The output tile (R rows x D, bf16 for the final output,
     // fp32 for a split's partial) is assembled row-major over Q, P and the ring (all
     // free once the last PV has completed) and written with bulk asynchronous copies:
     // for each block position i the Gc heads' rows are contiguous in global memory.
+    // Every role's outcome, the producers' and the MMA warp's included: an aborted producer
+    // may still drain copies into the ring, which the read-out below reuses.
+    const bool any_failed = __syncthreads_or(!role_ok) != 0;
     if (warp < 8) {
-        const bool have_o = !named_bar_or_256(!role_ok) && ntiles > 0;
+        const bool have_o = !any_failed && ntiles > 0;
         tc_fence_after();
         const int64_t part_base = (slot0 + c_split) * rstride + rbias;
         const bool final_out = (p.splits == 1);
