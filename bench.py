@@ -95,6 +95,11 @@ def parse_args():
                     help="headline run only: skip the other attention workloads' extra key")
     ap.add_argument("--cpu-budget", type=float, default=20.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds of oracle time for --impl reference")
+    ap.add_argument("--capture", metavar="WORKLOAD", default=None,
+                    help="profiler target: two block_attn calls on one layer of this attention workload, "
+                         "nothing timed")
+    ap.add_argument("--capture-batch", type=int, default=None,
+                    help="with --capture long_draft: its first N requests (a capture-sized cache)")
     return ap.parse_args()
 
 
@@ -1034,6 +1039,26 @@ def sel_bench(args, dfl, dev, rank, world):
 # ----------------------------------------------------------------------------- GPU arm
 
 
+def capture_case(args, dfl, dev):
+    """Two calls of the workload's own plan on one layer (the second is the one a profiler
+    captures with -s 1 -c 1); checks the device error word and prints the plan."""
+    import workloads
+
+    case = workloads.make_case(args.capture, device=dev, layers=1, batch=args.capture_batch)
+    splits = case.num_splits if args.splits < 0 else args.splits
+    for _ in range(2):
+        dfl.block_attn(case.q, case.k_cache, case.v_cache, case.page_table, case.seq_lens, case.block_len,
+                       causal=case.causal, window=case.window, scale=case.scale, num_splits=splits,
+                       kernel=args.kernel)
+    torch.cuda.synchronize()
+    err = dfl.read_error()
+    dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
+    plan = dfl.plan_info(dims, case.block_len, case.window, splits, args.kernel)
+    print(json.dumps({"capture": args.capture, "batch": case.batch, "kv_bytes": kv_bytes_per_step(case),
+                      "plan": plan, "error_word": err}), flush=True)
+    assert err == 0, "device-side check failed"
+
+
 def traffic_from_profiles(kernel_name, workload=None):
     """DRAM bytes per launch from the committed ncu summary of this kernel on this workload (records
     keyed "kernel@workload", or by the kernel alone for single-workload kernels), if the kernel
@@ -1152,6 +1177,11 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 
+    if args.capture:
+        capture_case(args, dfl, dev)
+        if dist:
+            dist.destroy_process_group()
+        return
     if args.config == ACCEPT_CONFIG:
         accept_bench(args, dfl, dev, rank, world)
         if dist:

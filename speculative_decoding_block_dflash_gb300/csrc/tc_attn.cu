@@ -701,6 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!allvis) vis = vis && key >= lo_s[col] && key <= hi_s[col];
                 return vis ? u2f(raw) * sl2 : -INFINITY;
             };
+            // Every column of this key lane visible (all but the chunk's edge keys and the
+            // window's or the block's own few): no selects, and the scale folds into one FMA.
+            // The running maxima are then finite, since pass 1 raises any -inf one.
+            const bool open = kvalid && allvis;
             // pass 1: does any score exceed the running max by more than the threshold?
             bool need = false;
 #pragma unroll 1
@@ -709,8 +713,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_row16(m_s + q * 16, mv);
                 uint32_t r16[16];
                 load16(sb + q * 16, r16);
+                if (open) {
 #pragma unroll
-                for (int u = 0; u < 16; ++u) need |= score(r16[u], q * 16 + u) > mv[u] + kRescaleThresh;
+                    for (int u = 0; u < 16; ++u) need |= fmaf(u2f(r16[u]), sl2, -mv[u]) > kRescaleThresh;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) need |= score(r16[u], q * 16 + u) > mv[u] + kRescaleThresh;
+                }
             }
             need = named_bar_or_256(need || dry);
             if (need) {
@@ -787,14 +796,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_row16(m_s + q * 16, mv);
                 uint32_t r16[16];
                 load16(sb + q * 16, r16);
+                float e[16];
+                if (open) {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) e[u] = ex2(fmaf(u2f(r16[u]), sl2, -mv[u]));
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const float sv = score(r16[u], q * 16 + u);
+                        e[u] = (sv == -INFINITY) ? 0.f : ex2(sv - mv[u]);
+                    }
+                }
                 uint32_t pk[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const float s0 = score(r16[2 * u], q * 16 + 2 * u);
-                    const float s1 = score(r16[2 * u + 1], q * 16 + 2 * u + 1);
-                    const float e0 = (s0 == -INFINITY) ? 0.f : ex2(s0 - mv[2 * u]);
-                    const float e1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - mv[2 * u + 1]);
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[2 * u], e[2 * u + 1]);
                     pk[u] = *reinterpret_cast<const uint32_t*>(&h2);
                 }
                 if (!dry) {

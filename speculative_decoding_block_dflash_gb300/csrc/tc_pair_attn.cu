@@ -624,6 +624,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!allvis) vis = vis && key >= lo_s[col] && key <= hi_s[col];
                 return vis ? u2f(raw) * sl2 : -INFINITY;
             };
+            // Every column of this key lane visible (all but the chunk's edge keys and the
+            // window's or the block's own few): no selects, and the scale folds into one FMA.
+            // The running maxima are then finite, since pass 1 raises any -inf one.
+            const bool open = kvalid && allvis;
             // pass 1: does any score of this CTA exceed its row's running max by more than the
             // threshold? Both CTAs exchange the answer (one word); only when either says yes
             // do they form and exchange the column maxima, so both take the same update.
@@ -634,8 +638,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_row16(m_s + col0 + q * 16, mv);
                 uint32_t r16[16];
                 load16(sb + q * 16, r16);
+                if (open) {
 #pragma unroll
-                for (int u = 0; u < 16; ++u) nd |= score(r16[u], col0 + q * 16 + u) > mv[u] + kRescaleThresh;
+                    for (int u = 0; u < 16; ++u) nd |= fmaf(u2f(r16[u]), sl2, -mv[u]) > kRescaleThresh;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) nd |= score(r16[u], col0 + q * 16 + u) > mv[u] + kRescaleThresh;
+                }
             }
             nd = bar_or_256(nd);
             if (tid == 0) st_async_f32(in_cta(nflag + (j & 1), peer), nd ? 1.f : 0.f, in_cta(nf_full + (j & 1), peer));
@@ -729,15 +738,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 load_row16(m_s + col0 + q * 16, mv);
                 uint32_t r16[16];
                 load16(sb + q * 16, r16);
+                float e[16];
+                if (open) {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) e[u] = ex2(fmaf(u2f(r16[u]), sl2, -mv[u]));
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const float sv = score(r16[u], col0 + q * 16 + u);
+                        e[u] = (sv == -INFINITY) ? 0.f : ex2(sv - mv[u]);
+                    }
+                }
                 uint32_t pk2[8];
                 float pr[16];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const float s0 = score(r16[2 * u], col0 + q * 16 + 2 * u);
-                    const float s1 = score(r16[2 * u + 1], col0 + q * 16 + 2 * u + 1);
-                    const float e0 = (s0 == -INFINITY) ? 0.f : ex2(s0 - mv[2 * u]);
-                    const float e1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - mv[2 * u + 1]);
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[2 * u], e[2 * u + 1]);
                     pk2[u] = *reinterpret_cast<const uint32_t*>(&h2);
                     pr[2 * u] = __low2float(h2);
                     pr[2 * u + 1] = __high2float(h2);

@@ -171,9 +171,11 @@ CONFIG_NAMES = ["tiny", "global_verify", "batch_sweep_b1", "batch_sweep_b2", "ba
                 "batch_sweep_b8", "sliding", "sliding_causal", "long_draft"]
 
 
-def make_case(name: str, device="cuda", layers: int = 1) -> Case:
+def make_case(name: str, device="cuda", layers: int = 1, batch: Optional[int] = None) -> Case:
     """One of the named workloads above. `layers` > 1 adds disjoint page tables
-    (distinct K/V per layer) so a benchmark can rotate through more bytes than L2."""
+    (distinct K/V per layer) so a benchmark can rotate through more bytes than L2.
+    `batch` takes the first requests of long_draft only (its requests are alike, so a
+    profiler can capture the same kernel on a fraction of the 17 GB cache)."""
     if name == "tiny":
         return make_custom(name, 1, 9, 1, 1, 64, [128], dtype=torch.float32, identity_pages=True,
                            scale=1.0 / 8.0, seed=1234 + 0, device=device)
@@ -191,7 +193,8 @@ def make_case(name: str, device="cuda", layers: int = 1) -> Case:
                            causal=(name == "sliding_causal"), seed=1234 + 3, device=device)
     if name == "long_draft":
         sh = LONG_DRAFT
-        case = make_custom(name, sh["B"], sh["T"], sh["Hq"], sh["Hkv"], sh["D"], [sh["L"]] * sh["B"],
+        nb = sh["B"] if batch is None else batch
+        case = make_custom(name, nb, sh["T"], sh["Hq"], sh["Hkv"], sh["D"], [sh["L"]] * nb,
                            dtype=torch.bfloat16, pool_factor=1.0, layers=layers, seed=1234 + 4, device=device,
                            num_splits=sh["splits"])
         _projected_kv(case, hidden=5376, seed=1234 + 4)
