@@ -264,8 +264,8 @@ DFLASH_API const char* dflash_last_error_message(void);
  * DFLASH_ERR_WORKSPACE (request fewer splits). With num_splits = 0 the call takes the auto
  * plan if it fits, else the one-wave length-balanced plan (partials sized for one request)
  * if that fits, else the most uniform chunks that fit. The first call on a device resolves
- * the array's device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture. Every call clears the error word and
+ * the array's device address (cudaGetSymbolAddress) with that device current, once, and
+ * caches it. Every call clears the error word and
  * counters on `stream`, then reuses the array, which keeps the last call's
  * contents: calls that can overlap on the GPU (different streams, or
  * different host threads on the same device) race on it and must be ordered
