@@ -29,10 +29,10 @@
 // The row maxima must agree across the pair: each CTA sends its 128 column maxima to the
 // other with asynchronous stores that count their bytes on the receiver's mbarrier, and both
 // take the same lazy update. Each CTA writes the P of rows 0-63 into the even CTA's P^T
-// buffer and of rows 64-127 into the odd CTA's (one half local, one half remote). With one
-// P^T buffer, the ring order K(j+1) V(j) K(j+2) V(j+1) leaves the softmax of tile j+1 the whole
-// of S(j+2)'s K stream between PV(j) and PV(j+1) to write it, and the 32 KB of a second buffer
-// go to the ring.
+// buffer and of rows 64-127 into the odd CTA's (one half local, one half remote). P^T has two
+// buffers, so the softmax of tile j does not wait for PV(j-1): a single buffer left 7 ring
+// stages instead of 5, but each tile's V stages then sat in the ring through the next
+// softmax, and two buffers measured faster.
 //
 // Roles (384 threads): warps 0-7 softmax (warps w and w+4 share TMEM lanes 32(w%4).., and take
 // the rows 0-63 and 64-127), then the epilogue; warps 8-10 TMA producers (whole 16 KB ring
@@ -64,7 +64,7 @@ constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kNumProducers = 3;
 constexpr int kMmaWarp = 11;
-constexpr int kPBufs = 1;       // P^T buffers (1: the 32 KB of a second one go to the ring)
+constexpr int kPBufs = 2;       // P^T buffers: softmax j writes while PV(j-1) still reads
 constexpr int kPairKeys = 256;  // keys per pair tile
 constexpr int kOwnKeys = 128;   // keys of a pair tile whose K this CTA streams
 constexpr int kHalf = 64;       // Q / P rows held per CTA
@@ -774,10 +774,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int qq = 0; qq < 4; ++qq)
                     if (qq == q) ls[qq] += sm;
             }
-            // every thread's P stores (own and peer CTA) are made visible to the tensor cores,
-            // and its TMEM reads are ordered before the next MMAs; one thread of each CTA then
-            // tells the even CTA
-            fence_proxy_async_cluster();
+            // every thread's P stores are made visible to the tensor cores (a warp writes
+            // either only its own CTA's buffer, which needs the CTA-scope fence alone, or only
+            // the peer's) and its TMEM reads are ordered before the next MMAs; one thread of
+            // each CTA then tells the even CTA. (An arrive per warp measured slower: each
+            // cluster-scope release costs about what the barrier saves.)
+            if (p_local)
+                fence_proxy_async_smem();
+            else
+                fence_proxy_async_cluster();
             tc_fence_before();
             bar_sync_256();
             if (tid == 0) mbar_arrive_cluster(p_full_bar);
