@@ -704,11 +704,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Every column of this key lane visible (all but the chunk's edge keys and the
             // window's or the block's own few): no selects, and the scale folds into one FMA.
             // The running maxima are then finite, since pass 1 raises any -inf one.
-            const bool open = kvalid && allvis;
-            // pass 1: does any score exceed the running max by more than the threshold?
+            // (the dry run sends half of the warps down each path, so both are fetched)
+            const bool open = dry ? (half == 0) : (kvalid && allvis);
+            // pass 1: does any score exceed the running max by more than the threshold? On
+            // the first tile every running max is -inf, so the answer is yes without looking.
             bool need = false;
 #pragma unroll 1
-            for (int q = half; q < NQ; q += 2) {
+            for (int q = half; q < (j == 0 ? 0 : NQ); q += 2) {
                 float mv[16];
                 load_row16(m_s + q * 16, mv);
                 uint32_t r16[16];
@@ -721,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int u = 0; u < 16; ++u) need |= score(r16[u], q * 16 + u) > mv[u] + kRescaleThresh;
                 }
             }
-            need = named_bar_or_256(need || dry);
+            need = named_bar_or_256(need || dry || j == 0);
             if (need) {
                 // new row maxima: each warp's column maxima (transposing shuffle reduction,
                 // one column per lane), then the maximum over the 4 warps of the column's half
@@ -911,114 +913,115 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 bulk_wait_read_0();  // the tile must stay in shared memory until the copies have read it
         }
+    }
 
-        if (x.fused) {
-            // ------------------------------------------------------------ split combine
-            // The splits CTAs of this (request, row group) are co-resident (cooperative
-            // launch). Each publishes its partial (the bulk copy above, the lse stores
-            // before it), arrives on the group's counter and waits for all of them; then
-            // each combines a slice of the group's R x D outputs:
-            //   m = max_c lse_c, w_c = exp(lse_c - m), out = sum_c w_c o_c / sum_c w_c,
-            //   lse = m + log(sum_c w_c)
-            // The last CTA to finish resets the two counters to zero for the next call.
+    if (x.fused) {
+        // ------------------------------------------------------------ split combine
+        // The splits CTAs of this (request, row group) are co-resident (cooperative
+        // launch). Each publishes its partial (the bulk copy above, the lse stores
+        // before it), arrives on the group's counter and waits for all of them; then
+        // all 12 warps of each combine a slice of the group's R x D outputs (one float4
+        // column per thread: a global_verify slice of 288 float4s takes one round of loads):
+        //   m = max_c lse_c, w_c = exp(lse_c - m), out = sum_c w_c o_c / sum_c w_c,
+        //   lse = m + log(sum_c w_c)
+        // The last CTA to finish resets the two counters to zero for the next call.
+        __threadfence();
+        __syncthreads();
+        int32_t* cnt = p.counters + 2 * (b * gridDim.y + blockIdx.y);
+        bool arrived = true;
+        if (tid == 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
             __threadfence();
-            named_bar_sync_256();
-            int32_t* cnt = p.counters + 2 * (b * gridDim.y + blockIdx.y);
-            bool arrived = true;
-            if (tid == 0) {
-                asm volatile("fence.proxy.async.global;" ::: "memory");
-                __threadfence();
-                atomicAdd(cnt, 1);
-                const unsigned long long t_start = globaltimer();
-                while (ld_acquire_gpu(cnt) < n_split) {
-                    if (globaltimer() - t_start > p.wait_ns) {
-                        raise_error(p.err, DFLASH_DEVERR_TIMEOUT);
-                        arrived = false;
-                        break;
-                    }
+            atomicAdd(cnt, 1);
+            const unsigned long long t_start = globaltimer();
+            while (ld_acquire_gpu(cnt) < n_split) {
+                if (globaltimer() - t_start > p.wait_ns) {
+                    raise_error(p.err, DFLASH_DEVERR_TIMEOUT);
+                    arrived = false;
+                    break;
                 }
             }
-            arrived = !named_bar_or_256(!arrived);
-            if (arrived) {
-                const int total = R * D;
-                const int per = ((total + n_split - 1) / n_split + 3) & ~3;
-                const int e0 = c_split * per;
-                const int e1 = min(total, e0 + per);
-                if (e0 < e1) {
-                    const int r0 = e0 / D;
-                    const int nr = (e1 - 1) / D - r0 + 1;
-                    float* w_sm = reinterpret_cast<float*>(smem + Lay::kQOff);  // [nr][splits] weights
-                    float* r_sm = w_sm + nr * n_split;                           // [nr][2]: 1/sum, lse
-                    for (int rr = warp; rr < nr; rr += 8) {
-                        const int64_t orow = orow_s[r0 + rr];
-                        float m = -INFINITY;
-                        const float* lse_row = p.part_lse + slot0 * rstride + rbias + orow;
-                        for (int c = lane; c < n_split; c += 32) m = fmaxf(m, __ldcg(lse_row + c * rstride));
+        }
+        arrived = __syncthreads_or(!arrived) == 0;
+        if (arrived) {
+            const int total = R * D;
+            const int per = ((total + n_split - 1) / n_split + 3) & ~3;
+            const int e0 = c_split * per;
+            const int e1 = min(total, e0 + per);
+            if (e0 < e1) {
+                const int r0 = e0 / D;
+                const int nr = (e1 - 1) / D - r0 + 1;
+                float* w_sm = reinterpret_cast<float*>(smem + Lay::kQOff);  // [nr][splits] weights
+                float* r_sm = w_sm + nr * n_split;                           // [nr][2]: 1/sum, lse
+                for (int rr = warp; rr < nr; rr += kThreads / 32) {
+                    const int64_t orow = orow_s[r0 + rr];
+                    float m = -INFINITY;
+                    const float* lse_row = p.part_lse + slot0 * rstride + rbias + orow;
+                    for (int c = lane; c < n_split; c += 32) m = fmaxf(m, __ldcg(lse_row + c * rstride));
 #pragma unroll
-                        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-                        float tot = 0.f;
-                        for (int c = lane; c < n_split; c += 32) {
-                            const float l = __ldcg(lse_row + c * rstride);
-                            const float w = (l == -INFINITY) ? 0.f : expf(l - m);
-                            w_sm[rr * n_split + c] = w;
-                            tot += w;
-                        }
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-                        if (lane == 0) {
-                            const bool empty_row = (m == -INFINITY) || !(tot > 0.f);
-                            r_sm[2 * rr] = empty_row ? 0.f : 1.f / tot;
-                            r_sm[2 * rr + 1] = empty_row ? -INFINITY : m + logf(tot);
-                        }
+                    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+                    float tot = 0.f;
+                    for (int c = lane; c < n_split; c += 32) {
+                        const float l = __ldcg(lse_row + c * rstride);
+                        const float w = (l == -INFINITY) ? 0.f : expf(l - m);
+                        w_sm[rr * n_split + c] = w;
+                        tot += w;
                     }
-                    named_bar_sync_256();
-                    for (int e = e0 + tid * 4; e < e1; e += 256 * 4) {
-                        const int r = e / D, d = e - r * D, rr = r - r0;
-                        const float inv = r_sm[2 * rr];
-                        const int64_t orow = orow_s[r];
-                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (inv > 0.f) {
-                            const float* base = p.part_out + (slot0 * rstride + rbias + orow) * D + d;
-                            const int64_t cstride = rstride * D;
-                            for (int c0 = 0; c0 < n_split; c0 += 16) {
-                                float4 v[16];
 #pragma unroll
-                                for (int k = 0; k < 16; ++k)
-                                    v[k] = c0 + k < n_split
-                                               ? __ldcg(reinterpret_cast<const float4*>(base + (c0 + k) * cstride))
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+                    if (lane == 0) {
+                        const bool empty_row = (m == -INFINITY) || !(tot > 0.f);
+                        r_sm[2 * rr] = empty_row ? 0.f : 1.f / tot;
+                        r_sm[2 * rr + 1] = empty_row ? -INFINITY : m + logf(tot);
+                    }
+                }
+                __syncthreads();
+                for (int e = e0 + tid * 4; e < e1; e += kThreads * 4) {
+                    const int r = e / D, d = e - r * D, rr = r - r0;
+                    const float inv = r_sm[2 * rr];
+                    const int64_t orow = orow_s[r];
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (inv > 0.f) {
+                        const float* base = p.part_out + (slot0 * rstride + rbias + orow) * D + d;
+                        const int64_t cstride = rstride * D;
+                        for (int c0 = 0; c0 < n_split; c0 += 16) {
+                            float4 v[16];
 #pragma unroll
-                                for (int k = 0; k < 16; ++k) {
-                                    const float w = c0 + k < n_split ? w_sm[rr * n_split + c0 + k] : 0.f;
-                                    acc.x = fmaf(w, v[k].x, acc.x);
-                                    acc.y = fmaf(w, v[k].y, acc.y);
-                                    acc.z = fmaf(w, v[k].z, acc.z);
-                                    acc.w = fmaf(w, v[k].w, acc.w);
-                                }
+                            for (int k = 0; k < 16; ++k)
+                                v[k] = c0 + k < n_split
+                                           ? __ldcg(reinterpret_cast<const float4*>(base + (c0 + k) * cstride))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) {
+                                const float w = c0 + k < n_split ? w_sm[rr * n_split + c0 + k] : 0.f;
+                                acc.x = fmaf(w, v[k].x, acc.x);
+                                acc.y = fmaf(w, v[k].y, acc.y);
+                                acc.z = fmaf(w, v[k].z, acc.z);
+                                acc.w = fmaf(w, v[k].w, acc.w);
                             }
                         }
-                        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-                        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-                        uint2 pk;
-                        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
-                        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
-                        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow * D + d) = pk;
                     }
-                    // a row's lse is written by the CTA whose slice holds the row's first element
-                    for (int rr = tid; rr < nr; rr += 256)
-                        if ((r0 + rr) * D >= e0 && p.lse) p.lse[orow_s[r0 + rr]] = r_sm[2 * rr + 1];
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                    pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow * D + d) = pk;
                 }
+                // a row's lse is written by the CTA whose slice holds the row's first element
+                for (int rr = tid; rr < nr; rr += kThreads)
+                    if ((r0 + rr) * D >= e0 && p.lse) p.lse[orow_s[r0 + rr]] = r_sm[2 * rr + 1];
             }
-            named_bar_sync_256();
-            if (tid == 0) {
-                // A CTA whose arrival wait ran out still counts itself here, so a group whose
-                // counters held stale arrivals (every CTA times out) is reset like any other.
-                __threadfence();
-                if (atomicAdd(cnt + 1, 1) == n_split - 1) {
-                    // every CTA of the group has passed (or given up) the arrival wait and read its slice
-                    atomicExch(cnt, 0);
-                    atomicExch(cnt + 1, 0);
-                }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            // A CTA whose arrival wait ran out still counts itself here, so a group whose
+            // counters held stale arrivals (every CTA times out) is reset like any other.
+            __threadfence();
+            if (atomicAdd(cnt + 1, 1) == n_split - 1) {
+                // every CTA of the group has passed (or given up) the arrival wait and read its slice
+                atomicExch(cnt, 0);
+                atomicExch(cnt + 1, 0);
             }
         }
     }
