@@ -343,6 +343,11 @@ dflash_status dflash_plan_call(const dflash_dims* dims, int32_t block_len, int32
         const cudaError_t e = tc_grid_info(p, &plan->ctas, &fused);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core grid query");
         plan->launches = (splits == 1 || fused) ? 1 : 2;
+    } else if (k == DFLASH_KERNEL_TC_PAIR) {
+        p.T = block_len;
+        const cudaError_t e = tc_pair_grid_ctas(p, &plan->ctas);
+        if (e != cudaSuccess) return cuda_fail(e, "CTA-pair grid query");
+        plan->launches = splits == 1 ? 1 : 2;
     } else {
         plan->ctas = work_units(dims, block_len, k) * splits;
         plan->launches = splits == 1 ? 1 : 2;

@@ -110,6 +110,7 @@ int tc_row_groups(const AttnParams& p);       // CTAs per (request, KV head, chu
 bool tc_pair_supports(const AttnParams& p);
 int tc_pair_ctas_per_split(const AttnParams& p);  // CTAs per split chunk (2 * B * Hkv * row groups)
 int tc_pair_row_groups(const AttnParams& p);      // pairs per (request, KV head, chunk)
+cudaError_t tc_pair_grid_ctas(const AttnParams& p, int64_t* ctas);  // CTAs of the persistent launch
 cudaError_t launch_tc_pair_attn(const AttnParams& p, cudaStream_t stream);
 
 // SM count of the current device (cached per device).

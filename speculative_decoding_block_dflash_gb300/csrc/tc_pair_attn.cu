@@ -48,6 +48,7 @@
 // before TMEM is freed, so neither exits while the other may still touch its memory.
 #include <cuda.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -77,10 +78,44 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThresh = 8.0f;
 
 struct PairExtra {
-    int32_t Gc;    // query heads per pair
-    int32_t n_rg;  // row groups per KV head (G / Gc)
-    int32_t Tb;    // block positions per CTA (ceil(T / 2)); CTA r holds positions [r*Tb, r*Tb + Tb)
+    int32_t Gc;     // query heads per pair
+    int32_t n_rg;   // row groups per KV head (G / Gc)
+    int32_t Tb;     // block positions per CTA (ceil(T / 2)); CTA r holds positions [r*Tb, r*Tb + Tb)
+    int32_t units;  // (request, KV head, row group, chunk) units: splits * Hkv * n_rg * B
 };
+
+// One unit of work of a CTA pair: a (request, KV head, row group, key chunk). Pair i of the
+// persistent grid takes units i, i + pairs, i + 2 pairs, ...; unit u is chunk u mod splits of
+// row-group slot (u / splits) mod (Hkv n_rg) of request u / (splits Hkv n_rg).
+struct PairUnit {
+    int32_t b, g, c_split, h0;
+    int32_t L;
+    bool len_ok;
+    Chunk ch;
+    int32_t t0, ntiles, chunk_pages, first_page;
+};
+
+__device__ __forceinline__ PairUnit pair_unit(const AttnParams& p, const PairExtra& x, int u)
+{
+    PairUnit U;
+    const int ys = p.Hkv * x.n_rg;
+    U.c_split = u % p.splits;
+    const int y = (u / p.splits) % ys;
+    U.b = u / (p.splits * ys);
+    U.g = y / x.n_rg;
+    const int rg = y % x.n_rg;
+    U.h0 = U.g * p.G + rg * x.Gc;
+    U.L = __ldg(p.seq_lens + U.b);
+    U.len_ok = seq_len_ok(p, U.L);
+    U.ch.kb = 0;
+    U.ch.ke = 0;
+    if (U.len_ok) U.ch = split_chunk(U.L, p.T, p.window, p.page_size, p.splits, U.c_split);
+    U.t0 = (U.ch.kb / p.page_size) * p.page_size;
+    U.ntiles = (U.ch.kb < U.ch.ke) ? (U.ch.ke - U.t0 + kPairKeys - 1) / kPairKeys : 0;
+    U.chunk_pages = U.ntiles * (kPairKeys / p.page_size);
+    U.first_page = U.t0 / p.page_size;
+    return U;
+}
 
 __host__ __device__ constexpr int pair_pow2ceil(int x)
 {
@@ -103,8 +138,8 @@ struct PairLayout {
     static constexpr int kStagesFit = (227 * 1024 - 1024 - kRingOff - kSmallBytes) / kStageBytes;
     static constexpr int kStages = kStagesFit > 10 ? 10 : kStagesFit;
     static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-    // barriers: full[S] empty[S] s_full[2] p_full p_free[kPBufs] nf_full[2] px_full[2] lx_full drain
-    static constexpr int kNumBars = 2 * kStages + 9 + kPBufs;
+    // barriers: full[S] empty[S] s_full[2] p_full p_free[kPBufs] nf_full[2] px_full[2] lx_full[2] drain
+    static constexpr int kNumBars = 2 * kStages + 10 + kPBufs;
     static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) / 16 * 16;  // tmem base, abort flag
     static constexpr int kMOff = kMiscOff + 16;             // float m_s[128]
     static constexpr int kAOff = kMOff + kN * 4;            // float a_s[128] (1/l at the end)
@@ -113,8 +148,8 @@ struct PairLayout {
     static constexpr int kLaccOff = kSumOff + 8 * 64 * 4;   // float l_acc[128]: this CTA's keys' row sums
     static constexpr int kPxOff = kLaccOff + kN * 4;        // float px[2][128]: the peer's maxima
     static constexpr int kNfOff = kPxOff + 2 * kN * 4;      // float nflag[2] (16 B): the peer's flags
-    static constexpr int kLxOff = kNfOff + 16;              // float lx[128]: the peer's row sums
-    static constexpr int kLoOff = kLxOff + kN * 4;          // int lo_s[128]
+    static constexpr int kLxOff = kNfOff + 16;              // float lx[2][128]: the peer's row sums
+    static constexpr int kLoOff = kLxOff + 2 * kN * 4;      // int lo_s[128]
     static constexpr int kHiOff = kLoOff + kN * 4;          // int hi_s[128]
     static constexpr int kRowOff = kHiOff + kN * 4;         // int64 orow_s[128]
     static constexpr int kPidOff = kRowOff + kN * 8;        // int pid_s[4][kMaxPids]
@@ -219,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_free = s_full + 3;    // [kPBufs] PV of tile j done: P^T buffer j mod kPBufs is free
     uint64_t* nf_full = p_free + kPBufs;  // [2] the peer's "raise the maxima" flag of the tile (4 bytes)
     uint64_t* px_full = nf_full + 2;  // [2] the peer's 128 column maxima have landed (512 bytes)
-    uint64_t* lx_full = nf_full + 4;  // the peer's 128 row sums have landed (512 bytes)
-    uint64_t* drain = nf_full + 5;
+    uint64_t* lx_full = nf_full + 4;  // [2] the peer's 128 row sums of a unit have landed (512 bytes)
+    uint64_t* drain = nf_full + 6;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kMiscOff + 4);
     float* m_s = reinterpret_cast<float*>(smem + Lay::kMOff);
@@ -242,35 +277,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const bool leader = (rank == 0);
-    const int c_split = blockIdx.x >> 1;
-    const int b = blockIdx.z;
-    const int g = blockIdx.y / x.n_rg;
-    const int rg = blockIdx.y % x.n_rg;
+    const int pair_id = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
     const int T = p.T;
     const int Psz = p.page_size;
-    const int h0 = g * p.G + rg * x.Gc;
     const int rows_mine = x.Gc * x.Tb;  // Q rows this CTA loads (of its kHalf)
-
-    const int32_t L = __ldg(p.seq_lens + b);
-    const bool len_ok = seq_len_ok(p, L);
-    Chunk ch;
-    ch.kb = 0;
-    ch.ke = 0;
-    if (len_ok) ch = split_chunk(L, T, p.window, Psz, p.splits, c_split);
-    const int t0 = (ch.kb / Psz) * Psz;
-    const int ntiles = (ch.kb < ch.ke) ? (ch.ke - t0 + kPairKeys - 1) / kPairKeys : 0;
     const int pages_per_tile = kPairKeys / Psz;
-    const int chunk_pages = ntiles * pages_per_tile;
-    const int first_page = t0 / Psz;
 
     const int pw = warp - kProducerWarp;
     int32_t* pid_w = pid_s + (pw >= 0 && pw < kNumProducers ? pw : 0) * kMaxPids;
-    auto load_window = [&](int base) {
+    // page ids of the unit's relative pages [base, base + kMaxPids) -> this producer warp's pid_w;
+    // pages past the chunk and invalid ids map to the out-of-bounds coordinate num_pages
+    auto load_window = [&](const PairUnit& U, int base) {
         for (int k = lane; k < kMaxPids; k += 32) {
             const int pr = base + k;
             int32_t id = p.num_pages;  // out-of-bounds coordinate: the copy fills zeros
-            if (pr < chunk_pages && t0 + pr * Psz < ch.ke) {
-                const int32_t v = __ldg(p.page_table + (int64_t)b * p.max_pages + first_page + pr);
+            if (pr < U.chunk_pages && U.t0 + pr * Psz < U.ch.ke) {
+                const int32_t v = __ldg(p.page_table + (int64_t)U.b * p.max_pages + U.first_page + pr);
                 if (v >= 0 && v < p.num_pages)
                     id = v;
                 else
@@ -296,42 +319,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(px_full, 1);
         mbar_init(px_full + 1, 1);
         mbar_init(lx_full, 1);
+        mbar_init(lx_full + 1, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
-        if (!len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        // the exchange barriers of tiles 0 and 1 and of the row sums expect the peer's bytes
+        // the exchange barriers of tiles 0 and 1, and of the row sums of units 0 and 1, expect
+        // the peer's bytes
         mbar_expect_tx(nf_full, 4);
         mbar_expect_tx(nf_full + 1, 4);
         mbar_expect_tx(px_full, kN * 4);
         mbar_expect_tx(px_full + 1, kN * 4);
         mbar_expect_tx(lx_full, kN * 4);
+        mbar_expect_tx(lx_full + 1, kN * 4);
     }
-    if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
-        if (ntiles > 0) load_window(0);
-    } else if (warp == kMmaWarp) {
+    if (warp == kMmaWarp) {
         tmem_alloc2(tmem_slot, Lay::kTmemCols);
         tmem_relinquish2();
-    } else if (tid < kN) {
-        // column c of S^T / O^T: rows [0, 64) come from the even CTA's Q, [64, 128) from the odd's
-        const int hc = tid / kHalf, lr = tid % kHalf;
-        const int i = hc * x.Tb + lr / x.Gc, hh = lr % x.Gc;
-        int32_t lo = -(1 << 30), hi = (1 << 30);
-        int64_t orow = -1;
-        if (lr < rows_mine && i < T) {
-            const KeyRange kr = row_range(L, T, i, p.causal, p.window);
-            lo = kr.lo;
-            hi = kr.hi;
-            orow = (int64_t)(b * T + i) * p.Hq + (h0 + hh);
-        }
-        lo_s[tid] = lo;
-        hi_s[tid] = hi;
-        orow_s[tid] = orow;
-        m_s[tid] = -INFINITY;
-        a_s[tid] = 1.f;
-        l_acc[tid] = 0.f;
-    } else if (tid < kSoftmaxThreads) {
-        // zero this CTA's Q rows [rows_mine, kHalf) of every 64-dim chunk (the copy writes the rest)
+    } else if (tid >= kN && tid < kSoftmaxThreads) {
+        // zero this CTA's Q rows [rows_mine, kHalf) of every 64-dim chunk, once: every unit's
+        // copy writes the same rows [0, rows_mine)
         const int pad = kHalf - rows_mine;
         for (int idx = tid - kN; idx < KC * pad * 8; idx += kSoftmaxThreads - kN) {
             const int kc = idx / (pad * 8);
@@ -350,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_s = tmem;                 // S^T buffers: columns [0, 128) and [128, 256)
     const uint32_t tmem_o = tmem + 2 * kN;        // O^T chunk c: columns [256 + 128c, ..)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    bool role_ok = true;
 
     auto load16 = [&](uint32_t taddr, uint32_t (&r16)[16]) {
         tmem_ld16(taddr, r16);
@@ -362,22 +367,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
         // ------------------------------------------------------------ TMA producers
+        // The ring runs on across units: stage seq of the whole sequence goes to slot seq mod S,
+        // and the first stage of each unit also carries the unit's Q.
         const uint32_t full0 = in_cta(full, 0);
         bool ok = true;
-        int wbase = 0;
         uint32_t issued_parity[S];
 #pragma unroll
         for (int s = 0; s < S; ++s) issued_parity[s] = 2;  // 2 = nothing outstanding
-        if (ntiles > 0) {
-            const int box = Psz * 128;  // bytes of one page x 64 dims
-            int seq = 0;
-            for (int k = 0; k < 2 * ntiles && ok; ++k) {
+        const int box = Psz * 128;  // bytes of one page x 64 dims
+        int seq = 0;
+        int last_k = -1;            // sequence number of the last K stage so far (reads Q)
+#pragma unroll 1
+        for (int unit = pair_id; unit < x.units && ok; unit += npairs) {
+            const PairUnit U = pair_unit(p, x, unit);
+            if (U.ntiles == 0) continue;
+            int wbase = 0;
+            load_window(U, 0);
+            const int seq0 = seq;
+#pragma unroll 1
+            for (int k = 0; k < 2 * U.ntiles && ok; ++k) {
                 bool is_k;
                 int tile;
-                pair_ring_unit(k, ntiles, is_k, tile);
+                pair_ring_unit(k, U.ntiles, is_k, tile);
                 const int n_st = is_k ? KC : 4 * VC2;
 #pragma unroll 1
                 for (int sq = 0; sq < n_st && ok; ++sq, ++seq) {
+                    const int prev_k = last_k;
+                    if (is_k) last_k = seq;
                     if (seq % kNumProducers != pw) continue;
                     // relative pages this stage reads: K: own 128 keys; V: quarter of 64 keys
                     const int rel0 = tile * pages_per_tile +
@@ -385,26 +401,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int npg = (is_k ? kOwnKeys : 64) / Psz;
                     if (rel0 < wbase || rel0 + npg > wbase + kMaxPids) {
                         wbase = rel0;
-                        load_window(wbase);
+                        load_window(U, wbase);
                     }
                     const int slot = seq % S;
                     const uint32_t ph = (uint32_t)((seq / S) & 1);
                     // a polling wait with a short sleep between polls: producers spinning flat out
                     // beside the softmax warps slow it down, and a suspending wait wakes late
                     if (lane == 0) ok = backoff_wait(empty + slot, ph ^ 1u, abort_flag, p.err, p.wait_ns);
+                    const bool with_q = (seq == seq0);
+                    // The unit's Q replaces the previous unit's: the pair MMAs of that unit's last
+                    // K stage must be done. The slot wait above covers stages up to seq - S.
+                    if (lane == 0 && ok && with_q && prev_k >= 0 && prev_k > seq - S)
+                        ok = backoff_wait(empty + prev_k % S, (uint32_t)((prev_k / S) & 1), abort_flag, p.err,
+                                          p.wait_ns);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     if (lane == 0) {
                         uint8_t* dst = ring + slot * kStageBytes;
-                        const bool with_q = (seq == 0);
                         // the even CTA expects both CTAs' bytes of the stage on its barrier
                         const uint32_t qbytes = with_q ? (uint32_t)(x.Gc * x.Tb * 128 * KC) : 0u;
                         if (leader) mbar_expect_tx(full + slot, 2u * (kStageBytes + qbytes));
                         const uint32_t fb = full0 + (uint32_t)(slot * 8);
                         if (with_q)
                             for (int kc = 0; kc < KC; ++kc)
-                                tma_load_3d_pair(q_s + kc * kHalf * 128, &tm_q, fb, kc * 64, h0,
-                                                 b * T + (int)rank * x.Tb);
+                                tma_load_3d_pair(q_s + kc * kHalf * 128, &tm_q, fb, kc * 64, U.h0,
+                                                 U.b * T + (int)rank * x.Tb);
                         // the stage's page ids go to registers before its copies are issued (each
                         // copy instruction is also a compiler memory barrier)
                         int32_t ids[8];
@@ -413,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (is_k) {
 #pragma unroll
                             for (int pg = 0; pg < 8; ++pg)
-                                if (pg < npg) tma_load_4d_pair(dst + pg * box, &tm_k, fb, sq * 64, g, 0, ids[pg]);
+                                if (pg < npg) tma_load_4d_pair(dst + pg * box, &tm_k, fb, sq * 64, U.g, 0, ids[pg]);
                         } else {
                             const int c = sq % VC2;
                             const int d0 = c * 256 + (int)rank * 128;
@@ -422,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (pg < npg)
 #pragma unroll
                                     for (int m = 0; m < 2; ++m)
-                                        tma_load_4d_pair(dst + m * 8192 + pg * box, &tm_v, fb, d0 + m * 64, g, 0,
+                                        tma_load_4d_pair(dst + m * 8192 + pg * box, &tm_v, fb, d0 + m * 64, U.g, 0,
                                                          ids[pg]);
                         }
                         issued_parity[slot] = ph;
@@ -449,40 +470,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-        role_ok = ok;
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
-        bool ok = true;
-        int seq = 0;
-        // V rows past seq_len in the sequence's last, partial page are zeroed before PV in both
-        // CTAs' copies of the stage (the zero probabilities there must not meet non-finite
-        // garbage); the peer's copy through distributed shared memory
-        auto zero_tail = [&](int tile, int q, uint32_t st_off) {
-            const int key0 = t0 + tile * kPairKeys + q * 64;
-            const int zlo = L - key0;
-            if (L % Psz != 0 && zlo > 0 && zlo < 64 && ch.ke == L) {
-                const int zhi = min(64, ((L + Psz - 1) / Psz) * Psz - key0);
-                const int rows = zhi - zlo;
-                const uint32_t peer_st = in_cta(smem + st_off, peer);
-                for (int idx = lane; idx < rows * 16; idx += 32) {
-                    const int m = idx / (rows * 8);
-                    const int rem = idx - m * rows * 8;
-                    const uint32_t off = (uint32_t)(m * 8192 + (zlo + rem / 8) * 128 + (rem % 8) * 16);
-                    *reinterpret_cast<uint4*>(smem + st_off + off) = make_uint4(0, 0, 0, 0);
-                    st_cluster_v4(peer_st + off, make_uint4(0, 0, 0, 0));
-                }
-                fence_proxy_async_cluster();
-            }
-            __syncwarp();
-        };
-        if (!leader) {
-            // the odd CTA's MMA warp has no role: the even CTA issues the pair MMAs
-        } else {
+        // Tiles are numbered across the pair's units (gj): the S^T buffer, the P^T buffer and
+        // the phases of s_full, p_full and p_free follow gj; the accumulate flags follow the
+        // tile's place in its unit.
+        if (leader) {
             constexpr uint32_t idesc_s = make_idesc(256, kN, 0, 0);  // S^T  = K . Q^T
             constexpr uint32_t idesc_o = make_idesc(256, kN, 1, 1);  // O^T += V^T . P^T
             const uint32_t q_addr = smem_u32(q_s);
             const uint32_t p_addr = smem_u32(smem + Lay::kPOff);
             const uint32_t ring_addr = smem_u32(ring);
+            bool ok = true;
+            int seq = 0;
+            int G = 0;  // tiles of the earlier units
             auto wait_lane0 = [&](uint64_t* bar, uint32_t par) -> bool {
                 bool got = true;
                 if (lane == 0) got = ring_wait_cluster(bar, par, abort_flag, p.err, p.wait_ns);
@@ -501,62 +502,92 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 ++seq;
             };
-            for (int k = 0; k < 2 * ntiles && ok; ++k) {
-                bool is_k;
-                int j;
-                pair_ring_unit(k, ntiles, is_k, j);
-                if (is_k) {
-                    // S^T(j) into buffer j mod 2: its previous tile j - 2 has been read by both
-                    // softmaxes (their P(j-2) was waited for by the V(j-2) unit)
-                    const uint32_t sb = tmem_s + (uint32_t)(j & 1) * kN;
 #pragma unroll 1
-                    for (int kc = 0; kc < KC && ok; ++kc) {
-                        uint32_t st;
-                        int slot;
-                        ok = next_stage(st, slot);
-                        if (!ok) break;
-                        tc_fence_after();
-                        if (lane == 0) {
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                tc_mma2(sb, sw128_desc(st + kk * 32, 16, 1024),
-                                        sw128_desc(q_addr + kc * kHalf * 128 + kk * 32, 16, 1024), idesc_s,
-                                        (kc > 0 || kk > 0) ? 1u : 0u);
+            for (int unit = pair_id; unit < x.units && ok; unit += npairs) {
+                const PairUnit U = pair_unit(p, x, unit);
+                if (U.ntiles == 0) continue;
+                // V rows past seq_len in the sequence's last, partial page are zeroed before PV in
+                // both CTAs' copies of the stage (the zero probabilities there must not meet
+                // non-finite garbage); the peer's copy through distributed shared memory
+                auto zero_tail = [&](int tile, int q, uint32_t st_off) {
+                    const int key0 = U.t0 + tile * kPairKeys + q * 64;
+                    const int zlo = U.L - key0;
+                    if (U.L % Psz != 0 && zlo > 0 && zlo < 64 && U.ch.ke == U.L) {
+                        const int zhi = min(64, ((U.L + Psz - 1) / Psz) * Psz - key0);
+                        const int rows = zhi - zlo;
+                        const uint32_t peer_st = in_cta(smem + st_off, peer);
+                        for (int idx = lane; idx < rows * 16; idx += 32) {
+                            const int m = idx / (rows * 8);
+                            const int rem = idx - m * rows * 8;
+                            const uint32_t off = (uint32_t)(m * 8192 + (zlo + rem / 8) * 128 + (rem % 8) * 16);
+                            *reinterpret_cast<uint4*>(smem + st_off + off) = make_uint4(0, 0, 0, 0);
+                            st_cluster_v4(peer_st + off, make_uint4(0, 0, 0, 0));
                         }
-                        release(slot);
+                        fence_proxy_async_cluster();
+                    }
+                    __syncwarp();
+                };
+#pragma unroll 1
+                for (int k = 0; k < 2 * U.ntiles && ok; ++k) {
+                    bool is_k;
+                    int j;
+                    pair_ring_unit(k, U.ntiles, is_k, j);
+                    const int gj = G + j;
+                    if (is_k) {
+                        // S^T(gj) into buffer gj mod 2: its previous tile gj - 2 has been read by
+                        // both softmaxes (their P(gj-2) was waited for by the V(gj-2) unit, which
+                        // comes earlier in the ring order, in this unit or the one before)
+                        const uint32_t sb = tmem_s + (uint32_t)(gj & 1) * kN;
+#pragma unroll 1
+                        for (int kc = 0; kc < KC && ok; ++kc) {
+                            uint32_t st;
+                            int slot;
+                            ok = next_stage(st, slot);
+                            if (!ok) break;
+                            tc_fence_after();
+                            if (lane == 0) {
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    tc_mma2(sb, sw128_desc(st + kk * 32, 16, 1024),
+                                            sw128_desc(q_addr + kc * kHalf * 128 + kk * 32, 16, 1024), idesc_s,
+                                            (kc > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            release(slot);
+                        }
+                        if (!ok) break;
+                        if (lane == 0) tc_commit2_both(s_full + (gj & 1));
+                        __syncwarp();
+                        continue;
+                    }
+                    ok = wait_lane0(p_full, (uint32_t)(gj & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t pb_addr = p_addr + (uint32_t)((gj % kPBufs) * Lay::kPBuf);
+#pragma unroll 1
+                    for (int q = 0; q < 4 && ok; ++q) {
+#pragma unroll 1
+                        for (int c = 0; c < VC2 && ok; ++c) {
+                            uint32_t st;
+                            int slot;
+                            ok = next_stage(st, slot);
+                            if (!ok) break;
+                            zero_tail(j, q, st - smem_u32(smem));
+                            tc_fence_after();
+                            if (lane == 0) {
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    tc_mma2(tmem_o + c * kN, sw128_desc(st + kk * 2048, 8192, 1024),
+                                            sw32_desc(pb_addr + q * Lay::kPQuarter + kk * 512, 2048, 256), idesc_o,
+                                            (j > 0 || q > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            release(slot);
+                        }
                     }
                     if (!ok) break;
-                    if (lane == 0) tc_commit2_both(s_full + (j & 1));
+                    if (lane == 0) tc_commit2_both(p_free + gj % kPBufs);
                     __syncwarp();
-                    continue;
                 }
-                ok = wait_lane0(p_full, (uint32_t)(j & 1));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t pb_addr = p_addr + (uint32_t)((j % kPBufs) * Lay::kPBuf);
-#pragma unroll 1
-                for (int q = 0; q < 4 && ok; ++q) {
-#pragma unroll 1
-                    for (int c = 0; c < VC2 && ok; ++c) {
-                        uint32_t st;
-                        int slot;
-                        ok = next_stage(st, slot);
-                        if (!ok) break;
-                        zero_tail(j, q, st - smem_u32(smem));
-                        tc_fence_after();
-                        if (lane == 0) {
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                tc_mma2(tmem_o + c * kN, sw128_desc(st + kk * 2048, 8192, 1024),
-                                        sw32_desc(pb_addr + q * Lay::kPQuarter + kk * 512, 2048, 256), idesc_o,
-                                        (j > 0 || q > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        release(slot);
-                    }
-                }
-                if (!ok) break;
-                if (lane == 0) tc_commit2_both(p_free + j % kPBufs);
-                __syncwarp();
+                G += U.ntiles;
             }
             // drain our MMAs before either CTA frees TMEM or leaves (they read both CTAs' memory)
             if (lane == 0) {
@@ -567,19 +598,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
         }
-        role_ok = ok;
+        // (the odd CTA's MMA warp has no role: the even CTA issues the pair MMAs)
     } else {
         // ------------------------------------------------------------ softmax (warps 0-7)
         const float sl2 = p.scale * kLog2e;
         const bool plain = (p.causal == 0 && p.window == 0);
-        // a key inside every row's range [max lo, min hi] needs no test per row
-        int lo_all = -(1 << 30), hi_all = (1 << 30);
-        if (!plain) {
-            for (int r = 0; r < kN; ++r) {
-                lo_all = max(lo_all, lo_s[r]);
-                hi_all = min(hi_all, hi_s[r]);
-            }
-        }
         const int kl = tid & 127;         // key lane of this CTA's 128 keys (TMEM lane)
         const int chh = tid >> 7;         // rows [64 chh, 64 chh + 64): the P^T buffer of CTA chh
         const int col0 = chh * kHalf;
@@ -596,9 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t p_full_bar = in_cta(p_full, 0);
         bool ok = true;
         int nx = 0;     // maxima exchanges so far (they happen only on tiles that raise a row max)
-        // row sums over this warp's 32 keys and all tiles so far: lane l holds the sum of row
-        // col0 + 16q + (l mod 16) in ls[q]
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        int G = 0;      // tiles of the earlier units: tile j of a unit is tile G + j of the pair
+        int un = 0;     // units done (the row-sum exchange buffer of unit un is un mod 2)
         const int lcol = col0 + (lane & 15);
         auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
             bool got = true;
@@ -609,253 +631,300 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto wait_pv = [&](int t) -> bool {
             return group_wait(p_free + t % kPBufs, (uint32_t)((t / kPBufs) & 1));
         };
-        for (int j = 0; j < ntiles && ok; ++j) {
-            if (!group_wait(s_full + (j & 1), (uint32_t)((j >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t sb = tmem_s + (uint32_t)(j & 1) * kN + lane_base + (uint32_t)col0;
-            const int key = t0 + j * kPairKeys + pk;
-            const bool kvalid = key >= ch.kb && key < ch.ke;
-            const bool allvis = plain || (key >= lo_all && key <= hi_all);
-            auto score = [&](uint32_t raw, int col) -> float {
-                bool vis = kvalid;
-                if (!allvis) vis = vis && key >= lo_s[col] && key <= hi_s[col];
-                return vis ? u2f(raw) * sl2 : -INFINITY;
-            };
-            // Every column of this key lane visible (all but the chunk's edge keys and the
-            // window's or the block's own few): no selects, and the scale folds into one FMA.
-            // The running maxima are then finite, since pass 1 raises any -inf one.
-            const bool open = kvalid && allvis;
-            // pass 1: does any score of this CTA exceed its row's running max by more than the
-            // threshold? Both CTAs exchange the answer (one word); only when either says yes
-            // do they form and exchange the column maxima, so both take the same update.
-            bool nd = false;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                float mv[16];
-                load_row16(m_s + col0 + q * 16, mv);
-                uint32_t r16[16];
-                load16(sb + q * 16, r16);
-                if (open) {
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) nd |= fmaf(u2f(r16[u]), sl2, -mv[u]) > kRescaleThresh;
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) nd |= score(r16[u], col0 + q * 16 + u) > mv[u] + kRescaleThresh;
+        for (int unit = pair_id; unit < x.units && ok; unit += npairs) {
+            const PairUnit U = pair_unit(p, x, unit);
+            if (tid == 0 && leader && !U.len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
+            // the unit's rows: column c of S^T / O^T is row c mod 64 of CTA c / 64's Q
+            if (tid < kN) {
+                const int hc = tid / kHalf, lr = tid % kHalf;
+                const int i = hc * x.Tb + lr / x.Gc, hh = lr % x.Gc;
+                int32_t lo = -(1 << 30), hi = (1 << 30);
+                int64_t orow = -1;
+                if (lr < rows_mine && i < T) {
+                    const KeyRange kr = row_range(U.L, T, i, p.causal, p.window);
+                    lo = kr.lo;
+                    hi = kr.hi;
+                    orow = (int64_t)(U.b * T + i) * p.Hq + (U.h0 + hh);
+                }
+                lo_s[tid] = lo;
+                hi_s[tid] = hi;
+                orow_s[tid] = orow;
+                m_s[tid] = -INFINITY;
+                a_s[tid] = 1.f;
+                l_acc[tid] = 0.f;
+            }
+            bar_sync_256();
+            // a key inside every row's range [max lo, min hi] needs no test per row
+            int lo_all = -(1 << 30), hi_all = (1 << 30);
+            if (!plain) {
+                for (int r = 0; r < kN; ++r) {
+                    lo_all = max(lo_all, lo_s[r]);
+                    hi_all = min(hi_all, hi_s[r]);
                 }
             }
-            nd = bar_or_256(nd);
-            if (tid == 0) st_async_f32(in_cta(nflag + (j & 1), peer), nd ? 1.f : 0.f, in_cta(nf_full + (j & 1), peer));
-            if (!group_wait(nf_full + (j & 1), (uint32_t)((j >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            const bool need = nd || nflag[j & 1] != 0.f;
-            // the flag of tile j has been read: expect the peer's flag of tile j + 2
-            if (tid == 0) mbar_expect_tx(nf_full + (j & 1), 4);
-            if (need) {
-                // column maxima over this warp's 32 keys (transposing shuffle reduction), then
-                // over this CTA's 128 keys, then with the peer's
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t r16[16];
-                    load16(sb + q * 16, r16);
-                    float v[16];
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) v[u] = score(r16[u], col0 + q * 16 + u);
-                    const float mx = pair_transpose_max16(v, lane);
-                    if (lane < 16) red[warp * 64 + q * 16 + lane] = mx;
-                }
-                bar_sync_256();
-                float mloc = -INFINITY;
-                if (tid < kN) {
-                    const int hc = tid >> 6, cl = tid & 63;
-                    mloc = fmaxf(fmaxf(red[(hc * 4 + 0) * 64 + cl], red[(hc * 4 + 1) * 64 + cl]),
-                                 fmaxf(red[(hc * 4 + 2) * 64 + cl], red[(hc * 4 + 3) * 64 + cl]));
-                    st_async_f32(in_cta(px + (nx & 1) * kN + tid, peer), mloc, in_cta(px_full + (nx & 1), peer));
-                }
-                if (!group_wait(px_full + (nx & 1), (uint32_t)((nx >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                if (tid < kN) {
-                    const float mx = fmaxf(mloc, px[(nx & 1) * kN + tid]);
-                    const float mo = m_s[tid];
-                    if (mx > mo + kRescaleThresh) {
-                        m_s[tid] = mx;
-                        a_s[tid] = (mo == -INFINITY) ? 0.f : ex2(mo - mx);
-                    } else {
-                        a_s[tid] = 1.f;
-                    }
-                }
-                bar_sync_256();
-                // px of this exchange has been read: expect the peer's maxima of exchange nx + 2
-                if (tid == 0) mbar_expect_tx(px_full + (nx & 1), kN * 4);
-                ++nx;
-                // the row sums so far follow the new maxima
-#pragma unroll
-                for (int q = 0; q < 4; ++q) ls[q] *= a_s[lcol + q * 16];
-                if (j > 0) {
-                    // O^T holds tiles < j once PV(j-1) is done: rescale it in TMEM
-                    if (!wait_pv(j - 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    constexpr int nsplit = 2 / VC2;  // warps w and w+4: one chunk each, or half the columns
-                    const int c = (warp >> 2) % VC2;
-#pragma unroll 1
-                    for (int q = (warp >> 2) / VC2; q < kN / 16; q += nsplit) {
-                        uint32_t r16[16];
-                        const uint32_t ta = tmem_o + c * kN + lane_base + q * 16;
-                        load16(ta, r16);
-                        float av[16];
-                        load_row16(a_s + q * 16, av);
-#pragma unroll
-                        for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * av[u]);
-                        tmem_st16(ta, r16);
-                    }
-                    tmem_st_wait();
-                }
-            }
-            if (j >= kPBufs) {
-                // the P^T buffer of tile j: PV(j - kPBufs) must have read it
-                if (!wait_pv(j - kPBufs)) {
+            // row sums over this warp's 32 keys and the unit's tiles so far: lane l holds the sum
+            // of row col0 + 16q + (l mod 16) in ls[q]
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < U.ntiles && ok; ++j) {
+                const int gj = G + j;
+                if (!group_wait(s_full + (gj & 1), (uint32_t)((gj >> 1) & 1))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-            }
-            // pass 2: P = exp2(s - m) as bf16 pairs into the P^T buffer of CTA chh, and the
-            // rounded P (what the PV MMA reads) summed over the warp's keys into the row sums.
-            // A rolled loop: the softmax's steady-state code stays small enough for the
-            // instruction cache.
+                const uint32_t sb = tmem_s + (uint32_t)(gj & 1) * kN + lane_base + (uint32_t)col0;
+                const int key = U.t0 + j * kPairKeys + pk;
+                const bool kvalid = key >= U.ch.kb && key < U.ch.ke;
+                const bool allvis = plain || (key >= lo_all && key <= hi_all);
+                auto score = [&](uint32_t raw, int col) -> float {
+                    bool vis = kvalid;
+                    if (!allvis) vis = vis && key >= lo_s[col] && key <= hi_s[col];
+                    return vis ? u2f(raw) * sl2 : -INFINITY;
+                };
+                // Every column of this key lane visible (all but the chunk's edge keys and the
+                // window's or the block's own few): no selects, and the scale folds into one FMA.
+                // The running maxima are then finite, since pass 1 raises any -inf one.
+                const bool open = kvalid && allvis;
+                // pass 1: does any score of this CTA exceed its row's running max by more than the
+                // threshold? Both CTAs exchange the answer (one word); only when either says yes
+                // do they form and exchange the column maxima, so both take the same update.
+                bool nd = false;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                float mv[16];
-                load_row16(m_s + col0 + q * 16, mv);
-                uint32_t r16[16];
-                load16(sb + q * 16, r16);
-                float e[16];
-                if (open) {
+                for (int q = 0; q < 4; ++q) {
+                    float mv[16];
+                    load_row16(m_s + col0 + q * 16, mv);
+                    uint32_t r16[16];
+                    load16(sb + q * 16, r16);
+                    if (open) {
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) e[u] = ex2(fmaf(u2f(r16[u]), sl2, -mv[u]));
-                } else {
+                        for (int u = 0; u < 16; ++u) nd |= fmaf(u2f(r16[u]), sl2, -mv[u]) > kRescaleThresh;
+                    } else {
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const float sv = score(r16[u], col0 + q * 16 + u);
-                        e[u] = (sv == -INFINITY) ? 0.f : ex2(sv - mv[u]);
+                        for (int u = 0; u < 16; ++u) nd |= score(r16[u], col0 + q * 16 + u) > mv[u] + kRescaleThresh;
                     }
                 }
-                uint32_t pk2[8];
-                float pr[16];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[2 * u], e[2 * u + 1]);
-                    pk2[u] = *reinterpret_cast<const uint32_t*>(&h2);
-                    pr[2 * u] = __low2float(h2);
-                    pr[2 * u + 1] = __high2float(h2);
+                nd = bar_or_256(nd);
+                if (tid == 0)
+                    st_async_f32(in_cta(nflag + (gj & 1), peer), nd ? 1.f : 0.f, in_cta(nf_full + (gj & 1), peer));
+                if (!group_wait(nf_full + (gj & 1), (uint32_t)((gj >> 1) & 1))) {
+                    ok = false;
+                    break;
                 }
-                const uint32_t dst = prow0 + (uint32_t)((j % kPBufs) * Lay::kPBuf + q * 2048);
-                const uint4 lo4 = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
-                const uint4 hi4 = make_uint4(pk2[4], pk2[5], pk2[6], pk2[7]);
-                if (p_local) {
-                    uint8_t* d8 = smem + (dst - smem_u32(smem));
-                    *reinterpret_cast<uint4*>(d8 + pswz0) = lo4;
-                    *reinterpret_cast<uint4*>(d8 + pswz1) = hi4;
-                } else {
-                    st_cluster_v4(dst + pswz0, lo4);
-                    st_cluster_v4(dst + pswz1, hi4);
-                }
-                const float sm = pair_transpose_sum16(pr, lane);
+                const bool need = nd || nflag[gj & 1] != 0.f;
+                // the flag of tile gj has been read: expect the peer's flag of tile gj + 2
+                if (tid == 0) mbar_expect_tx(nf_full + (gj & 1), 4);
+                if (need) {
+                    // column maxima over this warp's 32 keys (transposing shuffle reduction), then
+                    // over this CTA's 128 keys, then with the peer's
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t r16[16];
+                        load16(sb + q * 16, r16);
+                        float v[16];
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq)
-                    if (qq == q) ls[qq] += sm;
+                        for (int u = 0; u < 16; ++u) v[u] = score(r16[u], col0 + q * 16 + u);
+                        const float mx = pair_transpose_max16(v, lane);
+                        if (lane < 16) red[warp * 64 + q * 16 + lane] = mx;
+                    }
+                    bar_sync_256();
+                    float mloc = -INFINITY;
+                    if (tid < kN) {
+                        const int hc = tid >> 6, cl = tid & 63;
+                        mloc = fmaxf(fmaxf(red[(hc * 4 + 0) * 64 + cl], red[(hc * 4 + 1) * 64 + cl]),
+                                     fmaxf(red[(hc * 4 + 2) * 64 + cl], red[(hc * 4 + 3) * 64 + cl]));
+                        st_async_f32(in_cta(px + (nx & 1) * kN + tid, peer), mloc, in_cta(px_full + (nx & 1), peer));
+                    }
+                    if (!group_wait(px_full + (nx & 1), (uint32_t)((nx >> 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    if (tid < kN) {
+                        const float mx = fmaxf(mloc, px[(nx & 1) * kN + tid]);
+                        const float mo = m_s[tid];
+                        if (mx > mo + kRescaleThresh) {
+                            m_s[tid] = mx;
+                            a_s[tid] = (mo == -INFINITY) ? 0.f : ex2(mo - mx);
+                        } else {
+                            a_s[tid] = 1.f;
+                        }
+                    }
+                    bar_sync_256();
+                    // px of this exchange has been read: expect the peer's maxima of exchange nx + 2
+                    if (tid == 0) mbar_expect_tx(px_full + (nx & 1), kN * 4);
+                    ++nx;
+                    // the row sums so far follow the new maxima
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) ls[q] *= a_s[lcol + q * 16];
+                    if (j > 0) {
+                        // O^T holds the unit's tiles < j once PV(gj-1) is done: rescale it in TMEM
+                        if (!wait_pv(gj - 1)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        constexpr int nsplit = 2 / VC2;  // warps w and w+4: one chunk each, or half the columns
+                        const int c = (warp >> 2) % VC2;
+#pragma unroll 1
+                        for (int q = (warp >> 2) / VC2; q < kN / 16; q += nsplit) {
+                            uint32_t r16[16];
+                            const uint32_t ta = tmem_o + c * kN + lane_base + q * 16;
+                            load16(ta, r16);
+                            float av[16];
+                            load_row16(a_s + q * 16, av);
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) r16[u] = f2u(u2f(r16[u]) * av[u]);
+                            tmem_st16(ta, r16);
+                        }
+                        tmem_st_wait();
+                    }
+                }
+                if (gj >= kPBufs) {
+                    // the P^T buffer of tile gj: PV(gj - kPBufs) must have read it
+                    if (!wait_pv(gj - kPBufs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                // pass 2: P = exp2(s - m) as bf16 pairs into the P^T buffer of CTA chh, and the
+                // rounded P (what the PV MMA reads) summed over the warp's keys into the row sums.
+                // A rolled loop: the softmax's steady-state code stays small enough for the
+                // instruction cache.
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    float mv[16];
+                    load_row16(m_s + col0 + q * 16, mv);
+                    uint32_t r16[16];
+                    load16(sb + q * 16, r16);
+                    float e[16];
+                    if (open) {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) e[u] = ex2(fmaf(u2f(r16[u]), sl2, -mv[u]));
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const float sv = score(r16[u], col0 + q * 16 + u);
+                            e[u] = (sv == -INFINITY) ? 0.f : ex2(sv - mv[u]);
+                        }
+                    }
+                    uint32_t pk2[8];
+                    float pr[16];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[2 * u], e[2 * u + 1]);
+                        pk2[u] = *reinterpret_cast<const uint32_t*>(&h2);
+                        pr[2 * u] = __low2float(h2);
+                        pr[2 * u + 1] = __high2float(h2);
+                    }
+                    const uint32_t dst = prow0 + (uint32_t)((gj % kPBufs) * Lay::kPBuf + q * 2048);
+                    const uint4 lo4 = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
+                    const uint4 hi4 = make_uint4(pk2[4], pk2[5], pk2[6], pk2[7]);
+                    if (p_local) {
+                        uint8_t* d8 = smem + (dst - smem_u32(smem));
+                        *reinterpret_cast<uint4*>(d8 + pswz0) = lo4;
+                        *reinterpret_cast<uint4*>(d8 + pswz1) = hi4;
+                    } else {
+                        st_cluster_v4(dst + pswz0, lo4);
+                        st_cluster_v4(dst + pswz1, hi4);
+                    }
+                    const float sm = pair_transpose_sum16(pr, lane);
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq)
+                        if (qq == q) ls[qq] += sm;
+                }
+                // every thread's P stores are made visible to the tensor cores (a warp writes
+                // either only its own CTA's buffer, which needs the CTA-scope fence alone, or only
+                // the peer's) and its TMEM reads are ordered before the next MMAs; one thread of
+                // each CTA then tells the even CTA. (An arrive per warp measured slower: each
+                // cluster-scope release costs about what the barrier saves.)
+                if (p_local)
+                    fence_proxy_async_smem();
+                else
+                    fence_proxy_async_cluster();
+                tc_fence_before();
+                bar_sync_256();
+                if (tid == 0) mbar_arrive_cluster(p_full_bar);
             }
-            // every thread's P stores are made visible to the tensor cores (a warp writes
-            // either only its own CTA's buffer, which needs the CTA-scope fence alone, or only
-            // the peer's) and its TMEM reads are ordered before the next MMAs; one thread of
-            // each CTA then tells the even CTA. (An arrive per warp measured slower: each
-            // cluster-scope release costs about what the barrier saves.)
-            if (p_local)
-                fence_proxy_async_smem();
-            else
-                fence_proxy_async_cluster();
+            // the row sums over this CTA's keys: across the 4 warps of each half of the rows
+            if (ok && U.ntiles > 0 && lane < 16) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) red2[warp * 64 + q * 16 + lane] = ls[q];
+            }
+            bar_sync_256();
+            if (ok && U.ntiles > 0 && tid < kN) {
+                const int hc = tid >> 6, cl = tid & 63;
+                l_acc[tid] = (red2[(hc * 4 + 0) * 64 + cl] + red2[(hc * 4 + 1) * 64 + cl]) +
+                             (red2[(hc * 4 + 2) * 64 + cl] + red2[(hc * 4 + 3) * 64 + cl]);
+            }
+            bool have_o = ok && U.ntiles > 0;
+            if (have_o) have_o = ok = wait_pv(G + U.ntiles - 1);
+
+            // ------------------------------------------------------------ the unit's epilogue
+            tc_fence_after();
+            // row sums: this CTA's keys' part to the peer, the peer's part from it (two buffers:
+            // the peer may send the next unit's before this CTA has read this one's)
+            const int lb = un & 1;
+            if (tid < kN)
+                st_async_f32(in_cta(lx + lb * kN + tid, peer), have_o ? l_acc[tid] : 0.f, in_cta(lx_full + lb, peer));
+            {
+                bool got = true;
+                if (tid == 0) got = ring_wait_cluster(lx_full + lb, (uint32_t)((un >> 1) & 1), abort_flag, p.err, p.wait_ns);
+                if (bar_or_256(!got)) ok = false;
+            }
+            const int64_t part_base = (int64_t)U.c_split * p.B * p.T * p.Hq;
+            const bool final_out = (p.splits == 1);
+            if (tid < kN) {
+                const float tot = (have_o ? l_acc[tid] : 0.f) + lx[lb * kN + tid];
+                a_s[tid] = tot > 0.f ? 1.f / tot : 0.f;
+                // each CTA writes the lse of half of the rows
+                if ((tid >> 6) == (int)rank && orow_s[tid] >= 0) {
+                    const float lse_v = tot > 0.f ? (m_s[tid] + __log2f(tot)) * kLn2 : -INFINITY;
+                    if (final_out) {
+                        if (p.lse) p.lse[orow_s[tid]] = lse_v;
+                    } else {
+                        p.part_lse[part_base + orow_s[tid]] = lse_v;
+                    }
+                }
+            }
+            bar_sync_256();
+            // this unit's row sums have been read: expect the peer's of unit un + 2
+            if (tid == 0) mbar_expect_tx(lx_full + lb, kN * 4);
+            // O^T: warp w reads TMEM lanes 32(w%4).. = dims of chunk c; each column is one output
+            // row, and the warp's 32 lanes store 32 consecutive dims of it
+            {
+                constexpr int nsplit = 2 / VC2;
+                const int c = (warp >> 2) % VC2;
+                const int d = c * 256 + (int)rank * 128 + (warp & 3) * 32 + lane;
+#pragma unroll 1
+                for (int q = (warp >> 2) / VC2; q < kN / 16; q += nsplit) {
+                    uint32_t r16[16];
+                    if (have_o) {
+                        load16(tmem_o + c * kN + lane_base + q * 16, r16);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) r16[e] = 0u;
+                    }
+                    float iv[16];
+                    load_row16(a_s + q * 16, iv);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int64_t orow = orow_s[q * 16 + e];
+                        if (orow < 0) continue;
+                        const float v = u2f(r16[e]) * iv[e];
+                        if (final_out)
+                            static_cast<__nv_bfloat16*>(p.out)[orow * D + d] = __float2bfloat16_rn(v);
+                        else
+                            p.part_out[(part_base + orow) * D + d] = v;
+                    }
+                }
+            }
+            // the read-out is done with O^T (the next unit's first PV overwrites it only after this
+            // CTA's P of that unit's first tile) and with the tables the next unit rewrites
             tc_fence_before();
             bar_sync_256();
-            if (tid == 0) mbar_arrive_cluster(p_full_bar);
-        }
-        // the row sums over this CTA's keys: across the 4 warps of each half of the rows
-        if (ok && ntiles > 0 && lane < 16) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) red2[warp * 64 + q * 16 + lane] = ls[q];
-        }
-        bar_sync_256();
-        if (ok && ntiles > 0 && tid < kN) {
-            const int hc = tid >> 6, cl = tid & 63;
-            l_acc[tid] = (red2[(hc * 4 + 0) * 64 + cl] + red2[(hc * 4 + 1) * 64 + cl]) +
-                         (red2[(hc * 4 + 2) * 64 + cl] + red2[(hc * 4 + 3) * 64 + cl]);
-        }
-        bool good = ok && ntiles > 0;
-        if (good) good = wait_pv(ntiles - 1);
-        role_ok = good;
-    }
-
-    // ---------------------------------------------------------------- epilogue (warps 0-7)
-    if (warp < 8) {
-        const bool have_o = !bar_or_256(!role_ok) && ntiles > 0;
-        tc_fence_after();
-        // row sums: this CTA's keys' part to the peer, the peer's part from it
-        if (tid < kN) st_async_f32(in_cta(lx + tid, peer), have_o ? l_acc[tid] : 0.f, in_cta(lx_full, peer));
-        {
-            bool got = true;
-            if (tid == 0) got = ring_wait_cluster(lx_full, 0, abort_flag, p.err, p.wait_ns);
-            bar_or_256(!got);
-        }
-        const int64_t part_base = (int64_t)c_split * p.B * p.T * p.Hq;
-        const bool final_out = (p.splits == 1);
-        if (tid < kN) {
-            const float tot = (have_o ? l_acc[tid] : 0.f) + lx[tid];
-            a_s[tid] = tot > 0.f ? 1.f / tot : 0.f;
-            // each CTA writes the lse of half of the rows
-            if ((tid >> 6) == (int)rank && orow_s[tid] >= 0) {
-                const float lse_v = tot > 0.f ? (m_s[tid] + __log2f(tot)) * kLn2 : -INFINITY;
-                if (final_out) {
-                    if (p.lse) p.lse[orow_s[tid]] = lse_v;
-                } else {
-                    p.part_lse[part_base + orow_s[tid]] = lse_v;
-                }
-            }
-        }
-        bar_sync_256();
-        // O^T: warp w reads TMEM lanes 32(w%4).. = dims of chunk c; each column is one output
-        // row, and the warp's 32 lanes store 32 consecutive dims of it
-        constexpr int nsplit = 2 / VC2;
-        const int c = (warp >> 2) % VC2;
-        const int d = c * 256 + (int)rank * 128 + (warp & 3) * 32 + lane;
-#pragma unroll 1
-        for (int q = (warp >> 2) / VC2; q < kN / 16; q += nsplit) {
-            uint32_t r16[16];
-            if (have_o) {
-                load16(tmem_o + c * kN + lane_base + q * 16, r16);
-            } else {
-#pragma unroll
-                for (int u = 0; u < 16; ++u) r16[u] = 0u;
-            }
-            float iv[16];
-            load_row16(a_s + q * 16, iv);
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int64_t orow = orow_s[q * 16 + u];
-                if (orow < 0) continue;
-                const float v = u2f(r16[u]) * iv[u];
-                if (final_out)
-                    static_cast<__nv_bfloat16*>(p.out)[orow * D + d] = __float2bfloat16_rn(v);
-                else
-                    p.part_out[(part_base + orow) * D + d] = v;
-            }
+            G += U.ntiles;
+            ++un;
         }
     }
 
@@ -890,16 +959,56 @@ EncodeTiledFn pair_encode_fn()
     return fn;
 }
 
+// CTA pairs of tc_pair_attn_kernel<D> that fit the device at once (cached per device).
+template <int D>
+cudaError_t pair_resident_pairs(int* pairs)
+{
+    using Lay = PairLayout<D>;
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cached[dev] == 0) {
+        auto kern = tc_pair_attn_kernel<D>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = Lay::kAlloc;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        cached[dev] = n > 0 ? n : 1;
+    }
+    *pairs = cached[dev];
+    return cudaSuccess;
+}
+
+// A persistent grid: one CTA pair per cluster slot the device holds at once (or one per unit
+// when there are fewer units), each pair looping over its units.
 template <int D>
 cudaError_t launch_pair_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
                           const PairExtra& x, cudaStream_t stream)
 {
     using Lay = PairLayout<D>;
     auto kern = tc_pair_attn_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+    int pairs = 0;
+    cudaError_t e = pair_resident_pairs<D>(&pairs);
     if (e != cudaSuccess) return e;
+    pairs = std::min(pairs, x.units);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * p.splits, p.Hkv * x.n_rg, p.B);
+    cfg.gridDim = dim3(2 * pairs);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Lay::kAlloc;
     cfg.stream = stream;
@@ -941,6 +1050,18 @@ int tc_pair_ctas_per_split(const AttnParams& p)
     return gc > 0 ? 2 * p.B * p.Hkv * (p.G / gc) : 0;
 }
 
+cudaError_t tc_pair_grid_ctas(const AttnParams& p, int64_t* ctas)
+{
+    const int gc = pair_choose_gc(p.G, p.T);
+    if (gc <= 0) return cudaErrorNotSupported;
+    const int64_t units = (int64_t)p.splits * p.Hkv * (p.G / gc) * p.B;
+    int pairs = 0;
+    cudaError_t e = (p.D == 512) ? pair_resident_pairs<512>(&pairs) : pair_resident_pairs<256>(&pairs);
+    if (e != cudaSuccess) return e;
+    *ctas = 2 * std::min<int64_t>(pairs, units);
+    return cudaSuccess;
+}
+
 int tc_pair_row_groups(const AttnParams& p)
 {
     const int gc = pair_choose_gc(p.G, p.T);
@@ -956,6 +1077,9 @@ cudaError_t launch_tc_pair_attn(const AttnParams& p, cudaStream_t stream)
     x.Gc = pair_choose_gc(p.G, p.T);
     x.n_rg = p.G / x.Gc;
     x.Tb = (p.T + 1) / 2;
+    const int64_t units = (int64_t)p.splits * p.Hkv * x.n_rg * p.B;
+    if (units > (int64_t)INT32_MAX) return cudaErrorNotSupported;
+    x.units = (int32_t)units;
 
     CUtensorMap tq, tk, tv;
     {

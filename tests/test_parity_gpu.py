@@ -265,7 +265,9 @@ def test_cta_pair_agrees_with_the_single_cta_kernel():
     assert dfl.plan_info(dims, case.block_len, 0, 0, "auto")["kernel_name"] == "tc_pair_attn_kernel"
     plan = dfl.plan_info(dims, case.block_len, 0, 0, "tc_pair")
     assert plan["kernel_name"] == "tc_pair_attn_kernel" and not plan["balanced"]
-    assert plan["ctas"] == 2 * case.batch * case.num_kv_heads * plan["num_splits"]
+    # a persistent grid of CTA pairs: one per unit, or one per cluster slot when there are more
+    units = case.batch * case.num_kv_heads * plan["num_splits"]
+    assert plan["ctas"] % 2 == 0 and 2 <= plan["ctas"] <= 2 * units
     out, lse = run(case, kernel="tc_pair", num_splits=0)
     check_full(case, out, lse)
     a, la = run(case, kernel="tc", num_splits=plan["num_splits"])
@@ -285,6 +287,27 @@ def test_cta_pair_shapes(T, Hq, Hkv, D, causal, window):
     for splits in (1, 3):
         out, lse = run(case, kernel="tc_pair", num_splits=splits)
         check_full(case, out, lse)
+
+
+@pytest.mark.parametrize("D,Hkv,causal,window", [(512, 4, False, 0), (256, 4, True, 0), (512, 4, False, 700)])
+def test_cta_pair_many_units_per_pair(D, Hkv, causal, window):
+    # more (request, KV head, chunk) units than the device holds CTA pairs, so each pair runs
+    # several units back to back with its ring, barriers and TMEM carried over; ragged lengths
+    # leave some chunks with no keys at all (units without tiles)
+    lens = [40, 3000, 17, 9000, 300, 5000, 64, 1200]
+    case = workloads.make_custom("pairmany", 8, 16, 32, Hkv, D, lens, causal=causal, window=window,
+                                 seed=45 + D, device="cuda")
+    maybe_skip(case, "tc_pair")
+    dims = dfl.make_dims(case.q, case.k_cache, case.page_table, case.block_len)
+    splits = 12
+    plan = dfl.plan_info(dims, case.block_len, window, splits, "tc_pair")
+    units = case.batch * Hkv * splits
+    assert plan["ctas"] < 2 * units, plan  # pairs take more than one unit each
+    out, lse = run(case, kernel="tc_pair", num_splits=splits)
+    check_full(case, out, lse)
+    # the same call again on the same grid (the barriers' phases start over per launch)
+    out2, lse2 = run(case, kernel="tc_pair", num_splits=splits)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
 
 
 def test_cta_pair_garbage_beyond_seq_len_does_not_leak():
