@@ -891,11 +891,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // this unit's row sums have been read: expect the peer's of unit un + 2
             if (tid == 0) mbar_expect_tx(lx_full + lb, kN * 4);
             // O^T: warp w reads TMEM lanes 32(w%4).. = dims of chunk c; each column is one output
-            // row, and the warp's 32 lanes store 32 consecutive dims of it
+            // row. A warp's 16 rows x 32 dims go through a 2 KB scratch in the idle P^T buffers
+            // (the peer writes this CTA's P^T again only after this CTA's next raise flag), so
+            // that each lane stores 4 consecutive dims of a row: 4 stores of 16 bytes per lane
+            // per 16 rows in place of 16 of 4 bytes.
             {
                 constexpr int nsplit = 2 / VC2;
                 const int c = (warp >> 2) % VC2;
-                const int d = c * 256 + (int)rank * 128 + (warp & 3) * 32 + lane;
+                const int dbase = c * 256 + (int)rank * 128 + (warp & 3) * 32;
+                float* scr = reinterpret_cast<float*>(smem + Lay::kPOff) + warp * 512;  // [16 rows][32 dims]
+                const int er = lane >> 3;        // row within a group of 4 this lane stores
+                const int dq = (lane & 7) * 4;   // its 4 dims within the warp's 32
 #pragma unroll 1
                 for (int q = (warp >> 2) / VC2; q < kN / 16; q += nsplit) {
                     uint32_t r16[16];
@@ -907,15 +913,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     float iv[16];
                     load_row16(a_s + q * 16, iv);
+                    // the output indices of this lane's 4 rows go to registers before any global
+                    // store (a store through a global pointer may alias shared memory for the
+                    // compiler, which would keep each later shared load behind it)
+                    int64_t orows[4];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int64_t orow = orow_s[q * 16 + e];
+                    for (int s4 = 0; s4 < 4; ++s4) orows[s4] = orow_s[q * 16 + 4 * s4 + er];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) scr[e * 32 + lane] = u2f(r16[e]) * iv[e];
+                    __syncwarp();
+                    float4 v4[4];
+#pragma unroll
+                    for (int s4 = 0; s4 < 4; ++s4)
+                        v4[s4] = *reinterpret_cast<const float4*>(scr + (4 * s4 + er) * 32 + dq);
+                    __syncwarp();
+#pragma unroll
+                    for (int s4 = 0; s4 < 4; ++s4) {
+                        const int64_t orow = orows[s4];
                         if (orow < 0) continue;
-                        const float v = u2f(r16[e]) * iv[e];
-                        if (final_out)
-                            static_cast<__nv_bfloat16*>(p.out)[orow * D + d] = __float2bfloat16_rn(v);
-                        else
-                            p.part_out[(part_base + orow) * D + d] = v;
+                        if (final_out) {
+                            const __nv_bfloat162 lo = __floats2bfloat162_rn(v4[s4].x, v4[s4].y);
+                            const __nv_bfloat162 hi = __floats2bfloat162_rn(v4[s4].z, v4[s4].w);
+                            uint2 pk;
+                            pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+                            pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+                            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + orow * D + dbase + dq) = pk;
+                        } else {
+                            *reinterpret_cast<float4*>(p.part_out + (part_base + orow) * D + dbase + dq) = v4[s4];
+                        }
                     }
                 }
             }
