@@ -857,16 +857,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l_acc[tid] = (red2[(hc * 4 + 0) * 64 + cl] + red2[(hc * 4 + 1) * 64 + cl]) +
                              (red2[(hc * 4 + 2) * 64 + cl] + red2[(hc * 4 + 3) * 64 + cl]);
             }
-            bool have_o = ok && U.ntiles > 0;
-            if (have_o) have_o = ok = wait_pv(G + U.ntiles - 1);
-
             // ------------------------------------------------------------ the unit's epilogue
-            tc_fence_after();
+            // The row sums and the lse need only the softmax's own results: they are exchanged
+            // and written while the last PV of the unit is still running.
+            const bool have_l = ok && U.ntiles > 0;
             // row sums: this CTA's keys' part to the peer, the peer's part from it (two buffers:
             // the peer may send the next unit's before this CTA has read this one's)
             const int lb = un & 1;
             if (tid < kN)
-                st_async_f32(in_cta(lx + lb * kN + tid, peer), have_o ? l_acc[tid] : 0.f, in_cta(lx_full + lb, peer));
+                st_async_f32(in_cta(lx + lb * kN + tid, peer), have_l ? l_acc[tid] : 0.f, in_cta(lx_full + lb, peer));
             {
                 bool got = true;
                 if (tid == 0) got = ring_wait_cluster(lx_full + lb, (uint32_t)((un >> 1) & 1), abort_flag, p.err, p.wait_ns);
@@ -875,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t part_base = (int64_t)U.c_split * p.B * p.T * p.Hq;
             const bool final_out = (p.splits == 1);
             if (tid < kN) {
-                const float tot = (have_o ? l_acc[tid] : 0.f) + lx[lb * kN + tid];
+                const float tot = (have_l ? l_acc[tid] : 0.f) + lx[lb * kN + tid];
                 a_s[tid] = tot > 0.f ? 1.f / tot : 0.f;
                 // each CTA writes the lse of half of the rows
                 if ((tid >> 6) == (int)rank && orow_s[tid] >= 0) {
@@ -890,6 +889,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bar_sync_256();
             // this unit's row sums have been read: expect the peer's of unit un + 2
             if (tid == 0) mbar_expect_tx(lx_full + lb, kN * 4);
+            bool have_o = have_l;
+            if (have_o) have_o = ok = wait_pv(G + U.ntiles - 1);
+            tc_fence_after();
             // O^T: warp w reads TMEM lanes 32(w%4).. = dims of chunk c; each column is one output
             // row. A warp's 16 rows x 32 dims go through a 2 KB scratch in the idle P^T buffers
             // (the peer writes this CTA's P^T again only after this CTA's next raise flag), so
