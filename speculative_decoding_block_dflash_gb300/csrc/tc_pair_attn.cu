@@ -84,9 +84,9 @@ struct PairExtra {
     int32_t units;  // (request, KV head, row group, chunk) units: splits * Hkv * n_rg * B
 };
 
-// One unit of work of a CTA pair: a (request, KV head, row group, key chunk). Pair i of the
-// persistent grid takes units i, i + pairs, i + 2 pairs, ...; unit u is chunk u mod splits of
-// row-group slot (u / splits) mod (Hkv n_rg) of request u / (splits Hkv n_rg).
+// One unit of work of a CTA pair: a (request, KV head, row group, key chunk). Unit u is chunk
+// u mod splits of row-group slot (u / splits) mod (Hkv n_rg) of request u / (splits Hkv n_rg);
+// the units of one (request, row group) form group u / splits.
 struct PairUnit {
     int32_t b, g, c_split, h0;
     int32_t L;
@@ -95,7 +95,75 @@ struct PairUnit {
     int32_t t0, ntiles, chunk_pages, first_page;
 };
 
-__device__ __forceinline__ PairUnit pair_unit(const AttnParams& p, const PairExtra& x, int u)
+// How units are dealt to the P pairs of the persistent grid. With U = qP + r units and r > 0,
+// dealing them round-robin leaves P - r pairs idle for the last round. With split chunks
+// (splits > 1) the chunks are instead sized by who runs them: r "small" pairs take q + 1 units
+// each and P - r "large" pairs q units, and within every group the chunks of large pairs get
+// q + 1 tiles for every q of the small pairs' chunks, so every pair streams about U/P units of
+// keys. The large pairs' (P - r) q chunks are spread evenly over the groups, as the first
+// chunks of each group; every chunk keeps its own partial slot, so the split combine is
+// unchanged. (Uniform chunks on long_draft's 512 units over 76 pairs left 20 pairs idle for
+// one unit of the seven.)
+struct PairPlan {
+    int32_t npairs, q, r, groups, large;
+    bool balanced;
+};
+
+__device__ __forceinline__ PairPlan pair_plan(const AttnParams& p, const PairExtra& x)
+{
+    PairPlan pp;
+    pp.npairs = (int32_t)(gridDim.x >> 1);
+    pp.q = x.units / pp.npairs;
+    pp.r = x.units % pp.npairs;
+    pp.groups = x.units / p.splits;
+    pp.balanced = p.splits > 1 && pp.r != 0 && pp.q >= 1;
+    pp.large = (pp.npairs - pp.r) * pp.q;
+    return pp;
+}
+
+// chunks of group gr dealt to large pairs (the group's first ones)
+__device__ __forceinline__ int32_t pair_large_in_group(const PairPlan& pp, int32_t gr)
+{
+    return (int32_t)(((int64_t)(gr + 1) * pp.large) / pp.groups - ((int64_t)gr * pp.large) / pp.groups);
+}
+
+// The k-th unit of pair `pr`, or -1 past its last.
+__device__ __forceinline__ int32_t pair_item(const AttnParams& p, const PairExtra& x, const PairPlan& pp, int32_t pr,
+                                             int32_t k)
+{
+    if (!pp.balanced) {
+        const int64_t u = (int64_t)pr + (int64_t)k * pp.npairs;
+        return u < x.units ? (int32_t)u : -1;
+    }
+    const int32_t S = p.splits;
+    if (pr >= pp.r) {
+        // large pair: large chunk i = (pr - r) q + k, in group order; group gr holds large
+        // chunks [floor(gr L / G), floor((gr + 1) L / G))
+        if (k >= pp.q) return -1;
+        const int64_t i = (int64_t)(pr - pp.r) * pp.q + k;
+        const int32_t gr = (int32_t)(((i + 1) * pp.groups + pp.large - 1) / pp.large) - 1;
+        const int32_t c = (int32_t)(i - ((int64_t)gr * pp.large) / pp.groups);
+        return c + S * gr;
+    }
+    // small pair: small chunk i = pr (q + 1) + k; group gr holds small chunks
+    // [gr S - floor(gr L / G), ...): the last group whose start is <= i, by bisection
+    if (k > pp.q) return -1;
+    const int64_t i = (int64_t)pr * (pp.q + 1) + k;
+    int32_t lo = 0, hi = pp.groups - 1;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        const int64_t start = (int64_t)mid * S - ((int64_t)mid * pp.large) / pp.groups;
+        if (start <= i)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int64_t start = (int64_t)lo * S - ((int64_t)lo * pp.large) / pp.groups;
+    const int32_t c = pair_large_in_group(pp, lo) + (int32_t)(i - start);
+    return c + S * lo;
+}
+
+__device__ __forceinline__ PairUnit pair_unit(const AttnParams& p, const PairExtra& x, const PairPlan& pp, int u)
 {
     PairUnit U;
     const int ys = p.Hkv * x.n_rg;
@@ -109,7 +177,36 @@ __device__ __forceinline__ PairUnit pair_unit(const AttnParams& p, const PairExt
     U.len_ok = seq_len_ok(p, U.L);
     U.ch.kb = 0;
     U.ch.ke = 0;
-    if (U.len_ok) U.ch = split_chunk(U.L, p.T, p.window, p.page_size, p.splits, U.c_split);
+    if (U.len_ok) {
+        if (!pp.balanced) {
+            U.ch = split_chunk(U.L, p.T, p.window, p.page_size, p.splits, U.c_split);
+        } else {
+            // the request's union key range [lo, L), cut at whole pair tiles from the page
+            // boundary below lo, in proportion to the chunks' weights (q + 1 for the group's
+            // first `nl` chunks, which large pairs run, and q for the rest)
+            int32_t lo = 0;
+            if (p.window > 0) {
+                lo = U.L - p.T - p.window + 1;
+                if (lo < 0) lo = 0;
+            }
+            const int32_t base = (lo / p.page_size) * p.page_size;
+            const int64_t ntot = (U.L - base + kPairKeys - 1) / kPairKeys;
+            const int32_t nl = pair_large_in_group(pp, u / p.splits);
+            const int64_t wq1 = pp.q + 1, wq = pp.q;
+            const int64_t wt = nl * wq1 + (int64_t)(p.splits - nl) * wq;
+            auto cum = [&](int32_t c) -> int64_t {
+                return c <= nl ? c * wq1 : nl * wq1 + (int64_t)(c - nl) * wq;
+            };
+            const int64_t t_b = (2 * ntot * cum(U.c_split) + wt) / (2 * wt);
+            const int64_t t_e = (2 * ntot * cum(U.c_split + 1) + wt) / (2 * wt);
+            int64_t kb = base + t_b * kPairKeys, ke = base + t_e * kPairKeys;
+            if (kb < lo) kb = lo;
+            if (ke > U.L) ke = U.L;
+            if (kb > U.L) kb = U.L;
+            U.ch.kb = (int32_t)kb;
+            U.ch.ke = (int32_t)ke;
+        }
+    }
     U.t0 = (U.ch.kb / p.page_size) * p.page_size;
     U.ntiles = (U.ch.kb < U.ch.ke) ? (U.ch.ke - U.t0 + kPairKeys - 1) / kPairKeys : 0;
     U.chunk_pages = U.ntiles * (kPairKeys / p.page_size);
@@ -278,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t peer = rank ^ 1u;
     const bool leader = (rank == 0);
     const int pair_id = blockIdx.x >> 1;
-    const int npairs = gridDim.x >> 1;
+    const PairPlan pp = pair_plan(p, x);
     const int T = p.T;
     const int Psz = p.page_size;
     const int rows_mine = x.Gc * x.Tb;  // Q rows this CTA loads (of its kHalf)
@@ -378,8 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int seq = 0;
         int last_k = -1;            // sequence number of the last K stage so far (reads Q)
 #pragma unroll 1
-        for (int unit = pair_id; unit < x.units && ok; unit += npairs) {
-            const PairUnit U = pair_unit(p, x, unit);
+        for (int k_unit = 0; ok; ++k_unit) {
+            const int unit = pair_item(p, x, pp, pair_id, k_unit);
+            if (unit < 0) break;
+            const PairUnit U = pair_unit(p, x, pp, unit);
             if (U.ntiles == 0) continue;
             int wbase = 0;
             load_window(U, 0);
@@ -503,8 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++seq;
             };
 #pragma unroll 1
-            for (int unit = pair_id; unit < x.units && ok; unit += npairs) {
-                const PairUnit U = pair_unit(p, x, unit);
+            for (int k_unit = 0; ok; ++k_unit) {
+                const int unit = pair_item(p, x, pp, pair_id, k_unit);
+                if (unit < 0) break;
+                const PairUnit U = pair_unit(p, x, pp, unit);
                 if (U.ntiles == 0) continue;
                 // V rows past seq_len in the sequence's last, partial page are zeroed before PV in
                 // both CTAs' copies of the stage (the zero probabilities there must not meet
@@ -632,8 +733,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             return group_wait(p_free + t % kPBufs, (uint32_t)((t / kPBufs) & 1));
         };
 #pragma unroll 1
-        for (int unit = pair_id; unit < x.units && ok; unit += npairs) {
-            const PairUnit U = pair_unit(p, x, unit);
+        for (int k_unit = 0; ok; ++k_unit) {
+            const int unit = pair_item(p, x, pp, pair_id, k_unit);
+            if (unit < 0) break;
+            const PairUnit U = pair_unit(p, x, pp, unit);
             if (tid == 0 && leader && !U.len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
             // the unit's rows: column c of S^T / O^T is row c mod 64 of CTA c / 64's Q
             if (tid < kN) {
