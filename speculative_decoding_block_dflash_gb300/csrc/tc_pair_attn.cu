@@ -10,7 +10,10 @@
 // half of the heads would each read every K/V byte.
 //
 // Here two CTAs of a cluster share one (request, KV head, key chunk) and every K/V byte
-// enters exactly one SM. A "pair tile" is 256 keys. The even CTA issues 2-SM MMAs:
+// enters exactly one SM. The grid is persistent: one pair per cluster slot the device holds
+// at once, each running its share of the (request, KV head, row group, chunk) units back to
+// back with its ring, barriers and TMEM carried over (see PairPlan for how units are dealt).
+// A "pair tile" is 256 keys. The even CTA issues 2-SM MMAs:
 //   S^T [256 keys x 128 rows]  = K [256 x D] . Q^T          A = K: each CTA streams its own
 //                                                            128 keys; B = Q^T: each CTA holds
 //                                                            its 64 rows of Q
@@ -42,6 +45,10 @@
 // their rings in the same order K(0) K(1) V(0) K(2) V(1) ... so a stage sits at the same
 // offset in both, as the pair MMA needs, and both CTAs' copies of a stage count their bytes on
 // one barrier in the even CTA (the 2-CTA form of the tensor copy), which alone waits on it.
+//
+// After a unit's last tile the softmax warps exchange the row sums with the peer, write the
+// lse, and read O^T out to the output or the split partials; the next unit's copies and S
+// MMAs run meanwhile, and its first PV waits for the read-out (it overwrites O^T).
 //
 // Every wait is bounded (p.wait_ns); on expiry the kernel records DFLASH_DEVERR_TIMEOUT,
 // drains its own copies and MMAs, and both CTAs still meet at the final cluster barrier
