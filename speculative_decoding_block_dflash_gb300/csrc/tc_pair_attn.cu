@@ -12,7 +12,8 @@
 // Here two CTAs of a cluster share one (request, KV head, key chunk) and every K/V byte
 // enters exactly one SM. The grid is persistent: one pair per cluster slot the device holds
 // at once, each running its share of the (request, KV head, row group, chunk) units back to
-// back with its ring, barriers and TMEM carried over (see PairPlan for how units are dealt).
+// back with its ring, barriers and TMEM carried over (see PairPlan for how units are dealt;
+// a pair's consecutive chunks of one group run as one piece, with one epilogue).
 // A "pair tile" is 256 keys. The even CTA issues 2-SM MMAs:
 //   S^T [256 keys x 128 rows]  = K [256 x D] . Q^T          A = K: each CTA streams its own
 //                                                            128 keys; B = Q^T: each CTA holds
@@ -46,7 +47,7 @@
 // offset in both, as the pair MMA needs, and both CTAs' copies of a stage count their bytes on
 // one barrier in the even CTA (the 2-CTA form of the tensor copy), which alone waits on it.
 //
-// After a unit's last tile the softmax warps exchange the row sums with the peer, write the
+// After a piece's last tile the softmax warps exchange the row sums with the peer, write the
 // lse, and read O^T out to the output or the split partials; the next unit's copies and S
 // MMAs run meanwhile, and its first PV waits for the read-out (it overwrites O^T).
 //
@@ -95,7 +96,7 @@ struct PairExtra {
 // u mod splits of row-group slot (u / splits) mod (Hkv n_rg) of request u / (splits Hkv n_rg);
 // the units of one (request, row group) form group u / splits.
 struct PairUnit {
-    int32_t b, g, c_split, h0;
+    int32_t b, g, c_split, n_run, h0;
     int32_t L;
     bool len_ok;
     Chunk ch;
@@ -108,9 +109,11 @@ struct PairUnit {
 // each and P - r "large" pairs q units, and within every group the chunks of large pairs get
 // q + 1 tiles for every q of the small pairs' chunks, so every pair streams about U/P units of
 // keys. The large pairs' (P - r) q chunks are spread evenly over the groups, as the first
-// chunks of each group; every chunk keeps its own partial slot, so the split combine is
-// unchanged. (Uniform chunks on long_draft's 512 units over 76 pairs left 20 pairs idle for
-// one unit of the seven.)
+// chunks of each group. (Uniform chunks on long_draft's 512 units over 76 pairs left 20 pairs
+// idle for one unit of the seven.) Either way a pair's consecutive items that are consecutive
+// chunks of one group form a run, which the pair streams as one piece with one epilogue: its
+// partial goes to the slot of the run's first chunk, and the other slots get an lse of -inf,
+// which the split combine skips.
 struct PairPlan {
     int32_t npairs, q, r, groups, large;
     bool balanced;
@@ -170,11 +173,34 @@ __device__ __forceinline__ int32_t pair_item(const AttnParams& p, const PairExtr
     return c + S * lo;
 }
 
-__device__ __forceinline__ PairUnit pair_unit(const AttnParams& p, const PairExtra& x, const PairPlan& pp, int u)
+// The run of the pair's items that starts at its k-th: the first unit, or -1 past the last,
+// and in n the number of items that continue it with the next chunks of the same group. A run
+// is one piece of work: its chunks' keys are one contiguous range, streamed and accumulated
+// in TMEM as one, with one epilogue.
+__device__ __forceinline__ int32_t pair_run(const AttnParams& p, const PairExtra& x, const PairPlan& pp, int32_t pr,
+                                            int32_t k, int32_t& n)
+{
+    n = 0;
+    const int32_t u = pair_item(p, x, pp, pr, k);
+    if (u < 0) return -1;
+    n = 1;
+    while (true) {
+        const int32_t v = pair_item(p, x, pp, pr, k + n);
+        if (v != u + n || v / p.splits != u / p.splits) break;
+        ++n;
+    }
+    return u;
+}
+
+// Unit u with the n - 1 chunks after it in its group (a run): the keys of chunks
+// [u mod splits, u mod splits + n) of the group, the partial slot of the first.
+__device__ __forceinline__ PairUnit pair_unit(const AttnParams& p, const PairExtra& x, const PairPlan& pp, int u,
+                                              int n)
 {
     PairUnit U;
     const int ys = p.Hkv * x.n_rg;
     U.c_split = u % p.splits;
+    U.n_run = n;
     const int y = (u / p.splits) % ys;
     U.b = u / (p.splits * ys);
     U.g = y / x.n_rg;
@@ -187,6 +213,8 @@ __device__ __forceinline__ PairUnit pair_unit(const AttnParams& p, const PairExt
     if (U.len_ok) {
         if (!pp.balanced) {
             U.ch = split_chunk(U.L, p.T, p.window, p.page_size, p.splits, U.c_split);
+            U.ch.ke = split_chunk(U.L, p.T, p.window, p.page_size, p.splits, U.c_split + n - 1).ke;
+            if (U.ch.ke < U.ch.kb) U.ch.ke = U.ch.kb;
         } else {
             // the request's union key range [lo, L), cut at whole pair tiles from the page
             // boundary below lo, in proportion to the chunks' weights (q + 1 for the group's
@@ -205,7 +233,7 @@ __device__ __forceinline__ PairUnit pair_unit(const AttnParams& p, const PairExt
                 return c <= nl ? c * wq1 : nl * wq1 + (int64_t)(c - nl) * wq;
             };
             const int64_t t_b = (2 * ntot * cum(U.c_split) + wt) / (2 * wt);
-            const int64_t t_e = (2 * ntot * cum(U.c_split + 1) + wt) / (2 * wt);
+            const int64_t t_e = (2 * ntot * cum(U.c_split + n) + wt) / (2 * wt);
             int64_t kb = base + t_b * kPairKeys, ke = base + t_e * kPairKeys;
             if (kb < lo) kb = lo;
             if (ke > U.L) ke = U.L;
@@ -482,10 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int seq = 0;
         int last_k = -1;            // sequence number of the last K stage so far (reads Q)
 #pragma unroll 1
-        for (int k_unit = 0; ok; ++k_unit) {
-            const int unit = pair_item(p, x, pp, pair_id, k_unit);
+        for (int k_item = 0, n_run = 0; ok; k_item += n_run) {
+            const int unit = pair_run(p, x, pp, pair_id, k_item, n_run);
             if (unit < 0) break;
-            const PairUnit U = pair_unit(p, x, pp, unit);
+            const PairUnit U = pair_unit(p, x, pp, unit, n_run);
             if (U.ntiles == 0) continue;
             int wbase = 0;
             load_window(U, 0);
@@ -609,10 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++seq;
             };
 #pragma unroll 1
-            for (int k_unit = 0; ok; ++k_unit) {
-                const int unit = pair_item(p, x, pp, pair_id, k_unit);
+            for (int k_item = 0, n_run = 0; ok; k_item += n_run) {
+                const int unit = pair_run(p, x, pp, pair_id, k_item, n_run);
                 if (unit < 0) break;
-                const PairUnit U = pair_unit(p, x, pp, unit);
+                const PairUnit U = pair_unit(p, x, pp, unit, n_run);
                 if (U.ntiles == 0) continue;
                 // V rows past seq_len in the sequence's last, partial page are zeroed before PV in
                 // both CTAs' copies of the stage (the zero probabilities there must not meet
@@ -740,10 +768,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             return group_wait(p_free + t % kPBufs, (uint32_t)((t / kPBufs) & 1));
         };
 #pragma unroll 1
-        for (int k_unit = 0; ok; ++k_unit) {
-            const int unit = pair_item(p, x, pp, pair_id, k_unit);
+        for (int k_item = 0, n_run = 0; ok; k_item += n_run) {
+            const int unit = pair_run(p, x, pp, pair_id, k_item, n_run);
             if (unit < 0) break;
-            const PairUnit U = pair_unit(p, x, pp, unit);
+            const PairUnit U = pair_unit(p, x, pp, unit, n_run);
             if (tid == 0 && leader && !U.len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
             // the unit's rows: column c of S^T / O^T is row c mod 64 of CTA c / 64's Q
             if (tid < kN) {
@@ -993,6 +1021,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (p.lse) p.lse[orow_s[tid]] = lse_v;
                     } else {
                         p.part_lse[part_base + orow_s[tid]] = lse_v;
+                        // the slots of the run's later chunks hold nothing: an lse of -inf, whose
+                        // partial rows the combine does not read
+                        for (int c = 1; c < U.n_run; ++c)
+                            p.part_lse[part_base + (int64_t)c * p.B * p.T * p.Hq + orow_s[tid]] = -INFINITY;
                     }
                 }
             }
