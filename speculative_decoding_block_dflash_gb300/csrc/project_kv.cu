@@ -8,31 +8,38 @@
 //   V[s_t, h, d] = bf16( sum_k hidden[t, k] * W_v[h*D + d, k] )
 // where slot s maps to page s / page_size, position s % page_size.
 //
-// One persistent CTA per SM walks output tiles of 256 tokens x 256 features (of K or of V),
-// the tile index t = m * (2 * n_half) + nt (feature tiles fastest, so that the CTAs running at
-// once share their hidden rows and the whole weight set stays in L2). Warp roles:
-//   warp 0     TMA producer: per 64-wide slice of the hidden dimension, a 256 x 64 box of
-//              hidden and a 256 x 64 box of the weight (both 128-byte swizzled) into a
-//              3-stage ring;
-//   warp 1     MMA issuer: two tcgen05.mma M=128 N=256 K=16 per 16-wide step (token rows
-//              0-127 and 128-255 against the same weight rows), fp32 accumulators in all
-//              512 TMEM columns;
-//   warps 2-9  epilogue: two warps per TMEM lane quarter (one per accumulator), thread =
+// The grid is persistent and made of CTA pairs (clusters of 2 sharing each tcgen05 MMA,
+// cta_group::2), one pair per cluster slot the device holds at once. A pair walks output tiles
+// of 256 tokens x 256 features (of K or of V), the tile index t = m * (2 * n_half) + nt
+// (feature tiles fastest, so that the pairs running at once share their hidden rows and the
+// whole weight set stays in L2). CTA r of a pair owns tokens [128 r, 128 r + 128) of the tile.
+// Per 64-wide slice of the hidden dimension each CTA lands 16 KB of its hidden rows and 16 KB
+// of weight rows (features [128 r, 128 r + 128) of the tile), and the even CTA issues one
+// M=256 N=256 K=16 MMA per 16-wide step, taking the B operand's halves from both CTAs. Each
+// CTA's TMEM receives its 128 token rows x 256 features, in one of two accumulators (256
+// columns each) that alternate between tiles, so the epilogue of a tile runs while the MMAs
+// of the next one do. (Against a single-CTA 256 x 256 tile in one 512-column accumulator, which
+// lands the same bytes per flop: 244 -> 235 us on the 8192-token workload; a 256 x 512 pair
+// tile, which lands a quarter fewer bytes per flop but fills TMEM with one accumulator: 239 us.)
+// Warp roles per CTA:
+//   warp 0     TMA producer: the CTA's two boxes of a stage into a 6-stage ring of 32 KB,
+//              counted on the even CTA's barrier;
+//   warp 1     MMA issuer (even CTA);
+//   warps 2-9  epilogue: two warps per TMEM lane quarter (one per 128-feature half), thread =
 //              token row, 16 columns at a time, bf16 pack and two 16-byte stores into the
 //              token's cache slot.
-// A 256-row tile halves the bytes each SM must land per flop against a 128-row one: the
-// tensor copies into one SM, not the MMAs, bound this kernel.
 //
-// When the tiles leave a partial last round (tiles mod CTAs = rem, 2 * rem <= CTAs) and the
-// caller gives a workspace, the last rem tiles are split along the hidden dimension into two
-// halves that run on 2 * rem CTAs of the last round. The first half to reach its epilogue
-// (an arrival counter) writes its fp32 accumulator to the workspace and raises a flag; the
-// other waits for the flag (bounded), adds the partial to its own accumulator and writes the
-// bf16 rows. Both halves of a tile are in the same round, so the waiter only waits for a
-// CTA that is already writing. A tile whose second half lies
-// wholly past the last token skips that half's MMAs. Rows past the token count and hidden
-// columns past H are zero-filled by the tensor copies. Every wait is bounded
-// (DFLASH_DEVERR_TIMEOUT, the kernel returns).
+// When the tiles leave a partial last round (tiles mod pairs = rem, 2 * rem <= pairs) and the
+// caller gives a workspace, the last rem tiles are split in two along the hidden dimension,
+// the halves running on 2 * rem pairs of the last round. For each CTA rank, the first half to
+// reach its epilogue (an arrival counter) writes its fp32 accumulator rows to the workspace and
+// raises a flag; the other waits for the flag (bounded), adds the partial to its own
+// accumulator and writes the bf16 rows. Both halves of a tile are in the same round, so the
+// waiter only waits for a CTA that is already writing. Rows past the token count, hidden
+// columns past H and feature rows past N are zero-filled by the tensor copies. Every wait is
+// bounded (DFLASH_DEVERR_TIMEOUT, the kernel returns), and both CTAs of a pair meet at a
+// cluster barrier before TMEM is freed.
+#include <algorithm>
 #include <mutex>
 
 #include "tc_ptx.cuh"
@@ -42,25 +49,28 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBM = 256;  // tokens per tile (two 128-row MMA halves)
-constexpr int kBN = 256;  // features per tile
-constexpr int kBK = 64;   // hidden elements per stage (128 bytes: one swizzle row)
-constexpr int kStages = 3;
-constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBM = 256;      // tokens per pair tile (128 per CTA)
+constexpr int kRows = 128;    // tokens per CTA
+constexpr int kBN = 256;      // features per pair tile (the MMA's N; 128 of the weight rows per CTA)
+constexpr int kBK = 64;       // hidden elements per stage (128 bytes: one swizzle row)
+constexpr int kStages = 6;
+constexpr int kABytes = kRows * kBK * 2;        // this CTA's 128 hidden rows
+constexpr int kBBytes = (kBN / 2) * kBK * 2;    // this CTA's half of the weight rows
+constexpr int kStageBytes = kABytes + kBBytes;  // 32 KB
 constexpr int kTmaWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kTmemCols = 2 * kBN;  // accumulator of rows 0-127 in columns [0, 256), rows 128-255 in [256, 512)
+constexpr int kTmemCols = 2 * kBN;  // two accumulators: tile i in columns [256 (i mod 2), +256)
 constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 3;  // full, empty, acc_full, acc_empty, drain
+constexpr int kNumBars = 2 * kStages + 5;  // full, empty, acc_full[2], acc_empty[2], drain
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
 constexpr int kSmemUsed = kMiscOff + 16;
 constexpr int kAlloc = kSmemUsed + 1024;  // the ring is aligned up to 1024 bytes (swizzle atoms)
 static_assert(kAlloc <= 227 * 1024, "shared memory");
-constexpr size_t kProjectSyncBytes = 8192;  // two int32 per split tile, a fixed block
+static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
+constexpr size_t kProjectSyncBytes = 8192;  // two int32 per (split tile, CTA rank), a fixed block
+constexpr unsigned long long kCopyGraceNs = 200000ull;  // after an abort: time for copies in flight to land
 
 struct ProjParams {
     const int32_t* slot_mapping;
@@ -72,8 +82,8 @@ struct ProjParams {
     int32_t tiles;   // ceil(L / kBM) * 2 * n_half
     int32_t full_tiles;  // tiles computed whole; tiles [full_tiles, tiles) are split in two
     int32_t units;       // full_tiles + 2 * (tiles - full_tiles): the persistent loop's work units
-    float* partial;      // [tiles - full_tiles][kBM][kBN] fp32: the first half's accumulator
-    int32_t* sync;       // [tiles - full_tiles][2]: arrivals, partial-ready flag (zero between calls)
+    float* partial;      // [tiles - full_tiles][2 ranks][kRows][kBN] fp32: the first half's accumulator rows
+    int32_t* sync;       // [tiles - full_tiles][2 ranks][2]: arrivals, partial-ready flag (zero between calls)
     int64_t total_slots;
     int64_t sp, ss, sh;
 };
@@ -111,12 +121,15 @@ __device__ __forceinline__ int ld_acquire_gpu(const int32_t* ptr)
     return v;
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1)
+// A pair's 2-D tensor copy into this CTA's shared memory, its bytes counted on the mbarrier at
+// cluster address mbar_cluster (the even CTA's).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t mbar_cluster, int c0,
+                                                 int c1)
 {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster), "r"(c0), "r"(c1)
         : "memory");
 }
 
@@ -150,16 +163,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBarOff);
-    uint64_t* full = bars;                  // [kStages] TMA -> MMA: stage landed
-    uint64_t* empty = bars + kStages;       // [kStages] MMA -> TMA: stage consumed
-    uint64_t* acc_full = bars + 2 * kStages;  // MMA -> epilogue: the accumulators hold a finished tile
-    uint64_t* acc_empty = acc_full + 1;     // epilogue -> MMA: the accumulators have been read out
-    uint64_t* drain = acc_empty + 1;
+    uint64_t* full = bars;                    // [kStages] TMA -> MMA: both CTAs' boxes of the stage landed (even CTA)
+    uint64_t* empty = bars + kStages;         // [kStages] MMA -> TMA: stage consumed (both CTAs)
+    uint64_t* acc_full = bars + 2 * kStages;  // [2] MMA -> epilogue: accumulator b holds a finished tile (both CTAs)
+    uint64_t* acc_empty = acc_full + 2;       // [2] epilogues -> MMA: both CTAs have read accumulator b out (even CTA)
+    uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
     __shared__ int ticket_s;  // arrival order of this CTA's half of a split tile
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank == 0);
+    const int pair_id = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
     const int KB = (p.H + kBK - 1) / kBK;
     const int row_tiles = 2 * p.n_half;
 
@@ -168,29 +185,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, kEpiWarps);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_empty + b, 2 * kEpiWarps);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc2(tmem_slot, kTmemCols);
+        tmem_relinquish2();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kTmaWarp) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA producer (both CTAs)
+        const uint32_t full0 = mapa_shared(smem_u32(full), 0);
         bool ok = true;
         uint32_t issued_par[kStages];
 #pragma unroll
         for (int s = 0; s < kStages; ++s) issued_par[s] = 2;  // 2 = nothing issued
         int seq = 0;
-        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        for (int u = pair_id; u < p.units && ok; u += npairs) {
             const Unit w = unit_of(p, u, KB);
             const int m = w.tile / row_tiles;
             const int nt = w.tile - m * row_tiles;
@@ -200,96 +221,108 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kb = w.kb0; kb < w.kb1; ++kb, ++seq) {
                 const int s = seq % kStages;
                 const uint32_t ph = (uint32_t)(seq / kStages) & 1u;
-                if (lane == 0) ok = ring_wait(empty + s, ph ^ 1u, abort_flag, p.err);
+                // the even CTA's MMA commit frees the slot in both CTAs
+                if (lane == 0) ok = ring_wait_cluster(empty + s, ph ^ 1u, abort_flag, p.err, kTimeoutNs);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 if (lane == 0) {
                     uint8_t* st = ring + s * kStageBytes;
-                    mbar_expect_tx(full + s, kStageBytes);
-                    tma_load_2d(st, &tm_h, full + s, kb * kBK, m * kBM);
-                    tma_load_2d(st + kABytes, tw, full + s, kb * kBK, col0);
+                    // the even CTA's barrier counts both CTAs' bytes of the stage
+                    if (leader) mbar_expect_tx(full + s, 2u * kStageBytes);
+                    const uint32_t fb = full0 + (uint32_t)(s * 8);
+                    tma_load_2d_pair(st, &tm_h, fb, kb * kBK, m * kBM + (int)rank * kRows);
+                    tma_load_2d_pair(st + kABytes, tw, fb, kb * kBK, col0 + (int)rank * (kBN / 2));
                     issued_par[s] = ph;
                 }
                 __syncwarp();
             }
         }
-        // On an abort, no copy of ours may still be landing when the CTA exits.
         if (lane == 0 && !ok) {
-            for (int s = 0; s < kStages; ++s) {
-                if (issued_par[s] > 1) continue;
-                const unsigned long long t_start = globaltimer();
-                while (!mbar_try_wait(full + s, issued_par[s]) && globaltimer() - t_start < kTimeoutNs) {
+            // Copies of ours may still be landing. The even CTA waits for the stages it armed;
+            // both CTAs then give copies in flight a grace period (the odd CTA's copies count on
+            // the even CTA's barriers, which it cannot wait for) before this CTA may leave.
+            if (leader) {
+                for (int s = 0; s < kStages; ++s) {
+                    if (issued_par[s] > 1) continue;
+                    const unsigned long long t_start = globaltimer();
+                    while (!mbar_try_wait_cluster(full + s, issued_par[s]) && globaltimer() - t_start < kTimeoutNs) {
+                    }
                 }
+            }
+            const unsigned long long t_start = globaltimer();
+            while (globaltimer() - t_start < kCopyGraceNs) {
             }
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = make_idesc(kBM / 2, kBN, 0, 0);  // A (hidden) and B (weight) K-major
-        const uint32_t ring_addr = smem_u32(ring);
-        bool ok = true;
-        int seq = 0;
-        int i = 0;
-        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++i) {
-            const Unit w = unit_of(p, u, KB);
-            const int m = w.tile / row_tiles;
-            const bool two = m * kBM + kBM / 2 < p.L;  // the second 128-row half holds tokens
-            // the epilogue has read out the previous tile
-            if (lane == 0) ok = ring_wait(acc_empty, ((uint32_t)i & 1u) ^ 1u, abort_flag, p.err);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            tc_fence_after();
-            for (int kb = w.kb0; kb < w.kb1; ++kb, ++seq) {
-                const int s = seq % kStages;
-                const uint32_t ph = (uint32_t)(seq / kStages) & 1u;
-                if (lane == 0) ok = ring_wait(full + s, ph, abort_flag, p.err);
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (leader) {
+            constexpr uint32_t idesc = make_idesc(2 * kRows, kBN, 0, 0);  // M = 256 over the pair, K-major A and B
+            const uint32_t ring_addr = smem_u32(ring);
+            bool ok = true;
+            int seq = 0;
+            int i = 0;
+            for (int u = pair_id; u < p.units && ok; u += npairs, ++i) {
+                const Unit w = unit_of(p, u, KB);
+                const int ab = i & 1;  // accumulator of this tile
+                const uint32_t acc = tmem + (uint32_t)(ab * kBN);
+                // both CTAs' epilogues have read out the tile two back (accumulator ab's last use)
+                if (lane == 0)
+                    ok = ring_wait_cluster(acc_empty + ab, ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, p.err,
+                                           kTimeoutNs);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t sa = ring_addr + (uint32_t)(s * kStageBytes);
-                    const uint32_t sb = sa + kABytes;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++seq) {
+                    const int s = seq % kStages;
+                    const uint32_t ph = (uint32_t)(seq / kStages) & 1u;
+                    if (lane == 0) ok = ring_wait_cluster(full + s, ph, abort_flag, p.err, kTimeoutNs);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t sa = ring_addr + (uint32_t)(s * kStageBytes);
+                        const uint32_t sb = sa + kABytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        const uint64_t bdesc = sw128_desc(sb + kk * 32, 16, 1024);
-                        const uint32_t acc_flag = (kb > w.kb0 || kk > 0) ? 1u : 0u;
-                        tc_mma(tmem, sw128_desc(sa + kk * 32, 16, 1024), bdesc, idesc, acc_flag);
-                        if (two)
-                            tc_mma(tmem + kBN, sw128_desc(sa + kABytes / 2 + kk * 32, 16, 1024), bdesc, idesc,
-                                   acc_flag);
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            tc_mma2(acc, sw128_desc(sa + kk * 32, 16, 1024), sw128_desc(sb + kk * 32, 16, 1024), idesc,
+                                    (kb > w.kb0 || kk > 0) ? 1u : 0u);
+                        tc_commit2_both(empty + s);
                     }
-                    tc_commit(empty + s);
+                    __syncwarp();
                 }
+                if (!ok) break;
+                if (lane == 0) tc_commit2_both(acc_full + ab);
                 __syncwarp();
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(acc_full);
+            // our MMAs are complete before either CTA frees TMEM or leaves (they read both CTAs' memory)
+            if (lane == 0) {
+                tc_commit2_local(drain);
+                const unsigned long long t_start = globaltimer();
+                while (!mbar_try_wait(drain, 0) && globaltimer() - t_start < kTimeoutNs) {
+                }
+            }
             __syncwarp();
         }
-        // Our MMAs are complete before TMEM is released.
-        if (lane == 0) {
-            tc_commit(drain);
-            const unsigned long long t_start = globaltimer();
-            while (!mbar_try_wait(drain, 0) && globaltimer() - t_start < kTimeoutNs) {
-            }
-        }
-        __syncwarp();
+        // (the odd CTA's MMA warp has no role: the even CTA issues the pair MMAs)
     } else {
         // ------------------------------------------------------------ epilogue (thread = token row)
-        const int quarter = warp & 3;           // the TMEM lane quarter this warp may read
-        const int half = (warp - 2) >> 2;       // 0: rows 0-127 of the tile, 1: rows 128-255
-        const uint32_t acc = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(half * kBN);
+        const int quarter = warp & 3;      // the TMEM lane quarter this warp may read
+        constexpr int kCols = kBN / 2;     // columns per epilogue warp
+        const int half = (warp - 2) >> 2;  // 0: features [0, 128) of the tile, 1: [128, 256)
+        const int lrow = quarter * 32 + lane;  // row within this CTA's 128
+        const uint32_t acc_empty0 = mapa_shared(smem_u32(acc_empty), 0);
         int i = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+        for (int u = pair_id; u < p.units; u += npairs, ++i) {
             const Unit w = unit_of(p, u, KB);
             const int m = w.tile / row_tiles;
             const int nt = w.tile - m * row_tiles;
             const bool is_v = nt >= p.n_half;
-            const int col0 = (is_v ? nt - p.n_half : nt) * kBN;
-            const int ncols = min(kBN, p.N - col0);  // a multiple of 16
-            const bool active = m * kBM + half * (kBM / 2) < p.L;  // this half was computed
-            const int trow = half * (kBM / 2) + quarter * 32 + lane;  // row within the tile
-            const int row = m * kBM + trow;
+            const int col0 = (is_v ? nt - p.n_half : nt) * kBN + half * kCols;  // first feature of this half
+            const int ncols = max(0, min(kCols, p.N - col0));                     // a multiple of 16
+            const int ab = i & 1;
+            const uint32_t acc = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(ab * kBN + half * kCols);
+            const int row = m * kBM + (int)rank * kRows + lrow;
             __nv_bfloat16* dst = nullptr;  // this token's slot, or none
             if (row < p.L) {
                 const int32_t slot = __ldg(p.slot_mapping + row);
@@ -305,19 +338,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             // barrier, leaving the issue slots to the producer and MMA warps); the barrier's OR
             // gives all 8 warps the wait's outcome, so that they leave together.
             bool got = true;
-            if (threadIdx.x == 64) got = ring_wait(acc_full, (uint32_t)i & 1u, abort_flag, p.err);
+            if (threadIdx.x == 64)
+                got = ring_wait_cluster(acc_full + ab, (uint32_t)(i >> 1) & 1u, abort_flag, p.err, kTimeoutNs);
             const bool ok = !named_bar_or_256(!got);
             if (!ok) break;
             tc_fence_after();
-            // a split tile: the first half to arrive publishes its partial, the second adds it
+            // a split tile: per CTA rank, the first half to arrive publishes its partial rows,
+            // the second adds them
             int role = 0;  // 0: whole tile, 1: publish the partial, 2: add the partial and store
             float* part = nullptr;
             if (w.slot >= 0) {
-                int32_t* sync = p.sync + 2 * w.slot;
+                int32_t* sync = p.sync + 2 * (2 * w.slot + (int)rank);
                 if (threadIdx.x == 64) ticket_s = atomicAdd(sync, 1);
                 named_bar_sync_256();  // the 8 epilogue warps
                 role = ticket_s == 0 ? 1 : 2;
-                part = p.partial + (int64_t)w.slot * kBM * kBN + (int64_t)trow * kBN;
+                part = p.partial + ((int64_t)(2 * w.slot + (int)rank) * kRows + lrow) * kBN + half * kCols;
                 if (role == 2) {
                     // wait (bounded) until the first half's partial is visible
                     if (threadIdx.x == 64) {
@@ -329,47 +364,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                     named_bar_sync_256();  // the 8 epilogue warps
                 }
             }
-            if (active) {
-                for (int c = 0; c < ncols; c += 32) {
-                    uint32_t r0[16], r1[16];
-                    tmem_ld16(acc + c, r0);
-                    tmem_ld16(acc + c + 16, r1);  // inside the accumulator even when past ncols
-                    tmem_ld_wait();
-                    reg_fence16(r0);
-                    reg_fence16(r1);
-                    if (role == 1) {
-                        float4* pp = reinterpret_cast<float4*>(part + c);
+            for (int c = 0; c < ncols; c += 32) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(acc + c, r0);
+                tmem_ld16(acc + c + 16, r1);  // inside this half's 128 columns even when past ncols
+                tmem_ld_wait();
+                reg_fence16(r0);
+                reg_fence16(r1);
+                if (role == 1) {
+                    float4* pp = reinterpret_cast<float4*>(part + c);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            pp[v] = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
-                                                __uint_as_float(r0[4 * v + 2]), __uint_as_float(r0[4 * v + 3]));
-                            pp[4 + v] = make_float4(__uint_as_float(r1[4 * v]), __uint_as_float(r1[4 * v + 1]),
-                                                    __uint_as_float(r1[4 * v + 2]), __uint_as_float(r1[4 * v + 3]));
-                        }
-                        continue;
+                    for (int v = 0; v < 4; ++v) {
+                        pp[v] = make_float4(__uint_as_float(r0[4 * v]), __uint_as_float(r0[4 * v + 1]),
+                                            __uint_as_float(r0[4 * v + 2]), __uint_as_float(r0[4 * v + 3]));
+                        pp[4 + v] = make_float4(__uint_as_float(r1[4 * v]), __uint_as_float(r1[4 * v + 1]),
+                                                __uint_as_float(r1[4 * v + 2]), __uint_as_float(r1[4 * v + 3]));
                     }
-                    if (role == 2) {
-                        const float4* pp = reinterpret_cast<const float4*>(part + c);
+                    continue;
+                }
+                if (role == 2) {
+                    const float4* pp = reinterpret_cast<const float4*>(part + c);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const float4 a = __ldcg(pp + v), b = __ldcg(pp + 4 + v);
-                            r0[4 * v] = __float_as_uint(__uint_as_float(r0[4 * v]) + a.x);
-                            r0[4 * v + 1] = __float_as_uint(__uint_as_float(r0[4 * v + 1]) + a.y);
-                            r0[4 * v + 2] = __float_as_uint(__uint_as_float(r0[4 * v + 2]) + a.z);
-                            r0[4 * v + 3] = __float_as_uint(__uint_as_float(r0[4 * v + 3]) + a.w);
-                            r1[4 * v] = __float_as_uint(__uint_as_float(r1[4 * v]) + b.x);
-                            r1[4 * v + 1] = __float_as_uint(__uint_as_float(r1[4 * v + 1]) + b.y);
-                            r1[4 * v + 2] = __float_as_uint(__uint_as_float(r1[4 * v + 2]) + b.z);
-                            r1[4 * v + 3] = __float_as_uint(__uint_as_float(r1[4 * v + 3]) + b.w);
-                        }
+                    for (int v = 0; v < 4; ++v) {
+                        const float4 a = __ldcg(pp + v), b = __ldcg(pp + 4 + v);
+                        r0[4 * v] = __float_as_uint(__uint_as_float(r0[4 * v]) + a.x);
+                        r0[4 * v + 1] = __float_as_uint(__uint_as_float(r0[4 * v + 1]) + a.y);
+                        r0[4 * v + 2] = __float_as_uint(__uint_as_float(r0[4 * v + 2]) + a.z);
+                        r0[4 * v + 3] = __float_as_uint(__uint_as_float(r0[4 * v + 3]) + a.w);
+                        r1[4 * v] = __float_as_uint(__uint_as_float(r1[4 * v]) + b.x);
+                        r1[4 * v + 1] = __float_as_uint(__uint_as_float(r1[4 * v + 1]) + b.y);
+                        r1[4 * v + 2] = __float_as_uint(__uint_as_float(r1[4 * v + 2]) + b.z);
+                        r1[4 * v + 3] = __float_as_uint(__uint_as_float(r1[4 * v + 3]) + b.w);
                     }
-                    if (dst) {
-                        const int f0 = col0 + c;  // feature of column c: head f / D, dim f % D
-                        store16(dst + (int64_t)(f0 / p.D) * p.sh + f0 % p.D, r0);
-                        if (c + 16 < ncols) {
-                            const int f1 = f0 + 16;
-                            store16(dst + (int64_t)(f1 / p.D) * p.sh + f1 % p.D, r1);
-                        }
+                }
+                if (dst) {
+                    const int f0 = col0 + c;  // feature of column c: head f / D, dim f % D
+                    store16(dst + (int64_t)(f0 / p.D) * p.sh + f0 % p.D, r0);
+                    if (c + 16 < ncols) {
+                        const int f1 = f0 + 16;
+                        store16(dst + (int64_t)(f1 / p.D) * p.sh + f1 % p.D, r1);
                     }
                 }
             }
@@ -377,26 +410,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // publish: every thread's partial rows are written before the flag is raised
                 __threadfence();
                 named_bar_sync_256();  // the 8 epilogue warps
-                if (threadIdx.x == 64) atomicExch(p.sync + 2 * w.slot + 1, 1);
+                if (threadIdx.x == 64) atomicExch(p.sync + 2 * (2 * w.slot + (int)rank) + 1, 1);
             } else if (role == 2) {
                 named_bar_sync_256();  // the 8 epilogue warps
                 if (threadIdx.x == 64) {  // both halves are done with this slot: reset it
-                    p.sync[2 * w.slot] = 0;
-                    p.sync[2 * w.slot + 1] = 0;
+                    p.sync[2 * (2 * w.slot + (int)rank)] = 0;
+                    p.sync[2 * (2 * w.slot + (int)rank) + 1] = 0;
                 }
             }
+            // this CTA's read-out is done: one arrival per warp on the even CTA's barrier
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
+            if (lane == 0) mbar_arrive_cluster(acc_empty0 + (uint32_t)(ab * 8));
         }
     }
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // no CTA leaves while the pair MMAs or the peer may still touch its memory
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc2(tmem, kTmemCols);
     }
 }
 
@@ -433,18 +468,54 @@ bool encode_2d(EncodeTiledFn enc, CUtensorMap* map, const void* base, int64_t co
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Pairs of this kernel the current device holds at once (cached per device).
+cudaError_t resident_pairs(int* pairs)
+{
+    static int cached[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cached[dev] == 0) {
+        e = cudaFuncSetAttribute(project_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kAlloc;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, project_kv_kernel, &cfg);
+        if (e != cudaSuccess) return e;
+        cached[dev] = n > 0 ? n : 1;
+    }
+    *pairs = cached[dev];
+    return cudaSuccess;
+}
+
 }  // namespace
 
 int32_t project_kv_grid(int32_t L, int32_t N)
 {
     const int64_t tiles = (int64_t)((L + kBM - 1) / kBM) * 2 * ((N + kBN - 1) / kBN);
-    return (int32_t)std::min<int64_t>(tiles, device_sm_count());
+    int pairs = 0;
+    if (resident_pairs(&pairs) != cudaSuccess) return 0;
+    return (int32_t)(2 * std::min<int64_t>(tiles, pairs));
 }
 
 size_t project_kv_workspace_bytes()
 {
-    // the sync block, then one fp32 tile per split tile (at most half the CTAs' count)
-    return kProjectSyncBytes + (size_t)(device_sm_count() / 2) * kBM * kBN * sizeof(float);
+    // the sync block, then the fp32 rows of one split tile per two pairs (a split tile's halves
+    // take two pairs of the last round)
+    return kProjectSyncBytes + (size_t)(device_sm_count() / 4) * kBM * kBN * sizeof(float);
 }
 
 cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t hidden_stride, const void* w_k,
@@ -457,8 +528,8 @@ cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t 
     if (!enc) return cudaErrorNotSupported;
     const int32_t N = Hkv * D;
     CUtensorMap th, twk, twv;
-    if (!encode_2d(enc, &th, hidden, H, L, hidden_stride, kBM) || !encode_2d(enc, &twk, w_k, H, N, H, kBN) ||
-        !encode_2d(enc, &twv, w_v, H, N, H, kBN))
+    if (!encode_2d(enc, &th, hidden, H, L, hidden_stride, kRows) || !encode_2d(enc, &twk, w_k, H, N, H, 128) ||
+        !encode_2d(enc, &twv, w_v, H, N, H, 128))
         return cudaErrorInvalidValue;
     ProjParams p;
     p.slot_mapping = slot_mapping;
@@ -476,21 +547,34 @@ cudaError_t launch_project_kv(const void* hidden, int32_t L, int32_t H, int64_t 
     p.sp = sp;
     p.ss = ss;
     p.sh = sh;
-    const int grid = project_kv_grid(L, N);
+    int pairs = 0;
+    cudaError_t e = resident_pairs(&pairs);
+    if (e != cudaSuccess) return e;
+    pairs = std::min(pairs, p.tiles);
     // split the tiles of a partial last round in two along the hidden dimension when the
     // halves fit in that round and the workspace holds their partials
-    const int rem = p.tiles % grid;
+    const int rem = p.tiles % pairs;
     const int KB = (H + kBK - 1) / kBK;
-    const bool split = workspace && rem > 0 && 2 * rem <= grid && KB >= 2 &&
+    const bool split = workspace && rem > 0 && 2 * rem <= pairs && KB >= 2 &&
+                       2 * rem * 2 * 2 * (int64_t)sizeof(int32_t) <= (int64_t)kProjectSyncBytes &&
                        workspace_bytes >= kProjectSyncBytes + (size_t)rem * kBM * kBN * sizeof(float);
     p.full_tiles = split ? p.tiles - rem : p.tiles;
     p.units = split ? p.tiles + rem : p.tiles;
     p.sync = static_cast<int32_t*>(workspace);
     p.partial = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) + kProjectSyncBytes) : nullptr;
-    cudaError_t e = cudaFuncSetAttribute(project_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
-    if (e != cudaSuccess) return e;
-    project_kv_kernel<<<grid, kThreads, kAlloc, stream>>>(th, twk, twv, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * pairs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, project_kv_kernel, th, twk, twv, p);
 }
 
 }  // namespace dflash

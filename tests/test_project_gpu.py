@@ -96,8 +96,9 @@ def test_matches_oracle(L, H, Hkv, D, page_size):
 
 
 def test_strided_hidden_rows_and_many_tiles():
-    # rows of a wider buffer; more tiles than SMs so that CTAs loop over tiles
-    L, H, Hkv, D, P = 3000, 256, 4, 256, 16
+    # rows of a wider buffer; more tiles than CTA pairs (24 x 8 = 192 tiles of 256 x 256), so
+    # that pairs loop over tiles
+    L, H, Hkv, D, P = 6000, 256, 4, 256, 16
     num_pages = L // P + 8
     hidden, w_k, w_v, k_cache, v_cache = _inputs(L, H, Hkv, D, P, num_pages, seed=3, stride=H + 64)
     assert hidden.stride(0) == H + 64
@@ -168,8 +169,8 @@ def test_full_size_prefill_sampled_rows():
 
 @pytest.mark.parametrize("split", [True, False])
 def test_split_last_round_matches_oracle(split):
-    # 5000 tokens into 4 x 512 features: 20 x 16 = 320 tiles of 256 x 256 on 152 SMs leave 16
-    # for a third round, which the split runs as 32 halves along the hidden dimension
+    # 5000 tokens into 4 x 512 features: 20 x 16 = 320 tiles of 256 x 256 on 76 CTA pairs leave
+    # 16 for a fifth round, which the split runs as 32 halves along the hidden dimension
     L, H, Hkv, D, P = 5000, 512, 4, 512, 16
     num_pages = L // P + 8
     hidden, w_k, w_v, k_cache, v_cache = _inputs(L, H, Hkv, D, P, num_pages, seed=31)
