@@ -507,6 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < S; ++s) issued_parity[s] = 2;  // 2 = nothing outstanding
         const int box = Psz * 128;  // bytes of one page x 64 dims
+        // K/V pages are read once: they leave L2 first, ahead of the split partials, which the
+        // combine reads back after the kernel
+        const uint64_t kv_policy = l2_policy_evict_first();
         int seq = 0;
         int last_k = -1;            // sequence number of the last K stage so far (reads Q)
 #pragma unroll 1
@@ -568,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (is_k) {
 #pragma unroll
                             for (int pg = 0; pg < 8; ++pg)
-                                if (pg < npg) tma_load_4d_pair(dst + pg * box, &tm_k, fb, sq * 64, U.g, 0, ids[pg]);
+                                if (pg < npg)
+                                    tma_load_4d_pair_hint(dst + pg * box, &tm_k, fb, sq * 64, U.g, 0, ids[pg], kv_policy);
                         } else {
                             const int c = sq % VC2;
                             const int d0 = c * 256 + (int)rank * 128;
@@ -577,8 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 if (pg < npg)
 #pragma unroll
                                     for (int m = 0; m < 2; ++m)
-                                        tma_load_4d_pair(dst + m * 8192 + pg * box, &tm_v, fb, d0 + m * 64, U.g, 0,
-                                                         ids[pg]);
+                                        tma_load_4d_pair_hint(dst + m * 8192 + pg * box, &tm_v, fb, d0 + m * 64, U.g,
+                                                              0, ids[pg], kv_policy);
                         }
                         issued_parity[slot] = ph;
                     }

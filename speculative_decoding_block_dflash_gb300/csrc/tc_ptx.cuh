@@ -498,6 +498,26 @@ __device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// An L2 cache policy that makes the lines a load brings in the first to be evicted: for data
+// streamed once (K/V pages), so that it does not push out data that is read again later.
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_4d_pair with an L2 cache policy for the lines it reads.
+__device__ __forceinline__ void tma_load_4d_pair_hint(void* dst, const CUtensorMap* map, uint32_t mbar_cluster, int c0,
+                                                      int c1, int c2, int c3, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(policy)
+        : "memory");
+}
+
 // Generic stores into the peer CTA's shared memory (cluster addresses from mapa_shared).
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint4 v)
 {
