@@ -427,6 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < S; ++s) issued_parity[s] = 2;  // 2 = nothing outstanding
         if (ntiles > 0) {
             const int box = Psz * 128;  // bytes of one page x 64 dims
+            // K/V pages are read once: they leave L2 first, ahead of the split partials
+            const uint64_t kv_policy = l2_policy_evict_first();
             int seq = 0;                // index of the stage in the whole sequence; this warp fills seq = pw (mod kNumProducers)
             for (int k = 0; k < 2 * ntiles && ok; ++k) {
                 bool is_k;
@@ -474,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int pg = 0; pg < 8; ++pg)
                                     if (pg < pages_per_tile)
-                                        tma_load_4d(dst + pg * box, &tm_k, fb, sq * 64, g, 0, ids[pg]);
+                                        tma_load_4d_hint(dst + pg * box, &tm_k, fb, sq * 64, g, 0, ids[pg], kv_policy);
                             } else {
                                 const int h = sq / VC, c = sq % VC;
                                 const int ppg = 64 / Psz;  // pages per 64-key half
@@ -487,8 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (pg < ppg)
 #pragma unroll
                                         for (int m = 0; m < 2; ++m)
-                                            tma_load_4d(dst + m * 8192 + pg * box, &tm_v, fb, c * 128 + m * 64,
-                                                        g, 0, ids[pg]);
+                                            tma_load_4d_hint(dst + m * 8192 + pg * box, &tm_v, fb, c * 128 + m * 64,
+                                                             g, 0, ids[pg], kv_policy);
                             }
                             if (sl.extra)
                                 issued_extra |= 1u << sl.idx;
