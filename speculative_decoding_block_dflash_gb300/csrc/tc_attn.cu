@@ -215,10 +215,15 @@ __device__ __forceinline__ RingSlot ring_slot(int seq, int S, int E)
     return r;
 }
 
-// Length-balanced plan: the splits chunk slots of a row group are dealt to the B requests in
-// proportion to their key spans (every request gets at least one): request b gets
-// 1 + e(b+1) - e(b) slots with e(k) = round((splits - B) * span(0..k) / span(all)). Slot
-// `slot` is chunk c of n of request b, whose chunks start at slot `first`.
+// Length-balanced plan: the splits chunk slots of a row group are dealt to the B requests so
+// that the longest chunk is as short as it can be. With t_b the 128-key tiles of request b's
+// key span, C is the least tile count for which every request cut into ceil(t_b / C) chunks
+// fits the slots; the spare slots go one each to requests 0, 1, ... in turn. Request b then
+// has n_b chunks (split_chunk of n_b, none longer than C tiles), and slot `slot` is chunk c of
+// n of request b, whose chunks start at slot `first`. (Slots dealt in proportion to the spans,
+// rounded, left batch_sweep_b8's longest chunk at 33 tiles against 31 here, for a mean of 27.)
+// Every warp computes it alike: its lanes take the requests in turn, and with at most 32
+// requests the lanes test 32 candidate bounds at once, so that the common case costs one pass.
 struct ReqChunk {
     int32_t b, c, n, first;
 };
@@ -237,22 +242,110 @@ __device__ inline int64_t key_span(const AttnParams& p, int32_t b)
     return n > 0 ? n : 1;
 }
 
+// ceil(a / c) for 0 <= a < 2^24, c >= 1, through a float reciprocal and a one-step fix-up
+__device__ __forceinline__ int32_t ceil_div_small(int32_t a, int32_t c)
+{
+    const int32_t num = a + c - 1;
+    int32_t q = __float2int_rz(__fdividef((float)num, (float)c));
+    if (q * c > num)
+        --q;
+    else if ((q + 1) * c <= num)
+        ++q;
+    return q;
+}
+
 __device__ inline ReqChunk balanced_chunk(const AttnParams& p, int32_t slot)
 {
-    int64_t total = 0;
-    for (int32_t b = 0; b < p.B; ++b) total += key_span(p, b);
-    const int64_t extra = p.splits - p.B;
-    int64_t pref = 0;
-    int32_t first = 0, e0 = 0;
-    for (int32_t b = 0; b < p.B; ++b) {
-        pref += key_span(p, b);
-        const int32_t e1 = (int32_t)((2 * extra * pref + total) / (2 * total));
-        const int32_t n = 1 + e1 - e0;
-        if (slot < first + n) return ReqChunk{b, slot - first, n, first};
-        first += n;
-        e0 = e1;
+    // requests b = lane + 32 k (the plan has B <= splits <= DFLASH_MAX_SPLITS of them); their
+    // tile counts stay in registers
+    constexpr int kPerLane = (DFLASH_MAX_SPLITS + 31) / 32;
+    const int lane = threadIdx.x & 31;
+    int32_t tl[kPerLane];
+    int32_t tmax = 1, ttot = 0;
+    const int kUsed = (p.B + 31) / 32;  // groups of 32 requests that exist
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) {
+        const int32_t b = lane + 32 * k;
+        tl[k] = (k < kUsed && b < p.B) ? (int32_t)((key_span(p, b) + kTileKeys - 1) / kTileKeys) : 0;
+        tmax = max(tmax, tl[k]);
+        ttot += tl[k];
     }
-    return ReqChunk{p.B - 1, 0, 1, first};
+    tmax = __reduce_max_sync(0xffffffffu, tmax);
+    ttot = __reduce_add_sync(0xffffffffu, ttot);
+    // slots needed when no chunk exceeds C tiles
+    auto slots_for = [&](int32_t C) -> int32_t {
+        int32_t n = 0;
+#pragma unroll
+        for (int k = 0; k < kPerLane; ++k)
+            if (k < kUsed) n += tl[k] > 0 ? ceil_div_small(tl[k], C) : 0;
+        return __reduce_add_sync(0xffffffffu, n);
+    };
+    // the least C that fits. Lane j tests lo + j when there are at most 32 requests (the answer
+    // is usually within a few tiles of the mean); past that, or with more requests, gallop up
+    // from the mean, then bisect.
+    int32_t lo = max(1, (ttot + p.splits - 1) / p.splits);  // a C below lo cannot fit
+    int32_t C = lo;
+    int32_t used = -1;  // slots C takes, once known
+    if (kUsed == 1) {
+        const int32_t cj = lo + lane;
+        int32_t need = 0;
+        for (int32_t r = 0; r < p.B; ++r) need += ceil_div_small(__shfl_sync(0xffffffffu, tl[0], r), cj);
+        const uint32_t fits = __ballot_sync(0xffffffffu, need <= p.splits);
+        if (fits) {
+            C = lo + __ffs(fits) - 1;
+            used = __shfl_sync(0xffffffffu, need, __ffs(fits) - 1);
+        } else {
+            lo += 32;
+            C = lo;
+        }
+    }
+    if (used < 0 && slots_for(C) > p.splits) {
+        int32_t step = 1, hi = tmax;  // C = tmax always fits: B <= splits
+        for (;;) {
+            const int32_t c2 = min(tmax, lo + step);
+            if (slots_for(c2) <= p.splits) {
+                hi = c2;
+                break;
+            }
+            lo = c2 + 1;
+            step <<= 1;
+            if (c2 == tmax) break;  // not reached
+        }
+        while (lo < hi) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (slots_for(mid) <= p.splits)
+                hi = mid;
+            else
+                lo = mid + 1;
+        }
+        C = hi;
+    }
+    if (used < 0) used = slots_for(C);
+    const int32_t left = p.splits - used;
+    const int32_t every = left / p.B, some = left % p.B;
+    // the request whose chunks hold `slot`: an inclusive scan of n_b over the lanes, 32 at a time
+    int32_t base = 0;
+#pragma unroll
+    for (int k = 0; k < kPerLane; ++k) {
+        if (k >= kUsed) break;
+        const int32_t b = lane + 32 * k;
+        const int32_t n = b < p.B ? ceil_div_small(tl[k], C) + every + (b < some ? 1 : 0) : 0;
+        int32_t incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        const uint32_t hit = __ballot_sync(0xffffffffu, b < p.B && slot < base + incl);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            const int32_t nb = __shfl_sync(0xffffffffu, n, src);
+            const int32_t first = base + __shfl_sync(0xffffffffu, incl, src) - nb;
+            return ReqChunk{32 * k + src, slot - first, nb, first};
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return ReqChunk{p.B - 1, 0, 1, base};  // not reached: the n_b add up to the slots
 }
 
 template <int D, int N>
