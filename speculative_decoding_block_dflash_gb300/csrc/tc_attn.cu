@@ -254,42 +254,45 @@ __device__ __forceinline__ int32_t ceil_div_small(int32_t a, int32_t c)
     return q;
 }
 
+// Slots the requests need when no chunk exceeds C tiles (t_lane: lane's request's tiles), summed
+// over the warp. Out of line: it serves the rare search past 32 candidate bounds.
+__device__ __noinline__ int32_t balanced_slots_for(const AttnParams& p, int32_t t_lane, int32_t C)
+{
+    const int lane = threadIdx.x & 31;
+    int32_t n = ceil_div_small(t_lane, C);
+#pragma unroll 1
+    for (int32_t b = lane + 32; b < p.B; b += 32) n += ceil_div_small((int32_t)((key_span(p, b) + kTileKeys - 1) / kTileKeys), C);
+    return __reduce_add_sync(0xffffffffu, n);
+}
+
 __device__ inline ReqChunk balanced_chunk(const AttnParams& p, int32_t slot)
 {
-    // requests b = lane + 32 k (the plan has B <= splits <= DFLASH_MAX_SPLITS of them); their
-    // tile counts stay in registers
-    constexpr int kPerLane = (DFLASH_MAX_SPLITS + 31) / 32;
+    // requests b = lane + 32 k; loops stay rolled (this runs once per CTA, and unrolled it added
+    // a quarter to the kernel's code)
     const int lane = threadIdx.x & 31;
-    int32_t tl[kPerLane];
-    int32_t tmax = 1, ttot = 0;
-    const int kUsed = (p.B + 31) / 32;  // groups of 32 requests that exist
-#pragma unroll
-    for (int k = 0; k < kPerLane; ++k) {
-        const int32_t b = lane + 32 * k;
-        tl[k] = (k < kUsed && b < p.B) ? (int32_t)((key_span(p, b) + kTileKeys - 1) / kTileKeys) : 0;
-        tmax = max(tmax, tl[k]);
-        ttot += tl[k];
+    auto tiles_of = [&](int32_t b) -> int32_t { return (int32_t)((key_span(p, b) + kTileKeys - 1) / kTileKeys); };
+    const int32_t t_lane = lane < p.B ? tiles_of(lane) : 0;  // all of them when B <= 32
+    int32_t tmax = max(1, t_lane), ttot = t_lane;
+#pragma unroll 1
+    for (int32_t b = lane + 32; b < p.B; b += 32) {
+        const int32_t t = tiles_of(b);
+        tmax = max(tmax, t);
+        ttot += t;
     }
     tmax = __reduce_max_sync(0xffffffffu, tmax);
     ttot = __reduce_add_sync(0xffffffffu, ttot);
-    // slots needed when no chunk exceeds C tiles
-    auto slots_for = [&](int32_t C) -> int32_t {
-        int32_t n = 0;
-#pragma unroll
-        for (int k = 0; k < kPerLane; ++k)
-            if (k < kUsed) n += tl[k] > 0 ? ceil_div_small(tl[k], C) : 0;
-        return __reduce_add_sync(0xffffffffu, n);
-    };
+    auto slots_for = [&](int32_t C) -> int32_t { return balanced_slots_for(p, t_lane, C); };
     // the least C that fits. Lane j tests lo + j when there are at most 32 requests (the answer
     // is usually within a few tiles of the mean); past that, or with more requests, gallop up
     // from the mean, then bisect.
     int32_t lo = max(1, (ttot + p.splits - 1) / p.splits);  // a C below lo cannot fit
     int32_t C = lo;
     int32_t used = -1;  // slots C takes, once known
-    if (kUsed == 1) {
+    if (p.B <= 32) {
         const int32_t cj = lo + lane;
         int32_t need = 0;
-        for (int32_t r = 0; r < p.B; ++r) need += ceil_div_small(__shfl_sync(0xffffffffu, tl[0], r), cj);
+#pragma unroll 1
+        for (int32_t r = 0; r < p.B; ++r) need += ceil_div_small(__shfl_sync(0xffffffffu, t_lane, r), cj);
         const uint32_t fits = __ballot_sync(0xffffffffu, need <= p.splits);
         if (fits) {
             C = lo + __ffs(fits) - 1;
@@ -301,6 +304,7 @@ __device__ inline ReqChunk balanced_chunk(const AttnParams& p, int32_t slot)
     }
     if (used < 0 && slots_for(C) > p.splits) {
         int32_t step = 1, hi = tmax;  // C = tmax always fits: B <= splits
+#pragma unroll 1
         for (;;) {
             const int32_t c2 = min(tmax, lo + step);
             if (slots_for(c2) <= p.splits) {
@@ -311,6 +315,7 @@ __device__ inline ReqChunk balanced_chunk(const AttnParams& p, int32_t slot)
             step <<= 1;
             if (c2 == tmax) break;  // not reached
         }
+#pragma unroll 1
         while (lo < hi) {
             const int32_t mid = (lo + hi) >> 1;
             if (slots_for(mid) <= p.splits)
@@ -325,11 +330,11 @@ __device__ inline ReqChunk balanced_chunk(const AttnParams& p, int32_t slot)
     const int32_t every = left / p.B, some = left % p.B;
     // the request whose chunks hold `slot`: an inclusive scan of n_b over the lanes, 32 at a time
     int32_t base = 0;
-#pragma unroll
-    for (int k = 0; k < kPerLane; ++k) {
-        if (k >= kUsed) break;
-        const int32_t b = lane + 32 * k;
-        const int32_t n = b < p.B ? ceil_div_small(tl[k], C) + every + (b < some ? 1 : 0) : 0;
+#pragma unroll 1
+    for (int32_t b0 = 0; b0 < p.B; b0 += 32) {
+        const int32_t b = b0 + lane;
+        const int32_t t = b0 == 0 ? t_lane : (b < p.B ? tiles_of(b) : 0);
+        const int32_t n = b < p.B ? ceil_div_small(t, C) + every + (b < some ? 1 : 0) : 0;
         int32_t incl = n;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -341,7 +346,7 @@ __device__ inline ReqChunk balanced_chunk(const AttnParams& p, int32_t slot)
             const int src = __ffs(hit) - 1;
             const int32_t nb = __shfl_sync(0xffffffffu, n, src);
             const int32_t first = base + __shfl_sync(0xffffffffu, incl, src) - nb;
-            return ReqChunk{32 * k + src, slot - first, nb, first};
+            return ReqChunk{b0 + src, slot - first, nb, first};
         }
         base += __shfl_sync(0xffffffffu, incl, 31);
     }
