@@ -459,6 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         if (!len_ok) raise_error(p.err, DFLASH_DEVERR_SEQ_LEN);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        // Q's copies go out now, counted on ring stage 0's barrier (whose producer arms it with
+        // Q's bytes as well), so that Q lands while the producers still read the page table
+        if (ntiles > 0)
+            for (int kc = 0; kc < KC; ++kc) tma_load_3d(q_s + kc * N * 128, &tm_q, full, kc * 64, h0, b * T);
     }
     if (warp >= kProducerWarp && warp < kProducerWarp + kNumProducers) {
         if (ntiles > 0) load_window(0);
@@ -553,15 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (lane == 0) {
                             uint8_t* dst = sl.extra ? p_s + sl.idx * Lay::kPBytes : ring + sl.idx * kStageBytes;
-                            // The Q tile rides on the first stage's barrier: the MMA warp's first
-                            // wait covers it. (A separate barrier completed by the tensor-copy unit
-                            // and waited on ahead of the ring made every later K/V copy of the CTA
-                            // land about twice as late.)
+                            // The Q tile rides on the first stage's barrier (thread 0 issued its
+                            // copies at set-up): the MMA warp's first wait covers it. (A separate
+                            // barrier completed by the tensor-copy unit and waited on ahead of the
+                            // ring made every later K/V copy of the CTA land about twice as late.)
                             const bool with_q = (seq == 0);
                             mbar_expect_tx(fb, kStageBytes + (with_q ? (uint32_t)(R * 128 * KC) : 0u));
-                            if (with_q)
-                                for (int kc = 0; kc < KC; ++kc)
-                                    tma_load_3d(q_s + kc * N * 128, &tm_q, fb, kc * 64, h0, b * T);
                             // The stage's page ids go to registers before its copies are issued:
                             // each copy instruction is also a compiler memory barrier, so reading
                             // an id between two copies made every box wait for a shared-memory
