@@ -92,9 +92,11 @@ struct PairExtra {
     int32_t units;  // (request, KV head, row group, chunk) units: splits * Hkv * n_rg * B
 };
 
-// One unit of work of a CTA pair: a (request, KV head, row group, key chunk). Unit u is chunk
-// u mod splits of row-group slot (u / splits) mod (Hkv n_rg) of request u / (splits Hkv n_rg);
-// the units of one (request, row group) form group u / splits.
+// Unit u of the work is chunk u mod splits of row-group slot (u / splits) mod (Hkv n_rg) of
+// request u / (splits Hkv n_rg); the units of one (request, row group) form group u / splits.
+// What a pair streams at a time, called a unit in the roles' loops below, is a run of n_run
+// consecutive units of one group (usually one): its chunks' keys as one range, with one
+// epilogue and the partial slot of its first chunk.
 struct PairUnit {
     int32_t b, g, c_split, n_run, h0;
     int32_t L;
